@@ -1,0 +1,237 @@
+/*
+ * psgd.h -- C ABI of the GB300-native PowerSGD communication-hook step.
+ *
+ * One process, one GPU.  A data-parallel job of W workers is simulated by W
+ * replica gradient buckets resident in the same HBM; the "allreduce" of the
+ * pages is a mean over those W buckets, folded into the kernels that read
+ * them.  Every step of the method runs in CUDA kernels of this library; the
+ * host side only plans, allocates (at create time) and enqueues.
+ *
+ * Sources (web pages; the operations are restated here, not copied):
+ *   [DDP]  "DDP Communication Hooks" (PyTorch 1.11 documentation):
+ *          "PowerSGD State" (PowerSGDState and its items 1-4),
+ *          "PowerSGD Hooks" (powerSGD_hook steps 1-3.7, the vanilla-allreduce
+ *          note, the error-feedback memory warning),
+ *          "Default Communication Hooks" (allreduce_hook: the mean).
+ *   [DDP2] "DDP Communication Hooks" (spec-zone.ru translation of a later
+ *          version): "PowerSGD State" item 5, batch_tensors_with_same_shape.
+ *   [AMP]  "Automatic Mixed Precision package - torch.cuda.amp",
+ *          GradScaler: unscale, inf/NaN check, skipped step.
+ *
+ * Conventions for every call:
+ *   - Return value: PSGD_OK (0) or a positive informational code on success,
+ *     a negative PSGD_E* code on failure; psgd_last_error() then holds a
+ *     message (thread-local, valid until the next failing call on the thread).
+ *   - "device pointer" = CUDA global memory on the state's device; "host
+ *     pointer" = ordinary (pageable or pinned) CPU memory.  The caller owns
+ *     every pointer it passes; the library never frees or retains them past
+ *     the call (psgd_step: past the enqueued work).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  psgd_step enqueues only and never synchronises.
+ *   - Elements of a bucket are in bucket order: tensor 0 first, each tensor
+ *     row-major in its own shape, with no padding between tensors.
+ */
+#ifndef PSGD_H
+#define PSGD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct psgd_state psgd_state; /* opaque, library-owned */
+
+typedef enum { PSGD_F32 = 0, PSGD_F16 = 1 } psgd_dtype;
+
+#define PSGD_OK 0
+#define PSGD_SKIPPED_NONFINITE 1 /* [AMP] inf/NaN seen: step skipped, state kept   */
+#define PSGD_EINVAL (-1)         /* bad argument                                   */
+#define PSGD_ENOMEM (-2)         /* device or host allocation failed               */
+#define PSGD_ECUDA (-3)          /* a CUDA call failed                             */
+#define PSGD_ETIMEOUT (-4)       /* a bounded device-side wait gave up             */
+
+#define PSGD_MAX_RANK 32  /* largest matrix_approximation_rank ([DDP] item 1 names up to 32) */
+#define PSGD_MAX_WORLD 64 /* largest number of simulated replicas W              */
+
+/*
+ * psgd_plan -- host-only planner query (no GPU needed).
+ *
+ * [DDP] powerSGD_hook step 1: views the flat bucket as per-parameter tensors
+ * and splits them into a compressed group and an uncompressed group (every
+ * tensor of fewer than 2 dimensions is uncompressed).  A tensor of >= 2 dims
+ * is viewed as (shape[0], prod(shape[1:])) and compressed iff
+ *   (rows + cols) * matrix_approximation_rank * min_compression_rate < rows * cols
+ * ([DDP] "PowerSGD State" item 3; strict, evaluated in double precision).
+ *
+ *   dims, ndims, n_tensors : shapes, concatenated: tensor t has ndims[t]
+ *                            entries of dims starting after the previous ones.
+ *   compressed[n_tensors]  : out, 1 if the tensor is compressed.
+ *   ranks[n_tensors]       : out, min(rank, rows, cols) if compressed, else 0.
+ *   rows[n_tensors], cols[n_tensors] : out, the 2-D view (0,0 for < 2 dims).
+ *   Any of the out arrays may be NULL.
+ * Errors: PSGD_EINVAL for a negative dimension, n_tensors < 0 or rank outside
+ * [1, PSGD_MAX_RANK].
+ */
+int psgd_plan(const int64_t* dims, const int32_t* ndims, int32_t n_tensors,
+              int32_t matrix_approximation_rank, double min_compression_rate,
+              int32_t* compressed, int32_t* ranks, int64_t* rows, int64_t* cols);
+
+/*
+ * psgd_state_create -- [DDP] PowerSGDState(...) for one bucket layout.
+ *
+ * Hyper-parameters keep the pages' names and meaning ([DDP] items 1-4,
+ * [DDP2] item 5).  world_size = W simulated replicas.  grad_dtype is the type
+ * of the replica buckets passed to psgd_step (F16: GradScaler-scaled halves).
+ * Allocates on `device` everything a step needs: the per-replica error
+ * feedback store, P/Q memory and all scratch; psgd_step allocates nothing.
+ * The error store is kept twice (the current and the next step) so that a
+ * skipped step ([AMP]) leaves the state bit-identical.
+ * random_seed seeds the counter-based generator (Philox4x32-10) that draws
+ * the initial standard-normal Q when none was injected with psgd_set_q.
+ * Errors: PSGD_EINVAL (rank outside [1,32], world_size outside [1,64],
+ * negative dims, start_powerSGD_iter < 0, min_compression_rate < 0 or NaN,
+ * epsilon < 0), PSGD_ENOMEM, PSGD_ECUDA.  *out is NULL on failure.
+ */
+int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tensors,
+                      int32_t world_size, int32_t matrix_approximation_rank,
+                      int64_t start_powerSGD_iter, double min_compression_rate,
+                      int32_t use_error_feedback, int32_t warm_start,
+                      float orthogonalization_epsilon, uint64_t random_seed,
+                      int32_t batch_tensors_with_same_shape, psgd_dtype grad_dtype,
+                      int32_t device, psgd_state** out);
+
+/* Frees every device and host allocation of the state.  NULL is a no-op. */
+void psgd_state_destroy(psgd_state* s);
+
+/*
+ * psgd_step -- one call of [DDP] powerSGD_hook on the W replicas.
+ *
+ *   grads[W] : host array of W device pointers; grads[w] is replica w's flat
+ *              bucket of N elements of grad_dtype.  Read only.
+ *   out      : device pointer, N floats: the bucket every replica receives
+ *              (the hook's in-place update).  May alias grads[0] when
+ *              grad_dtype is F32; must not overlap any other grads[w].
+ *   inv_loss_scale : [AMP] unscale factor 1/scale multiplied into every
+ *              gradient element (1.0f when no scaler is used).
+ *   stream   : cudaStream_t; all work is enqueued on it, nothing waits.
+ *
+ * Semantics: while the call count is below start_powerSGD_iter, out is the
+ * replica mean of every element ([DDP] vanilla-allreduce note).  Afterwards
+ * the uncompressed tensors get their replica mean ([DDP] step 2) and each
+ * compressed tensor M gets P Q^T with P = orth(mean_w M_w Q) and
+ * Q = mean_w M_w^T P, M_w = replica w's gradient plus its error-feedback
+ * residual, which then becomes M_w - P Q^T ([DDP] steps 3.1-3.7).  If any
+ * unscaled gradient element is inf or NaN the step is skipped: state is left
+ * as it was, `out` is unspecified, psgd_step_status reports
+ * PSGD_SKIPPED_NONFINITE.  The call counter advances either way.
+ * Errors (synchronous): PSGD_EINVAL (NULL pointers, overlap), PSGD_ECUDA.
+ */
+int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_loss_scale,
+              void* stream);
+
+/*
+ * psgd_step_host -- psgd_step on HOST buffers: copies the W host buckets to
+ * the device (one cudaMemcpyAsync per replica; pinned memory makes them
+ * asynchronous), runs the step and copies `out` back to host memory, all on
+ * `stream`.  The device staging buffers are allocated on the first call (so
+ * the first call may return PSGD_ENOMEM) and reused afterwards.
+ *   host_grads[W] : host pointers, N elements of grad_dtype each.
+ *   host_out      : host pointer, N floats.
+ * Returns after enqueueing; host_out is valid once the stream is synchronised.
+ */
+int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out,
+                   float inv_loss_scale, void* stream);
+
+/*
+ * psgd_step_status -- synchronises `stream` and returns the outcome of the
+ * last step enqueued: PSGD_OK, PSGD_SKIPPED_NONFINITE, or PSGD_ECUDA.
+ */
+int psgd_step_status(psgd_state* s, void* stream);
+
+/*
+ * psgd_get_stats -- [DDP] "PowerSGD State": compression statistics.
+ *   numel_before : elements of the bucket (N).
+ *   numel_after  : elements exchanged per compressed step:
+ *                  sum over compressed tensors of (rows + cols) * rank, plus
+ *                  the uncompressed elements.
+ *   iter         : psgd_step calls so far.
+ * Any pointer may be NULL.
+ */
+int psgd_get_stats(const psgd_state* s, int64_t* numel_before, int64_t* numel_after,
+                   int64_t* iter);
+
+/*
+ * psgd_tensor_info -- the planner's view of tensor `tensor`:
+ * compressed flag, rows, cols, effective rank, first element in the bucket,
+ * and first element in the packed error layout of psgd_get_error (-1 for an
+ * uncompressed tensor).  Any out pointer may be NULL.
+ */
+int psgd_tensor_info(const psgd_state* s, int32_t tensor, int32_t* compressed,
+                     int64_t* rows, int64_t* cols, int32_t* rank,
+                     int64_t* bucket_offset, int64_t* packed_offset);
+
+/* Elements of one replica's packed error buffer (psgd_get_error/set_error). */
+int64_t psgd_error_numel(const psgd_state* s);
+
+/*
+ * psgd_set_q -- install Q for compressed tensor `tensor` from host memory,
+ * cols x rank floats, row-major (rank = the tensor's effective rank).
+ *   is_draw = 1 : the values are a standard-normal draw ([DDP] step 3.1: Q
+ *                 is initialised from a standard normal distribution and
+ *                 orthogonalised); it replaces the library's own draw the
+ *                 next time the tensor needs a fresh Q (its first compressed
+ *                 step, or every step when warm_start is 0) and is
+ *                 orthogonalised there.
+ *   is_draw = 0 : the values become the warm-start Q used as is by the next
+ *                 compressed step (checkpoint restore).
+ * Synchronous (blocks until the copy is done).  PSGD_EINVAL if the tensor is
+ * not compressed.
+ */
+int psgd_set_q(psgd_state* s, int32_t tensor, const float* host_in, int32_t is_draw);
+
+/* psgd_get_q -- the warm-start Q after the last committed step (cols x rank,
+ * host memory; zeros before the first compressed step).  Synchronous. */
+int psgd_get_q(psgd_state* s, int32_t tensor, float* host_out);
+
+/* psgd_get_p -- the orthogonalised P of the last committed compressed step
+ * (rows x rank, host memory; zeros before it).  Synchronous. */
+int psgd_get_p(psgd_state* s, int32_t tensor, float* host_out);
+
+/*
+ * psgd_get_error / psgd_set_error -- replica `replica`'s error-feedback
+ * residual ([DDP] "PowerSGD Hooks" warning: the extra memory that error
+ * feedback needs), packed: compressed tensors in bucket order, each
+ * row-major, at psgd_tensor_info's packed_offset; psgd_error_numel floats.
+ * dev_out / dev_in are device pointers; the work is enqueued on `stream`.
+ * PSGD_EINVAL when error feedback is off.
+ */
+int psgd_get_error(psgd_state* s, int32_t replica, float* dev_out, void* stream);
+int psgd_set_error(psgd_state* s, int32_t replica, const float* dev_in, void* stream);
+
+/* Bytes of device memory the state holds (error store, P/Q, scratch). */
+size_t psgd_workspace_bytes(const psgd_state* s);
+
+/*
+ * Kernel timing for measurement.  psgd_profile(s, 1) makes later psgd_step
+ * calls record a CUDA event pair around every kernel they launch (on the
+ * step's stream); 0 stops it.  psgd_profile_read synchronises the device,
+ * then returns for kernel kind `kind` (0 .. psgd_profile_kinds()-1) its name,
+ * the number of launches and the summed device time since the last read, and
+ * the algorithmic bytes one launch must move (the roofline numerator); it
+ * then clears that kind's record.
+ */
+int psgd_profile(psgd_state* s, int32_t enable);
+int32_t psgd_profile_kinds(void);
+int psgd_profile_read(psgd_state* s, int32_t kind, const char** name, int64_t* launches,
+                      double* total_ms, double* bytes_per_launch);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* psgd_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSGD_H */

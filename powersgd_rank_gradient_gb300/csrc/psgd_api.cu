@@ -1,0 +1,929 @@
+// Host side of the C ABI declared in include/psgd.h: the bucket planner, the
+// state's device memory, and the order in which a step's kernels are
+// enqueued.  No step of the method's arithmetic runs here.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/psgd.h"
+#include "psgd_kernels.cuh"
+#include "psgd_launch.h"
+
+using namespace psgd;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+#define PSGD_CUDA_TRY(expr)                                                            \
+  do {                                                                                 \
+    cudaError_t e_ = (expr);                                                           \
+    if (e_ != cudaSuccess)                                                             \
+      return fail(PSGD_ECUDA, std::string(#expr) + ": " + cudaGetErrorString(e_));      \
+  } while (0)
+
+struct HostTensor {
+  std::vector<int64_t> shape;
+  long long offset = 0;
+  long long numel = 0;
+  int compressed = 0;
+  long long rows = 0, cols = 0;
+  int rank = 0;
+  int cidx = -1;          // compressed ordinal
+  long long e_off = -1;   // packed error offset
+};
+
+int next_pow2(int r) {
+  int p = 1;
+  while (p < r) p <<= 1;
+  return p;
+}
+
+// "DDP Communication Hooks", "PowerSGD State" item 3 and "PowerSGD Hooks"
+// step 1: vectors are never compressed; a >= 2-D tensor viewed as
+// (shape[0], prod(shape[1:])) is compressed iff
+// (rows + cols) * rank * min_compression_rate < rows * cols.
+int plan_tensors(const int64_t* dims, const int32_t* ndims, int32_t n, int32_t rank, double mcr,
+                 std::vector<HostTensor>* out) {
+  if (n < 0) return fail(PSGD_EINVAL, "n_tensors < 0");
+  if (n > 0 && !ndims) return fail(PSGD_EINVAL, "ndims is NULL");
+  long long total_dims = 0;
+  for (int t = 0; t < n; ++t) total_dims += ndims[t] > 0 ? ndims[t] : 0;
+  if (total_dims > 0 && !dims) return fail(PSGD_EINVAL, "dims is NULL");
+  if (rank < 1 || rank > PSGD_MAX_RANK)
+    return fail(PSGD_EINVAL, "matrix_approximation_rank must be in [1, 32]");
+  if (!(mcr >= 0.0)) return fail(PSGD_EINVAL, "min_compression_rate must be >= 0");
+  out->clear();
+  long long off = 0;
+  int d = 0;
+  for (int t = 0; t < n; ++t) {
+    HostTensor h;
+    if (ndims[t] < 0) return fail(PSGD_EINVAL, "negative ndims");
+    long long numel = 1;
+    for (int k = 0; k < ndims[t]; ++k) {
+      const int64_t v = dims[d + k];
+      if (v < 0) return fail(PSGD_EINVAL, "negative dimension");
+      h.shape.push_back(v);
+      numel *= v;
+    }
+    d += ndims[t];
+    h.offset = off;
+    h.numel = numel;
+    if (ndims[t] >= 2 && numel > 0) {
+      h.rows = h.shape[0];
+      h.cols = numel / h.rows;
+      const double lhs = (double)((h.rows + h.cols) * (long long)rank) * mcr;
+      const double rhs = (double)(h.rows * h.cols);
+      if (lhs < rhs) {
+        h.compressed = 1;
+        h.rank = (int)std::min<long long>(rank, std::min(h.rows, h.cols));
+      }
+    } else if (ndims[t] >= 2) {
+      h.rows = h.shape[0];
+      h.cols = h.rows > 0 ? numel / h.rows : 0;
+    }
+    off += numel;
+    out->push_back(h);
+  }
+  return PSGD_OK;
+}
+
+enum Kind { K_MEAN = 0, K_PASS1, K_GRAM, K_SOLVE, K_APPLY, K_PASS2, K_QREDUCE, K_PASS3, K_COMMIT, K_RANDN, K_COUNT };
+const char* kKindNames[K_COUNT] = {"mean", "pass1", "gs_gram", "gs_solve", "gs_apply",
+                                   "pass2", "qreduce", "pass3", "commit", "randn"};
+
+struct EventPair {
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct psgd_state {
+  // configuration
+  int device = 0;
+  int W = 1;
+  int rank = 1;
+  int RP = 1;
+  long long start_iter = 0;
+  double mcr = 2.0;
+  int ef = 1;
+  int warm = 1;
+  float eps = 0.f;
+  unsigned long long seed = 0;
+  int batch = 0;
+  psgd_dtype dtype = PSGD_F32;
+  // plan
+  std::vector<HostTensor> tensors;
+  std::vector<TensorDesc> cdesc;
+  std::vector<Item> items;
+  std::vector<GsItem> gsp, gsq;
+  std::vector<int> gsp_first, gsp_count, gsq_first, gsq_count;
+  std::vector<Segment> unc_segs, all_segs;
+  long long N = 0, Nc = 0, Nc_pad = 0, Nunc = 0, Ne = 0;
+  long long p_total = 0, q_total = 0, pp_total = 0, qp_total = 0;
+  int pass2_src = 0;  // 0 mbar scratch, 1 error store, 2 gradients
+  // device memory
+  TensorDesc* d_tensors = nullptr;
+  Item* d_items = nullptr;
+  GsItem* d_gsp = nullptr;
+  GsItem* d_gsq = nullptr;
+  int* d_gs_index = nullptr;  // gsp_first | gsp_count | gsq_first | gsq_count
+  int* d_mask = nullptr;
+  Segment* d_unc = nullptr;
+  Segment* d_all = nullptr;
+  float* estore = nullptr;
+  float* mbar = nullptr;
+  float* Pf = nullptr;
+  float* Qf = nullptr;
+  float* qinit = nullptr;
+  float* qdraw = nullptr;
+  float* praw_part = nullptr;
+  float* praw = nullptr;
+  float* pgs = nullptr;
+  float* qpart = nullptr;
+  float* tmat = nullptr;
+  double* gram = nullptr;
+  Ctrl* ctrl = nullptr;
+  int* d_status = nullptr;
+  int* h_status = nullptr;  // pinned
+  size_t bytes = 0;
+  std::vector<void*> allocs;
+  // host staging for psgd_step_host
+  std::vector<void*> stage_grads;
+  float* stage_out = nullptr;
+  // counters
+  long long iter = 0;
+  long long compressed_launched = 0;
+  std::vector<int> pending_draw;  // per compressed tensor
+  int sms = 148;
+  // profiling
+  bool prof = false;
+  std::vector<std::vector<EventPair>> ev;
+  std::vector<EventPair> ev_pool;
+  double kind_bytes[K_COUNT] = {0};
+};
+
+namespace {
+
+int dalloc(psgd_state* s, void** p, size_t bytes) {
+  if (bytes == 0) {
+    *p = nullptr;
+    return PSGD_OK;
+  }
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    cudaGetLastError();
+    return fail(e == cudaErrorMemoryAllocation ? PSGD_ENOMEM : PSGD_ECUDA,
+                std::string("cudaMalloc(") + std::to_string(bytes) + "): " + cudaGetErrorString(e));
+  }
+  s->allocs.push_back(*p);
+  s->bytes += bytes;
+  return PSGD_OK;
+}
+
+template <typename T>
+int dupload(psgd_state* s, T** dst, const std::vector<T>& v) {
+  int rc = dalloc(s, (void**)dst, std::max<size_t>(1, v.size()) * sizeof(T));
+  if (rc) return rc;
+  if (!v.empty()) PSGD_CUDA_TRY(cudaMemcpy(*dst, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return PSGD_OK;
+}
+
+void add_segments(std::vector<Segment>* segs, long long off, long long len) {
+  const long long piece = 65536;
+  for (long long o = 0; o < len; o += piece) {
+    Segment sg;
+    sg.off = off + o;
+    sg.len = (int)std::min(piece, len - o);
+    sg.pad = 0;
+    segs->push_back(sg);
+  }
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int now = -1;
+    cudaGetDevice(&now);
+    if (prev >= 0 && now != prev) cudaSetDevice(prev);
+  }
+};
+
+// Builds the work lists of the compressed tensors.
+void build_plan(psgd_state* s) {
+  const int RP = s->RP;
+  const int CT = ctile_for(RP);
+  s->cdesc.clear();
+  s->items.clear();
+  s->gsp.clear();
+  s->gsq.clear();
+  s->gsp_first.clear();
+  s->gsp_count.clear();
+  s->gsq_first.clear();
+  s->gsq_count.clear();
+  s->unc_segs.clear();
+  s->all_segs.clear();
+  long long c_off = 0, p_off = 0, q_off = 0, pp_off = 0, qp_off = 0, e_off = 0;
+  long long unc = 0;
+  // uncompressed ranges, merged
+  long long run_start = -1, run_len = 0;
+  for (auto& h : s->tensors) {
+    if (h.compressed) {
+      if (run_len) add_segments(&s->unc_segs, run_start, run_len);
+      run_start = -1;
+      run_len = 0;
+      TensorDesc td;
+      td.g_off = h.offset;
+      td.c_off = c_off;
+      td.p_off = p_off;
+      td.q_off = q_off;
+      td.n = (int)h.rows;
+      td.m = (int)h.cols;
+      td.r = h.rank;
+      td.ctiles = (int)((h.cols + CT - 1) / CT);
+      td.rblocks = (int)((h.rows + kRowBlock - 1) / kRowBlock);
+      td.pp_off = pp_off;
+      td.qp_off = qp_off;
+      td.e_off = e_off;
+      td.vec = (h.cols % 4 == 0) && (h.offset % 4 == 0);
+      h.cidx = (int)s->cdesc.size();
+      h.e_off = e_off;
+      s->cdesc.push_back(td);
+      c_off += (h.numel + 31) / 32 * 32;
+      p_off += h.rows * RP;
+      q_off += h.cols * RP;
+      pp_off += (long long)td.ctiles * h.rows * RP;
+      qp_off += (long long)td.rblocks * h.cols * RP;
+      e_off += h.numel;
+    } else {
+      unc += h.numel;
+      if (h.numel == 0) continue;
+      if (run_len == 0) run_start = h.offset;
+      run_len += h.numel;
+    }
+  }
+  if (run_len) add_segments(&s->unc_segs, run_start, run_len);
+  add_segments(&s->all_segs, 0, s->N);
+  s->Nc_pad = c_off;
+  s->Ne = e_off;
+  s->Nunc = unc;
+  s->Nc = s->N - unc;
+  s->p_total = p_off;
+  s->q_total = q_off;
+  s->pp_total = pp_off;
+  s->qp_total = qp_off;
+
+  // pass items: (row block) x (column tile)
+  std::vector<int> group_of(s->cdesc.size(), 0);
+  if (s->batch) {
+    // batch_tensors_with_same_shape ("PowerSGD State" item 5 of the later
+    // page): same-shape tensors are scheduled next to each other.
+    std::vector<std::pair<int, int>> shapes;
+    for (size_t c = 0; c < s->cdesc.size(); ++c) {
+      std::pair<int, int> sh(s->cdesc[c].n, s->cdesc[c].m);
+      auto it = std::find(shapes.begin(), shapes.end(), sh);
+      group_of[c] = (int)(it - shapes.begin());
+      if (it == shapes.end()) shapes.push_back(sh);
+    }
+  }
+  for (size_t c = 0; c < s->cdesc.size(); ++c) {
+    const TensorDesc& td = s->cdesc[c];
+    for (int b = 0; b < td.rblocks; ++b)
+      for (int ct = 0; ct < td.ctiles; ++ct) {
+        Item it;
+        it.t = (int)c;
+        it.row0 = b * kRowBlock;
+        it.nrows = std::min(kRowBlock, td.n - it.row0);
+        it.col0 = ct * CT;
+        it.ncols = std::min(CT, td.m - it.col0);
+        it.rb = b;
+        it.ct = ct;
+        it.pad = group_of[c];
+        s->items.push_back(it);
+      }
+  }
+  // largest items first (static round-robin over a persistent grid); with
+  // batching, same-shape groups stay together.
+  std::stable_sort(s->items.begin(), s->items.end(), [&](const Item& x, const Item& y) {
+    if (s->batch && x.pad != y.pad) return x.pad < y.pad;
+    return (long long)x.nrows * x.ncols > (long long)y.nrows * y.ncols;
+  });
+  for (auto& it : s->items) it.pad = 0;
+
+  for (size_t c = 0; c < s->cdesc.size(); ++c) {
+    const TensorDesc& td = s->cdesc[c];
+    s->gsp_first.push_back((int)s->gsp.size());
+    for (int r0 = 0; r0 < td.n; r0 += kGsRows) s->gsp.push_back({(int)c, r0, std::min(kGsRows, td.n - r0), 0});
+    s->gsp_count.push_back((int)s->gsp.size() - s->gsp_first.back());
+    s->gsq_first.push_back((int)s->gsq.size());
+    for (int r0 = 0; r0 < td.m; r0 += kGsRows) s->gsq.push_back({(int)c, r0, std::min(kGsRows, td.m - r0), 0});
+    s->gsq_count.push_back((int)s->gsq.size() - s->gsq_first.back());
+  }
+}
+
+StepArgs make_args(psgd_state* s) {
+  StepArgs a;
+  memset(&a, 0, sizeof(a));
+  a.W = s->W;
+  a.f16 = s->dtype == PSGD_F16;
+  a.scale = 1.f;
+  a.invW = 1.f / (float)s->W;
+  a.estore = s->estore;
+  a.nc_pad = s->Nc_pad;
+  a.mbar = (s->pass2_src == 0) ? s->mbar : nullptr;
+  a.Pf = s->Pf;
+  a.Qf = s->Qf;
+  a.p_total = s->p_total;
+  a.q_total = s->q_total;
+  a.qinit = s->qinit;
+  a.qdraw = s->qdraw;
+  a.praw_part = s->praw_part;
+  a.praw = s->praw;
+  a.pgs = s->pgs;
+  a.qpart = s->qpart;
+  a.gram = s->gram;
+  a.tmat = s->tmat;
+  a.tensors = s->d_tensors;
+  a.items = s->d_items;
+  a.n_items = (int)s->items.size();
+  a.gsp_items = s->d_gsp;
+  a.n_gsp = (int)s->gsp.size();
+  a.gsq_items = s->d_gsq;
+  a.n_gsq = (int)s->gsq.size();
+  const int nt = (int)s->cdesc.size();
+  a.gsp_first = s->d_gs_index;
+  a.gsp_count = s->d_gs_index + nt;
+  a.gsq_first = s->d_gs_index + 2 * nt;
+  a.gsq_count = s->d_gs_index + 3 * nt;
+  a.n_tensors = nt;
+  a.ctrl = s->ctrl;
+  a.ef = s->ef;
+  a.warm_start = s->warm;
+  a.vec_ok = 1;
+  a.eps = s->eps;
+  return a;
+}
+
+// Kernel launches, optionally bracketed by profiling events.
+struct Launcher {
+  psgd_state* s;
+  cudaStream_t st;
+  EventPair cur{};
+  bool on = false;
+  int kind = 0;
+  void begin(int k) {
+    kind = k;
+    on = s->prof;
+    if (!on) return;
+    if (s->ev_pool.empty()) {
+      EventPair p;
+      cudaEventCreate(&p.a);
+      cudaEventCreate(&p.b);
+      s->ev_pool.push_back(p);
+    }
+    cur = s->ev_pool.back();
+    s->ev_pool.pop_back();
+    cudaEventRecord(cur.a, st);
+  }
+  void end() {
+    if (!on) return;
+    cudaEventRecord(cur.b, st);
+    s->ev[kind].push_back(cur);
+  }
+};
+
+template <int RP>
+struct Ops {
+  static void gs(psgd_state* s, const StepArgs& a, Launcher& L, int is_q) {
+    const int n_items = is_q ? a.n_gsq : a.n_gsp;
+    const int grid = std::max(1, std::min(n_items, s->sms * 4));
+    const float* src = is_q ? s->qdraw : s->praw_part;
+    float* dense = is_q ? nullptr : s->praw;
+    const float* src_dense = is_q ? s->qdraw : s->praw;
+    L.begin(K_GRAM);
+    launch_gram<RP>(a, src, dense, is_q, is_q ? 0 : 1, s->gram, grid, L.st);
+    L.end();
+    L.begin(K_SOLVE);
+    launch_solve<RP>(a, s->gram, is_q, L.st);
+    L.end();
+    L.begin(K_APPLY);
+    launch_apply<RP>(a, src_dense, s->pgs, is_q, -1, grid, L.st);
+    L.end();
+    L.begin(K_GRAM);
+    launch_gram<RP>(a, s->pgs, nullptr, is_q, 0, s->gram, grid, L.st);
+    L.end();
+    L.begin(K_SOLVE);
+    launch_solve<RP>(a, s->gram, is_q, L.st);
+    L.end();
+    L.begin(K_APPLY);
+    if (is_q)
+      launch_apply<RP>(a, s->pgs, s->qinit, 1, -1, grid, L.st);
+    else
+      launch_apply<RP>(a, s->pgs, s->Pf, 0, 1, grid, L.st);
+    L.end();
+  }
+
+  static void compressed(psgd_state* s, const StepArgs& a, Launcher& L, bool need_fresh,
+                         const std::vector<int>& mask) {
+    const int grid_items = std::max(1, std::min(a.n_items, s->sms * 2));
+    const int grid_q = std::max(1, std::min(a.n_gsq, s->sms * 4));
+    if (need_fresh) {
+      cudaMemcpyAsync(s->d_mask, mask.data(), mask.size() * sizeof(int), cudaMemcpyHostToDevice, L.st);
+      L.begin(K_RANDN);
+      launch_randn(a, s->d_mask, s->seed, (unsigned long long)s->iter, RP, grid_q, L.st);
+      L.end();
+      gs(s, a, L, 1);
+    }
+    L.begin(K_PASS1);
+    launch_pass1<RP>(a, grid_items, L.st);
+    L.end();
+    gs(s, a, L, 0);
+    L.begin(K_PASS2);
+    launch_pass2<RP>(a, s->pass2_src, grid_items, L.st);
+    L.end();
+    L.begin(K_QREDUCE);
+    launch_qreduce<RP>(a, grid_q, L.st);
+    L.end();
+    L.begin(K_PASS3);
+    launch_pass3<RP>(a, 0, grid_items, L.st);
+    L.end();
+  }
+
+  static void errview(psgd_state* s, const StepArgs& a, int mode, cudaStream_t st) {
+    const int grid_items = std::max(1, std::min(a.n_items, s->sms * 2));
+    launch_pass3<RP>(a, mode, grid_items, st);
+  }
+};
+
+template <template <int> class F, typename... Args>
+void by_rp(int rp, Args&&... args) {
+  switch (rp) {
+    case 1: F<1>::run(args...); break;
+    case 2: F<2>::run(args...); break;
+    case 4: F<4>::run(args...); break;
+    case 8: F<8>::run(args...); break;
+    case 16: F<16>::run(args...); break;
+    default: F<32>::run(args...); break;
+  }
+}
+
+template <int RP>
+struct RunCompressed {
+  static void run(psgd_state* s, const StepArgs& a, Launcher& L, bool need_fresh, const std::vector<int>& mask) {
+    Ops<RP>::compressed(s, a, L, need_fresh, mask);
+  }
+};
+template <int RP>
+struct RunErrView {
+  static void run(psgd_state* s, const StepArgs& a, int mode, cudaStream_t st) { Ops<RP>::errview(s, a, mode, st); }
+};
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const char* x = (const char*)a;
+  const char* y = (const char*)b;
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* psgd_last_error(void) { return g_last_error.c_str(); }
+
+int psgd_plan(const int64_t* dims, const int32_t* ndims, int32_t n_tensors, int32_t rank, double mcr,
+              int32_t* compressed, int32_t* ranks, int64_t* rows, int64_t* cols) {
+  std::vector<HostTensor> ts;
+  int rc = plan_tensors(dims, ndims, n_tensors, rank, mcr, &ts);
+  if (rc) return rc;
+  for (int t = 0; t < n_tensors; ++t) {
+    if (compressed) compressed[t] = ts[t].compressed;
+    if (ranks) ranks[t] = ts[t].rank;
+    if (rows) rows[t] = ts[t].rows;
+    if (cols) cols[t] = ts[t].cols;
+  }
+  return PSGD_OK;
+}
+
+void psgd_state_destroy(psgd_state* s) {
+  if (!s) return;
+  DeviceGuard g(s->device);
+  for (void* p : s->allocs) cudaFree(p);
+  for (void* p : s->stage_grads) cudaFree(p);
+  if (s->stage_out) cudaFree(s->stage_out);
+  if (s->h_status) cudaFreeHost(s->h_status);
+  for (auto& v : s->ev)
+    for (auto& e : v) {
+      cudaEventDestroy(e.a);
+      cudaEventDestroy(e.b);
+    }
+  for (auto& e : s->ev_pool) {
+    cudaEventDestroy(e.a);
+    cudaEventDestroy(e.b);
+  }
+  delete s;
+}
+
+int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tensors, int32_t world_size,
+                      int32_t rank, int64_t start_iter, double mcr, int32_t use_error_feedback,
+                      int32_t warm_start, float eps, uint64_t random_seed, int32_t batch,
+                      psgd_dtype grad_dtype, int32_t device, psgd_state** out) {
+  if (!out) return fail(PSGD_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (world_size < 1 || world_size > PSGD_MAX_WORLD) return fail(PSGD_EINVAL, "world_size must be in [1, 64]");
+  if (start_iter < 0) return fail(PSGD_EINVAL, "start_powerSGD_iter < 0");
+  if (!(eps >= 0.f)) return fail(PSGD_EINVAL, "orthogonalization_epsilon must be >= 0");
+  if (grad_dtype != PSGD_F32 && grad_dtype != PSGD_F16) return fail(PSGD_EINVAL, "grad_dtype");
+  psgd_state* s = new psgd_state();
+  int rc = plan_tensors(dims, ndims, n_tensors, rank, mcr, &s->tensors);
+  if (rc) {
+    delete s;
+    return rc;
+  }
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    delete s;
+    return fail(PSGD_ECUDA, "no such CUDA device");
+  }
+  DeviceGuard g(device);
+  s->device = device;
+  s->W = world_size;
+  s->rank = rank;
+  s->RP = next_pow2(rank);
+  s->start_iter = start_iter;
+  s->mcr = mcr;
+  s->ef = use_error_feedback ? 1 : 0;
+  s->warm = warm_start ? 1 : 0;
+  s->eps = eps;
+  s->seed = random_seed;
+  s->batch = batch ? 1 : 0;
+  s->dtype = grad_dtype;
+  for (auto& h : s->tensors) s->N += h.numel;
+  build_plan(s);
+  cudaDeviceGetAttribute(&s->sms, cudaDevAttrMultiProcessorCount, device);
+  // Where pass 2 reads the replica mean: a scratch copy written by pass 1
+  // costs 8 bytes per element; re-reading the W sources costs W * 4 (store)
+  // or W * sizeof(grad) (no error feedback).  Take the cheaper.
+  const int gsz = grad_dtype == PSGD_F16 ? 2 : 4;
+  const int reread = s->W * (s->ef ? 4 : gsz);
+  s->pass2_src = (reread <= 8) ? (s->ef ? 1 : 2) : 0;
+  if (s->W == 1 && s->ef) s->pass2_src = 1;
+
+  const size_t RP = s->RP;
+  const int nt = (int)s->cdesc.size();
+  std::vector<int> gs_index;
+  gs_index.insert(gs_index.end(), s->gsp_first.begin(), s->gsp_first.end());
+  gs_index.insert(gs_index.end(), s->gsp_count.begin(), s->gsp_count.end());
+  gs_index.insert(gs_index.end(), s->gsq_first.begin(), s->gsq_first.end());
+  gs_index.insert(gs_index.end(), s->gsq_count.begin(), s->gsq_count.end());
+#define TRY(x)                  \
+  do {                          \
+    int rc_ = (x);              \
+    if (rc_) {                  \
+      psgd_state_destroy(s);    \
+      return rc_;               \
+    }                           \
+  } while (0)
+  TRY(dupload(s, &s->d_tensors, s->cdesc));
+  TRY(dupload(s, &s->d_items, s->items));
+  TRY(dupload(s, &s->d_gsp, s->gsp));
+  TRY(dupload(s, &s->d_gsq, s->gsq));
+  TRY(dupload(s, &s->d_gs_index, gs_index));
+  TRY(dupload(s, &s->d_unc, s->unc_segs));
+  TRY(dupload(s, &s->d_all, s->all_segs));
+  TRY(dalloc(s, (void**)&s->d_mask, std::max(1, nt) * sizeof(int)));
+  if (s->ef) TRY(dalloc(s, (void**)&s->estore, 2 * (size_t)s->W * s->Nc_pad * sizeof(float)));
+  if (s->pass2_src == 0) TRY(dalloc(s, (void**)&s->mbar, (size_t)s->Nc_pad * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->Pf, 2 * (size_t)s->p_total * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->Qf, 2 * (size_t)s->q_total * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->qinit, (size_t)s->q_total * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->qdraw, (size_t)s->q_total * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->praw_part, (size_t)s->pp_total * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->praw, (size_t)s->p_total * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->pgs, (size_t)std::max(s->p_total, s->q_total) * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->qpart, (size_t)s->qp_total * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->tmat, std::max(1, nt) * RP * RP * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->gram, std::max<size_t>(1, std::max(s->gsp.size(), s->gsq.size())) * RP * RP * sizeof(double)));
+  TRY(dalloc(s, (void**)&s->ctrl, sizeof(Ctrl)));
+  TRY(dalloc(s, (void**)&s->d_status, sizeof(int)));
+  if (cudaMallocHost((void**)&s->h_status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    s->h_status = nullptr;
+    psgd_state_destroy(s);
+    return fail(PSGD_ENOMEM, "cudaMallocHost");
+  }
+  *s->h_status = 0;
+  // zero state: error store, factors, Q buffers, control block
+  auto zero = [&](void* p, size_t n) -> int {
+    if (p && n) PSGD_CUDA_TRY(cudaMemset(p, 0, n));
+    return PSGD_OK;
+  };
+  if (s->ef) TRY(zero(s->estore, 2 * (size_t)s->W * s->Nc_pad * sizeof(float)));
+  if (s->mbar) TRY(zero(s->mbar, (size_t)s->Nc_pad * sizeof(float)));
+  TRY(zero(s->Pf, 2 * (size_t)s->p_total * sizeof(float)));
+  TRY(zero(s->Qf, 2 * (size_t)s->q_total * sizeof(float)));
+  TRY(zero(s->qinit, (size_t)s->q_total * sizeof(float)));
+  TRY(zero(s->qdraw, (size_t)s->q_total * sizeof(float)));
+  TRY(zero(s->praw_part, (size_t)s->pp_total * sizeof(float)));
+  TRY(zero(s->praw, (size_t)s->p_total * sizeof(float)));
+  TRY(zero(s->ctrl, sizeof(Ctrl)));
+  TRY(zero(s->d_status, sizeof(int)));
+  s->pending_draw.assign(nt, 0);
+  s->ev.assign(K_COUNT, {});
+  // algorithmic bytes per launch of the streaming kernels
+  {
+    const double W = s->W;
+    const double g = gsz;
+    const double nc = (double)s->Nc;
+    s->kind_bytes[K_PASS1] = nc * (W * (g + (s->ef ? 8.0 : 0.0)) + (s->pass2_src == 0 ? 4.0 : 0.0));
+    const double src = s->pass2_src == 0 ? 4.0 : (s->pass2_src == 1 ? 4.0 * W : g * W);
+    s->kind_bytes[K_PASS2] = nc * src;
+    s->kind_bytes[K_PASS3] = nc * 4.0;
+    s->kind_bytes[K_MEAN] = (double)s->Nunc * (W * g + 4.0);
+  }
+  PSGD_CUDA_TRY(cudaDeviceSynchronize());
+  *out = s;
+  return PSGD_OK;
+#undef TRY
+}
+
+int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_loss_scale, void* stream) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (!grads || !out) return fail(PSGD_EINVAL, "grads/out is NULL");
+  const size_t gsz = s->dtype == PSGD_F16 ? 2 : 4;
+  for (int w = 0; w < s->W; ++w) {
+    if (!grads[w]) return fail(PSGD_EINVAL, "grads[w] is NULL");
+    const bool same = (grads[w] == (const void*)out);
+    if (ranges_overlap(grads[w], s->N * gsz, out, s->N * 4)) {
+      if (!(w == 0 && same && s->dtype == PSGD_F32))
+        return fail(PSGD_EINVAL, "out overlaps a replica bucket (only out == grads[0] for F32 is allowed)");
+    }
+  }
+  DeviceGuard g(s->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  StepArgs a = make_args(s);
+  for (int w = 0; w < s->W; ++w) a.grads.p[w] = grads[w];
+  a.out = out;
+  a.scale = inv_loss_scale;
+  int vec_ok = ((uintptr_t)out % 16 == 0);
+  for (int w = 0; w < s->W; ++w) vec_ok &= ((uintptr_t)grads[w] % (s->dtype == PSGD_F16 ? 8 : 16) == 0);
+  a.vec_ok = vec_ok;
+  Launcher L{s, st};
+  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, sizeof(int), st));
+  const int grid_seg = std::max(1, std::min<int>((int)s->all_segs.size(), s->sms * 4));
+  bool compressed_step = false;
+  if (s->iter < s->start_iter) {
+    // "Note that this communication hook enforces vanilla allreduce for the
+    // first state.start_powerSGD_iter iterations."
+    L.begin(K_MEAN);
+    launch_mean(a, s->d_all, (int)s->all_segs.size(), grid_seg, st);
+    L.end();
+  } else {
+    if (!s->unc_segs.empty()) {
+      L.begin(K_MEAN);
+      launch_mean(a, s->d_unc, (int)s->unc_segs.size(),
+                  std::max(1, std::min<int>((int)s->unc_segs.size(), s->sms * 4)), st);
+      L.end();
+    }
+    if (!s->cdesc.empty()) {
+      compressed_step = true;
+      const bool need_fresh = (!s->warm) || s->compressed_launched == 0;
+      std::vector<int> mask(s->cdesc.size(), 0);
+      if (need_fresh) {
+        for (size_t c = 0; c < s->cdesc.size(); ++c) {
+          mask[c] = s->pending_draw[c] ? 0 : 1;
+          s->pending_draw[c] = 0;
+        }
+      }
+      by_rp<RunCompressed>(s->RP, s, a, L, need_fresh, mask);
+      s->compressed_launched++;
+    }
+  }
+  L.begin(K_COMMIT);
+  launch_commit(s->ctrl, compressed_step ? 1 : 0, s->d_status, st);
+  L.end();
+  PSGD_CUDA_TRY(cudaGetLastError());
+  PSGD_CUDA_TRY(cudaMemcpyAsync(s->h_status, s->d_status, sizeof(int), cudaMemcpyDeviceToHost, st));
+  s->iter++;
+  return PSGD_OK;
+}
+
+int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out, float inv_loss_scale,
+                   void* stream) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (!host_grads || !host_out) return fail(PSGD_EINVAL, "host_grads/host_out is NULL");
+  DeviceGuard g(s->device);
+  const size_t gsz = s->dtype == PSGD_F16 ? 2 : 4;
+  if (s->stage_grads.empty()) {
+    s->stage_grads.assign(s->W, nullptr);
+    for (int w = 0; w < s->W; ++w) {
+      if (cudaMalloc(&s->stage_grads[w], std::max<size_t>(16, s->N * gsz)) != cudaSuccess) {
+        cudaGetLastError();
+        for (void* p : s->stage_grads)
+          if (p) cudaFree(p);
+        s->stage_grads.clear();
+        return fail(PSGD_ENOMEM, "staging buffers");
+      }
+    }
+    if (cudaMalloc((void**)&s->stage_out, std::max<size_t>(16, s->N * 4)) != cudaSuccess) {
+      cudaGetLastError();
+      for (void* p : s->stage_grads) cudaFree(p);
+      s->stage_grads.clear();
+      return fail(PSGD_ENOMEM, "staging buffers");
+    }
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int w = 0; w < s->W; ++w) {
+    if (!host_grads[w]) return fail(PSGD_EINVAL, "host_grads[w] is NULL");
+    PSGD_CUDA_TRY(cudaMemcpyAsync(s->stage_grads[w], host_grads[w], s->N * gsz, cudaMemcpyHostToDevice, st));
+  }
+  int rc = psgd_step(s, (const void* const*)s->stage_grads.data(), s->stage_out, inv_loss_scale, stream);
+  if (rc) return rc;
+  PSGD_CUDA_TRY(cudaMemcpyAsync(host_out, s->stage_out, s->N * 4, cudaMemcpyDeviceToHost, st));
+  return PSGD_OK;
+}
+
+int psgd_step_status(psgd_state* s, void* stream) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  DeviceGuard g(s->device);
+  PSGD_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+  return *s->h_status ? PSGD_SKIPPED_NONFINITE : PSGD_OK;
+}
+
+int psgd_get_stats(const psgd_state* s, int64_t* before, int64_t* after, int64_t* iter) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  long long b = 0, a = 0;
+  for (auto& h : s->tensors) {
+    b += h.numel;
+    a += h.compressed ? (h.rows + h.cols) * h.rank : h.numel;
+  }
+  if (before) *before = b;
+  if (after) *after = a;
+  if (iter) *iter = s->iter;
+  return PSGD_OK;
+}
+
+int psgd_tensor_info(const psgd_state* s, int32_t t, int32_t* compressed, int64_t* rows, int64_t* cols,
+                     int32_t* rank, int64_t* bucket_offset, int64_t* packed_offset) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (t < 0 || t >= (int)s->tensors.size()) return fail(PSGD_EINVAL, "tensor index out of range");
+  const HostTensor& h = s->tensors[t];
+  if (compressed) *compressed = h.compressed;
+  if (rows) *rows = h.rows;
+  if (cols) *cols = h.cols;
+  if (rank) *rank = h.rank;
+  if (bucket_offset) *bucket_offset = h.offset;
+  if (packed_offset) *packed_offset = h.compressed ? h.e_off : -1;
+  return PSGD_OK;
+}
+
+int64_t psgd_error_numel(const psgd_state* s) { return s ? s->Ne : 0; }
+
+namespace {
+int read_cur(psgd_state* s, int* cur) {
+  Ctrl c;
+  PSGD_CUDA_TRY(cudaMemcpy(&c, s->ctrl, sizeof(Ctrl), cudaMemcpyDeviceToHost));
+  *cur = c.cur;
+  return PSGD_OK;
+}
+int check_compressed(psgd_state* s, int t, HostTensor** h) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (t < 0 || t >= (int)s->tensors.size()) return fail(PSGD_EINVAL, "tensor index out of range");
+  *h = &s->tensors[t];
+  if (!(*h)->compressed) return fail(PSGD_EINVAL, "tensor is not compressed");
+  return PSGD_OK;
+}
+}  // namespace
+
+int psgd_set_q(psgd_state* s, int32_t t, const float* host_in, int32_t is_draw) {
+  HostTensor* h;
+  int rc = check_compressed(s, t, &h);
+  if (rc) return rc;
+  if (!host_in) return fail(PSGD_EINVAL, "host_in is NULL");
+  DeviceGuard g(s->device);
+  PSGD_CUDA_TRY(cudaDeviceSynchronize());
+  const TensorDesc& td = s->cdesc[h->cidx];
+  std::vector<float> buf((size_t)td.m * s->RP, 0.f);
+  for (long long j = 0; j < td.m; ++j)
+    for (int k = 0; k < td.r; ++k) buf[j * s->RP + k] = host_in[j * td.r + k];
+  if (is_draw) {
+    PSGD_CUDA_TRY(cudaMemcpy(s->qdraw + td.q_off, buf.data(), buf.size() * 4, cudaMemcpyHostToDevice));
+    s->pending_draw[h->cidx] = 1;
+    return PSGD_OK;
+  }
+  // Warm Q: fold the current factors into the error store (the residual stays
+  // the same), zero the committed P so the factors no longer correct anything,
+  // then install Q as the projection of the next step.
+  int cur = 0;
+  rc = read_cur(s, &cur);
+  if (rc) return rc;
+  StepArgs a = make_args(s);
+  if (s->ef) {
+    for (int w = 0; w < s->W; ++w) {
+      a.replica = w;
+      by_rp<RunErrView>(s->RP, s, a, 3, (cudaStream_t)0);
+    }
+    PSGD_CUDA_TRY(cudaGetLastError());
+  }
+  PSGD_CUDA_TRY(cudaMemset(s->Pf + (size_t)cur * s->p_total, 0, (size_t)s->p_total * 4));
+  PSGD_CUDA_TRY(cudaMemcpy(s->Qf + (size_t)cur * s->q_total + td.q_off, buf.data(), buf.size() * 4,
+                           cudaMemcpyHostToDevice));
+  int one = 1;
+  PSGD_CUDA_TRY(cudaMemcpy(&s->ctrl->warm_valid, &one, sizeof(int), cudaMemcpyHostToDevice));
+  if (s->compressed_launched == 0) s->compressed_launched = 1;
+  PSGD_CUDA_TRY(cudaDeviceSynchronize());
+  return PSGD_OK;
+}
+
+static int get_factor(psgd_state* s, int t, float* host_out, bool is_q) {
+  HostTensor* h;
+  int rc = check_compressed(s, t, &h);
+  if (rc) return rc;
+  if (!host_out) return fail(PSGD_EINVAL, "host_out is NULL");
+  DeviceGuard g(s->device);
+  PSGD_CUDA_TRY(cudaDeviceSynchronize());
+  int cur = 0;
+  rc = read_cur(s, &cur);
+  if (rc) return rc;
+  const TensorDesc& td = s->cdesc[h->cidx];
+  const long long rows = is_q ? td.m : td.n;
+  std::vector<float> buf((size_t)rows * s->RP);
+  const float* src = is_q ? s->Qf + (size_t)cur * s->q_total + td.q_off : s->Pf + (size_t)cur * s->p_total + td.p_off;
+  PSGD_CUDA_TRY(cudaMemcpy(buf.data(), src, buf.size() * 4, cudaMemcpyDeviceToHost));
+  for (long long j = 0; j < rows; ++j)
+    for (int k = 0; k < td.r; ++k) host_out[j * td.r + k] = buf[j * s->RP + k];
+  return PSGD_OK;
+}
+
+int psgd_get_q(psgd_state* s, int32_t t, float* host_out) { return get_factor(s, t, host_out, true); }
+int psgd_get_p(psgd_state* s, int32_t t, float* host_out) { return get_factor(s, t, host_out, false); }
+
+static int err_view(psgd_state* s, int32_t replica, float* ptr, void* stream, int mode) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (!s->ef) return fail(PSGD_EINVAL, "error feedback is off");
+  if (replica < 0 || replica >= s->W) return fail(PSGD_EINVAL, "replica out of range");
+  if (!ptr) return fail(PSGD_EINVAL, "buffer is NULL");
+  if (s->cdesc.empty()) return PSGD_OK;
+  DeviceGuard g(s->device);
+  StepArgs a = make_args(s);
+  a.replica = replica;
+  a.eio = ptr;
+  by_rp<RunErrView>(s->RP, s, a, mode, (cudaStream_t)stream);
+  PSGD_CUDA_TRY(cudaGetLastError());
+  return PSGD_OK;
+}
+
+int psgd_get_error(psgd_state* s, int32_t replica, float* dev_out, void* stream) {
+  return err_view(s, replica, dev_out, stream, 1);
+}
+int psgd_set_error(psgd_state* s, int32_t replica, const float* dev_in, void* stream) {
+  return err_view(s, replica, (float*)dev_in, stream, 2);
+}
+
+size_t psgd_workspace_bytes(const psgd_state* s) { return s ? s->bytes : 0; }
+
+int psgd_profile(psgd_state* s, int32_t enable) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  s->prof = enable != 0;
+  return PSGD_OK;
+}
+
+int32_t psgd_profile_kinds(void) { return K_COUNT; }
+
+int psgd_profile_read(psgd_state* s, int32_t kind, const char** name, int64_t* launches, double* total_ms,
+                      double* bytes_per_launch) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (kind < 0 || kind >= K_COUNT) return fail(PSGD_EINVAL, "kind out of range");
+  DeviceGuard g(s->device);
+  PSGD_CUDA_TRY(cudaDeviceSynchronize());
+  double ms = 0.0;
+  for (auto& e : s->ev[kind]) {
+    float x = 0.f;
+    cudaEventElapsedTime(&x, e.a, e.b);
+    ms += x;
+    s->ev_pool.push_back(e);
+  }
+  if (name) *name = kKindNames[kind];
+  if (launches) *launches = (int64_t)s->ev[kind].size();
+  if (total_ms) *total_ms = ms;
+  if (bytes_per_launch) *bytes_per_launch = s->kind_bytes[kind];
+  s->ev[kind].clear();
+  return PSGD_OK;
+}
+
+}  // extern "C"

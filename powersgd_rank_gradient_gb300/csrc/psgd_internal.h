@@ -1,0 +1,83 @@
+// Internal layout shared by the host planner (psgd_api.cu) and the kernels.
+//
+// HBM layout of a state (all offsets in elements):
+//   error store  : 2 (current/next) x W x Nc_pad floats.  Replica w's store for
+//                  tensor t starts at c_off[t] (aligned to 32 elements).  It
+//                  holds M_w of the last committed step; the residual is kept
+//                  in factored form, e_w = store_w - P Q^T, with (P, Q) the
+//                  factors of that step (see Pf/Qf).
+//   Pf[2], Qf[2] : the committed factors (rows x RP, cols x RP per tensor,
+//                  rank padded to RP = next power of two, unused columns 0).
+//                  Qf[cur] is also the warm-start projection of the next step.
+//   praw_part    : pass-1 partial P = Mbar Q, one slice per column tile.
+//   qpart        : pass-2 partial Q = Mbar^T P, one slice per row block.
+//   mbar         : optional scratch holding the replica mean of M (W >= 3).
+//   ctrl         : device integers: cur, warm_valid, nonfinite flag.
+#pragma once
+
+#include <stdint.h>
+
+namespace psgd {
+
+constexpr int kThreads = 256;      // threads per CTA of the streaming passes
+constexpr int kRowBlock = 512;     // rows per work item of the three passes
+constexpr int kGsRows = 1024;      // rows per work item of the Gram-Schmidt kernels
+
+// Columns per thread (CPT) and column-tile width of the streaming passes for
+// a padded rank RP: the per-thread accumulators hold CPT x RP floats.
+__host__ __device__ constexpr int cpt_for(int rp) { return rp <= 8 ? 4 : (rp == 16 ? 2 : 1); }
+__host__ __device__ constexpr int ctile_for(int rp) { return kThreads * cpt_for(rp); }
+
+struct TensorDesc {
+  long long g_off;   // first element in the bucket
+  long long c_off;   // first element in the packed error store / mbar
+  long long p_off;   // first element of the tensor's P (rows x RP)
+  long long q_off;   // first element of the tensor's Q (cols x RP)
+  long long pp_off;  // first element of praw_part (ctiles x rows x RP)
+  long long qp_off;  // first element of qpart (rblocks x cols x RP)
+  long long e_off;   // first element in the user-visible packed error (no padding)
+  int n, m, r;       // rows, cols, effective rank
+  int ctiles;        // column tiles
+  int rblocks;       // row blocks
+  int vec;           // rows are 16-byte aligned in the bucket (m % 4 == 0, g_off % 4 == 0)
+};
+
+// One work item of the streaming passes: a (row block) x (column tile) tile.
+struct Item {
+  int t;
+  int row0, nrows;
+  int col0, ncols;
+  int rb;   // row-block index within the tensor
+  int ct;   // column-tile index within the tensor
+  int pad;
+};
+
+// Row ranges of the small Gram-Schmidt kernels, over P (rows = n) or over Q
+// (rows = m).
+struct GsItem {
+  int t;
+  int row0, nrows;
+  int pad;
+};
+
+// An uncompressed range of the bucket, split into pieces of <= 64K elements.
+struct Segment {
+  long long off;
+  int len;
+  int pad;
+};
+
+struct Ctrl {
+  int cur;        // which half of the double-buffered state is current
+  int warm_valid; // a committed compressed step exists (warm Q available)
+  int flag;       // non-finite input seen in this step
+  int timeout;    // reserved: a bounded device-side wait gave up
+};
+
+constexpr int kMaxWorld = 64;
+
+struct GradPtrs {
+  const void* p[kMaxWorld];
+};
+
+}  // namespace psgd

@@ -1,0 +1,737 @@
+// Kernels of the PowerSGD hook step, templated on the padded rank RP.
+//
+// The step ("DDP Communication Hooks", "PowerSGD Hooks", powerSGD_hook
+// steps 3.1-3.7) runs as three streaming passes over every compressed matrix
+// plus a small Gram-Schmidt stage on P:
+//
+//   pass 1  M_w  = g_w * s + (store_w - P_old Q_old^T)     error feedback, unscale
+//           store'_w = M_w                                 (next half of the store)
+//           Mbar = mean_w M_w                              allreduce of P folded:
+//           P_raw = Mbar Q                                 mean_w(M_w Q) = Mbar Q
+//   GS      P = orth(P_raw)                                steps 3.3-3.4
+//   pass 2  Q' = Mbar^T P                                  steps 3.5-3.6 (mean folded)
+//   pass 3  out = P Q'^T                                   step 3.7
+//
+// The residual M_w - P Q'^T is never written: the store keeps M_w and the
+// factors (P, Q') of the step, and pass 1 of the next step subtracts P Q'^T
+// on the fly with the same fused multiply-add chain pass 3 uses for `out`,
+// so the value it sees is exactly fl(M_w - out).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "psgd_internal.h"
+
+namespace psgd {
+
+// ---------------------------------------------------------------------------
+// Arguments
+// ---------------------------------------------------------------------------
+struct StepArgs {
+  GradPtrs grads;
+  int W;
+  int f16;            // grads are __half
+  float scale;        // inverse loss scale
+  float invW;
+  float* out;
+  float* estore;      // error store: half b, replica w at (b * W + w) * nc_pad
+  long long nc_pad;
+  float* mbar;        // replica-mean scratch or nullptr
+  float* Pf;          // committed P, half b at b * p_total
+  float* Qf;          // committed Q, half b at b * q_total
+  long long p_total, q_total;
+  float* qinit;       // orthogonalised fresh Q (used when no warm Q)
+  float* qdraw;       // raw standard-normal draw before orthogonalisation
+  float* praw_part;   // pass-1 partials
+  float* praw;        // summed P_raw
+  float* pgs;         // first Gram-Schmidt sweep output (P and Q share it)
+  float* qpart;       // pass-2 partials
+  double* gram;       // per Gram-Schmidt item RP x RP
+  float* tmat;        // per tensor RP x RP transform
+  const TensorDesc* tensors;
+  const Item* items;
+  int n_items;
+  const GsItem* gsp_items;   // rows of P
+  int n_gsp;
+  const GsItem* gsq_items;   // rows of Q
+  int n_gsq;
+  const int* gsp_first;      // per tensor: first Gram-Schmidt item over P
+  const int* gsp_count;
+  const int* gsq_first;      // per tensor: first item over Q
+  const int* gsq_count;
+  int n_tensors;
+  Ctrl* ctrl;
+  int ef;
+  int warm_start;
+  int vec_ok;          // grads/out base pointers allow 16-byte (8 for f16) accesses
+  float eps;
+  // error get/set
+  int replica;
+  float* eio;          // user buffer (packed, e_off layout)
+};
+
+// ---------------------------------------------------------------------------
+// Memory helpers: streamed data bypasses L1 so the small Q tiles stay there.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_stream1(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+// The error store is read and written by the same pass (different halves),
+// so it is read with a plain (coherent) load.
+__device__ __forceinline__ float4 ld_cg4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_cg1(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_stream4(float* p, float4 v) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_stream1(float* p, float v) {
+  asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// NC consecutive elements of a gradient bucket as floats.  NC = 4 is one
+// vector access (the caller guarantees alignment); other widths go element by
+// element.
+template <int NC, typename GT>
+__device__ __forceinline__ void load_grad(const GT* p, float (&v)[NC]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    float t[1];
+    load_grad<1, GT>(p + c, t);
+    v[c] = t[0];
+  }
+}
+
+template <>
+__device__ __forceinline__ void load_grad<4, float>(const float* p, float (&v)[4]) {
+  float4 x = ld_stream4(p);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <>
+__device__ __forceinline__ void load_grad<1, float>(const float* p, float (&v)[1]) {
+  v[0] = ld_stream1(p);
+}
+template <>
+__device__ __forceinline__ void load_grad<4, __half>(const __half* p, float (&v)[4]) {
+  uint2 raw;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(raw.x), "=r"(raw.y)
+               : "l"(p));
+  __half2 a = *reinterpret_cast<__half2*>(&raw.x);
+  __half2 b = *reinterpret_cast<__half2*>(&raw.y);
+  float2 fa = __half22float2(a), fb = __half22float2(b);
+  v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+template <>
+__device__ __forceinline__ void load_grad<1, __half>(const __half* p, float (&v)[1]) {
+  unsigned short raw;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(raw) : "l"(p));
+  v[0] = __half2float(__ushort_as_half(raw));
+}
+
+template <int NC>
+__device__ __forceinline__ void load_f(const float* p, float (&v)[NC], bool stream) {
+  if constexpr (NC == 4) {
+    float4 x = stream ? ld_stream4(p) : ld_cg4(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) v[c] = stream ? ld_stream1(p + c) : ld_cg1(p + c);
+  }
+}
+template <int NC>
+__device__ __forceinline__ void store_f(float* p, const float (&v)[NC]) {
+  if constexpr (NC == 4) {
+    st_stream4(p, make_float4(v[0], v[1], v[2], v[3]));
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) st_stream1(p + c, v[c]);
+  }
+}
+
+// One row of a factor matrix (RP floats, 16-byte aligned when RP >= 4).
+template <int RP>
+__device__ __forceinline__ void load_row(const float* __restrict__ p, float (&v)[RP]) {
+  if constexpr (RP >= 4) {
+#pragma unroll
+    for (int k = 0; k < RP; k += 4) {
+      float4 x = __ldg(reinterpret_cast<const float4*>(p + k));
+      v[k] = x.x; v[k + 1] = x.y; v[k + 2] = x.z; v[k + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < RP; ++k) v[k] = __ldg(p + k);
+  }
+}
+
+// sum_k a[k] * b[k] as one fused multiply-add chain in increasing k.  Pass 3
+// (out) and pass 1 (the lazy residual) both use it, so they agree bit for bit.
+template <int RP>
+__device__ __forceinline__ float dot_chain(const float (&a)[RP], const float (&b)[RP]) {
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < RP; ++k) acc = fmaf(a[k], b[k], acc);
+  return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: error feedback + unscale + replica mean + P_raw = Mbar Q.
+// One CTA per (row block, column tile) item; a warp owns RW rows at a time,
+// its lanes stride the tile's columns NC at a time.  P_raw partials of the
+// tile are reduced across the warp and written per column tile.
+// ---------------------------------------------------------------------------
+template <int RP, int WT, typename GT, int RW, int NC>
+__device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& td,
+                                           const Item& item, const float* __restrict__ Qp,
+                                           const float* __restrict__ Qc,
+                                           const float* __restrict__ Pc, int cur, int& bad) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int W = WT > 0 ? WT : a.W;
+  const int nxt = cur ^ 1;
+  const long long m = td.m;
+  const int cend = item.col0 + item.ncols;
+  for (int rr = warp * RW; rr < item.nrows; rr += (kThreads / 32) * RW) {
+    float po[RW][RP];
+    float pacc[RW][RP];
+    bool rv[RW];
+#pragma unroll
+    for (int q = 0; q < RW; ++q) {
+      rv[q] = (rr + q) < item.nrows;
+      const int i = item.row0 + (rv[q] ? rr + q : rr);
+#pragma unroll
+      for (int k = 0; k < RP; ++k) { pacc[q][k] = 0.f; po[q][k] = 0.f; }
+      if (a.ef) load_row<RP>(Pc + td.p_off + (long long)i * RP, po[q]);
+    }
+    for (int c = item.col0 + lane * NC; c < cend; c += 32 * NC) {
+      // residual correction P_old[i,:] . Q_old[c,:]
+      float corr[RW][NC];
+      if (a.ef) {
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) {
+          float qo[RP];
+          load_row<RP>(Qc + td.q_off + (long long)(c + cc) * RP, qo);
+#pragma unroll
+          for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qo);
+        }
+      }
+      float mb[RW][NC];
+#pragma unroll
+      for (int q = 0; q < RW; ++q)
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) mb[q][cc] = 0.f;
+#pragma unroll(WT > 0 ? WT : 1)
+      for (int w = 0; w < W; ++w) {
+        const GT* g = reinterpret_cast<const GT*>(a.grads.p[w]);
+        float* ecur = a.estore + ((long long)cur * a.W + w) * a.nc_pad + td.c_off;
+        float* enxt = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off;
+#pragma unroll
+        for (int q = 0; q < RW; ++q) {
+          if (!rv[q]) continue;
+          const long long i = item.row0 + rr + q;
+          float gv[NC];
+          load_grad<NC, GT>(g + td.g_off + i * m + c, gv);
+          float ev[NC];
+          if (a.ef) load_f<NC>(ecur + i * m + c, ev, false);
+          float mv[NC];
+#pragma unroll
+          for (int cc = 0; cc < NC; ++cc) {
+            const float v = gv[cc] * a.scale;
+            bad |= !isfinite(v);
+            mv[cc] = a.ef ? v + (ev[cc] - corr[q][cc]) : v;
+            mb[q][cc] += mv[cc];
+          }
+          if (a.ef) store_f<NC>(enxt + i * m + c, mv);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < RW; ++q) {
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) mb[q][cc] *= a.invW;
+        if (a.mbar && rv[q]) store_f<NC>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * m + c, mb[q]);
+      }
+#pragma unroll
+      for (int cc = 0; cc < NC; ++cc) {
+        float qv[RP];
+        load_row<RP>(Qp + td.q_off + (long long)(c + cc) * RP, qv);
+#pragma unroll
+        for (int q = 0; q < RW; ++q)
+#pragma unroll
+          for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[k], pacc[q][k]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < RW; ++q) {
+#pragma unroll
+      for (int k = 0; k < RP; ++k) pacc[q][k] = warp_sum(pacc[q][k]);
+      if (rv[q] && lane == 0) {
+        float* dst = a.praw_part + td.pp_off +
+                     ((long long)item.ct * td.n + item.row0 + rr + q) * RP;
+#pragma unroll
+        for (int k = 0; k < RP; ++k) dst[k] = pacc[q][k];
+      }
+    }
+  }
+}
+
+template <int RP, int WT, typename GT, int RW>
+__global__ void __launch_bounds__(kThreads) k_pass1(const StepArgs a) {
+  const int cur = a.ctrl->cur;
+  const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
+  const float* Qc = a.Qf + (long long)cur * a.q_total;
+  const float* Pc = a.Pf + (long long)cur * a.p_total;
+  const float* Qp = use_init ? a.qinit : Qc;
+  int bad = 0;
+  for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+    const Item item = a.items[it];
+    const TensorDesc td = a.tensors[item.t];
+    if (td.vec && a.vec_ok)
+      pass1_tile<RP, WT, GT, RW, 4>(a, td, item, Qp, Qc, Pc, cur, bad);
+    else
+      pass1_tile<RP, WT, GT, RW, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
+}
+
+// ---------------------------------------------------------------------------
+// Gram-Schmidt stage.
+//
+// "PowerSGD Hooks" step 3.4 orthogonalises P column by column; "PowerSGD
+// State" item 4 adds epsilon to each column norm.  Every Gram-Schmidt
+// operation is a column operation, so the result is X T for an RP x RP upper
+// triangular T that depends only on the Gram matrix G = X^T X.  The stage
+// therefore (1) reduces G over row blocks in fp64 (k_gram), (2) runs modified
+// Gram-Schmidt with epsilon symbolically on G to get T (k_solve, one warp per
+// tensor, fp64), (3) applies X T (k_apply).  It runs twice (the second sweep
+// re-orthogonalises the first sweep's output), which keeps P^T P = I to fp32
+// rounding even when X is ill conditioned.
+// ---------------------------------------------------------------------------
+constexpr int kGramTile = 128;
+
+// Rows of P live as column-tile partials (nparts > 1) or dense (nparts == 1).
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float* __restrict__ src,
+                                                   float* __restrict__ dense_out, int is_q,
+                                                   int from_parts, double* __restrict__ gram_out) {
+  __shared__ float tile[kGramTile][RP + 1];
+  __shared__ double red[kThreads];
+  constexpr int PAIRS = RP * RP;
+  constexpr int PPT = PAIRS > kThreads ? PAIRS / kThreads : 1;   // pairs per thread
+  constexpr int GROUPS = PAIRS >= kThreads ? 1 : kThreads / PAIRS;
+  const GsItem* items = is_q ? a.gsq_items : a.gsp_items;
+  const int n_items = is_q ? a.n_gsq : a.n_gsp;
+  if (a.ctrl->flag) return;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const GsItem gi = items[it];
+    const TensorDesc td = a.tensors[gi.t];
+    const long long base = is_q ? td.q_off : td.p_off;
+    const int pair0 = (threadIdx.x % (PAIRS >= kThreads ? kThreads : PAIRS)) * PPT;
+    const int grp = PAIRS >= kThreads ? 0 : threadIdx.x / PAIRS;
+    double dacc[PPT];
+#pragma unroll
+    for (int u = 0; u < PPT; ++u) dacc[u] = 0.0;
+    for (int r0 = 0; r0 < gi.nrows; r0 += kGramTile) {
+      const int rows = min(kGramTile, gi.nrows - r0);
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < rows * RP; idx += kThreads) {
+        const int rr = idx / RP, k = idx % RP;
+        const long long row = gi.row0 + r0 + rr;
+        float v;
+        if (from_parts) {
+          v = 0.f;
+          for (int c = 0; c < td.ctiles; ++c) v += src[td.pp_off + ((long long)c * td.n + row) * RP + k];
+        } else {
+          v = src[base + row * RP + k];
+        }
+        if (k >= td.r) v = 0.f;
+        tile[rr][k] = v;
+        if (dense_out) dense_out[base + row * RP + k] = v;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < PPT; ++u) {
+        const int pa = (pair0 + u) / RP, pb = (pair0 + u) % RP;
+        float facc = 0.f;
+        int cnt = 0;
+        for (int rr = grp; rr < rows; rr += GROUPS) {
+          facc = fmaf(tile[rr][pa], tile[rr][pb], facc);
+          if (++cnt == 8) { dacc[u] += (double)facc; facc = 0.f; cnt = 0; }
+        }
+        dacc[u] += (double)facc;
+      }
+    }
+    // reduce the row groups
+#pragma unroll
+    for (int u = 0; u < PPT; ++u) {
+      __syncthreads();
+      red[threadIdx.x] = dacc[u];
+      __syncthreads();
+      if (threadIdx.x < (PAIRS >= kThreads ? kThreads : PAIRS)) {
+        double s = 0.0;
+        for (int g = 0; g < GROUPS; ++g) s += red[threadIdx.x + g * (PAIRS >= kThreads ? kThreads : PAIRS)];
+        gram_out[(long long)it * PAIRS + pair0 + u] = s;
+      }
+    }
+  }
+}
+
+// One warp per tensor: sum the item Gram matrices in item order, then modified
+// Gram-Schmidt with epsilon on the coefficient matrix.  Lane j holds column j
+// of T.
+template <int RP>
+__global__ void __launch_bounds__(32) k_solve(const StepArgs a, const double* __restrict__ gram_in,
+                                              int is_q, int only_init) {
+  __shared__ double G[RP * RP];
+  const int t = blockIdx.x;
+  const int lane = threadIdx.x;
+  if (a.ctrl->flag) return;
+  const TensorDesc td = a.tensors[t];
+  const int first = is_q ? a.gsq_first[t] : a.gsp_first[t];
+  const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
+  if (count == 0) return;
+  for (int idx = lane; idx < RP * RP; idx += 32) {
+    double s = 0.0;
+    for (int it = 0; it < count; ++it) s += gram_in[(long long)(first + it) * RP * RP + idx];
+    G[idx] = s;
+  }
+  __syncwarp();
+  const int r = td.r;
+  const double eps = (double)a.eps;
+  double tj[RP];
+#pragma unroll
+  for (int k = 0; k < RP; ++k) tj[k] = (k == lane && lane < r) ? 1.0 : 0.0;
+  for (int i = 0; i < r; ++i) {
+    double ti[RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) ti[k] = __shfl_sync(0xffffffffu, tj[k], i);
+    // lane k: (G t_i)[k]
+    double gk = 0.0;
+    if (lane < r) {
+#pragma unroll
+      for (int l = 0; l < RP; ++l) gk += G[lane * RP + l] * ti[l];
+    }
+    double tl = 0.0;
+#pragma unroll
+    for (int k = 0; k < RP; ++k)
+      if (k == lane) tl = ti[k];
+    double part = (lane < r) ? tl * gk : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    const double nrm = sqrt(fmax(part, 0.0));
+    const double sc = 1.0 / (nrm + eps);
+#pragma unroll
+    for (int k = 0; k < RP; ++k) ti[k] *= sc;
+    gk *= sc;
+    if (lane == i) {
+#pragma unroll
+      for (int k = 0; k < RP; ++k) tj[k] = ti[k];
+    }
+    double gall[RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) gall[k] = __shfl_sync(0xffffffffu, gk, k);
+    if (lane > i && lane < r) {
+      double d = 0.0;
+#pragma unroll
+      for (int k = 0; k < RP; ++k) d += gall[k] * tj[k];
+#pragma unroll
+      for (int k = 0; k < RP; ++k) tj[k] -= d * ti[k];
+    }
+  }
+  if (lane < RP) {
+    float* T = a.tmat + (long long)t * RP * RP;
+#pragma unroll
+    for (int k = 0; k < RP; ++k) T[k * RP + lane] = (lane < r) ? (float)tj[k] : 0.f;
+  }
+}
+
+// dst rows = src rows x T (thread per row).
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const float* __restrict__ src,
+                                                    float* __restrict__ dst, int is_q, int dst_half) {
+  __shared__ float T[RP * RP];
+  const GsItem* items = is_q ? a.gsq_items : a.gsp_items;
+  const int n_items = is_q ? a.n_gsq : a.n_gsp;
+  if (a.ctrl->flag) return;
+  // dst_half >= 0: write into half (cur ^ 1) of Pf/Qf (dst is the base)
+  long long half_off = 0;
+  if (dst_half >= 0) half_off = (long long)(a.ctrl->cur ^ 1) * (is_q ? a.q_total : a.p_total);
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const GsItem gi = items[it];
+    const TensorDesc td = a.tensors[gi.t];
+    const long long base = is_q ? td.q_off : td.p_off;
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < RP * RP; idx += kThreads) T[idx] = a.tmat[(long long)gi.t * RP * RP + idx];
+    __syncthreads();
+    for (int rr = threadIdx.x; rr < gi.nrows; rr += kThreads) {
+      const long long row = gi.row0 + rr;
+      float x[RP], y[RP];
+#pragma unroll
+      for (int k = 0; k < RP; ++k) { x[k] = src[base + row * RP + k]; y[k] = 0.f; }
+#pragma unroll
+      for (int l = 0; l < RP; ++l)
+#pragma unroll
+        for (int k = 0; k < RP; ++k) y[k] = fmaf(x[l], T[l * RP + k], y[k]);
+#pragma unroll
+      for (int k = 0; k < RP; ++k) dst[half_off + base + row * RP + k] = y[k];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: partial Q' = Mbar^T P over one (row block, column tile); each thread
+// owns CPT columns and accumulates CPT x RP sums over the block's rows.
+// SRC 0: Mbar scratch; 1: mean of the W store halves just written; 2: mean of
+// the W unscaled gradients (error feedback off).
+// ---------------------------------------------------------------------------
+constexpr int kPStage = 64;
+
+template <int RP, int SRC, typename GT, int NC>
+__device__ __forceinline__ void pass2_tile(const StepArgs& a, const TensorDesc& td, const Item& item,
+                                           const float* __restrict__ P, float (*ps)[RP]) {
+  constexpr int CPT = cpt_for(RP);
+  const long long m = td.m;
+  const int c0 = item.col0 + threadIdx.x * CPT;
+  const int nxt = a.ctrl->cur ^ 1;
+  float acc[CPT][RP];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c)
+#pragma unroll
+    for (int k = 0; k < RP; ++k) acc[c][k] = 0.f;
+  const int cend = item.col0 + item.ncols;
+  for (int sb = 0; sb < item.nrows; sb += kPStage) {
+    const int rows = min(kPStage, item.nrows - sb);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * RP; idx += kThreads)
+      ps[idx / RP][idx % RP] = P[td.p_off + (long long)(item.row0 + sb) * RP + idx];
+    __syncthreads();
+    if (c0 >= cend) continue;
+#pragma unroll 4
+    for (int i = 0; i < rows; ++i) {
+      const long long row = item.row0 + sb + i;
+      float mv[CPT];
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) mv[c] = 0.f;
+      if constexpr (NC == CPT) {
+        if constexpr (SRC == 0) {
+          load_f<NC>(a.mbar + td.c_off + row * m + c0, mv, true);
+        } else {
+          for (int w = 0; w < a.W; ++w) {
+            float v[NC];
+            if constexpr (SRC == 1) {
+              load_f<NC>(a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * m + c0, v, true);
+            } else {
+              load_grad<NC, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c0, v);
+#pragma unroll
+              for (int c = 0; c < NC; ++c) v[c] *= a.scale;
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) mv[c] += v[c];
+          }
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) mv[c] *= a.invW;
+        }
+      } else {
+        // unaligned tensor: element by element
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          if (c0 + c >= cend) continue;
+          if constexpr (SRC == 0) {
+            mv[c] = ld_stream1(a.mbar + td.c_off + row * m + c0 + c);
+          } else {
+            float s = 0.f;
+            for (int w = 0; w < a.W; ++w) {
+              float v[1];
+              if constexpr (SRC == 1) {
+                v[0] = ld_stream1(a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * m + c0 + c);
+              } else {
+                load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c0 + c, v);
+                v[0] *= a.scale;
+              }
+              s += v[0];
+            }
+            mv[c] = s * a.invW;
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < CPT; ++c)
+#pragma unroll
+        for (int k = 0; k < RP; ++k) acc[c][k] = fmaf(mv[c], ps[i][k], acc[c][k]);
+    }
+  }
+  // columns of this thread
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    if (c0 + c >= cend) continue;
+    float* dst = a.qpart + td.qp_off + ((long long)item.rb * td.m + c0 + c) * RP;
+#pragma unroll
+    for (int k = 0; k < RP; ++k) dst[k] = acc[c][k];
+  }
+}
+
+template <int RP, int SRC, typename GT>
+__global__ void __launch_bounds__(kThreads) k_pass2(const StepArgs a) {
+  __shared__ __align__(16) float ps[kPStage][RP];
+  if (a.ctrl->flag) return;
+  const float* P = a.Pf + (long long)(a.ctrl->cur ^ 1) * a.p_total;
+  constexpr int CPT = cpt_for(RP);
+  for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+    const Item item = a.items[it];
+    const TensorDesc td = a.tensors[item.t];
+    // CPT-wide vector accesses need rows aligned to CPT elements; the store and
+    // mbar are, the gradient rows are when the tensor is marked vec.
+    const bool vec = (SRC == 2) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
+    if (vec)
+      pass2_tile<RP, SRC, GT, CPT>(a, td, item, P, ps);
+    else
+      pass2_tile<RP, SRC, GT, 1>(a, td, item, P, ps);
+  }
+}
+
+// Q'[j] = sum over row blocks of the partials, in row-block order; written
+// into the next half of Qf.
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
+  if (a.ctrl->flag) return;
+  float* Q = a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
+  for (int it = blockIdx.x; it < a.n_gsq; it += gridDim.x) {
+    const GsItem gi = a.gsq_items[it];
+    const TensorDesc td = a.tensors[gi.t];
+    for (int idx = threadIdx.x; idx < gi.nrows * RP; idx += kThreads) {
+      const long long j = gi.row0 + idx / RP;
+      const int k = idx % RP;
+      float s = 0.f;
+      for (int b = 0; b < td.rblocks; ++b) s += a.qpart[td.qp_off + ((long long)b * td.m + j) * RP + k];
+      Q[td.q_off + j * RP + k] = s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 3: out = P Q'^T.  Each thread keeps its CPT columns of Q' in registers.
+// MODE 0: write out (bucket layout).  MODE 1: materialise replica `a.replica`'s
+// residual store - P Q^T of the committed half into a.eio.  MODE 2: set the
+// store from a.eio + P Q^T.  MODE 3: fold the factors into the store in place
+// (store -= P Q^T), after which the factors can be replaced.
+// ---------------------------------------------------------------------------
+template <int RP, int MODE, int NC>
+__device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& td, const Item& item,
+                                           const float* __restrict__ P, const float* __restrict__ Q,
+                                           float (*ps)[RP], float* __restrict__ store) {
+  constexpr int CPT = cpt_for(RP);
+  const long long m = td.m;
+  const int c0 = item.col0 + threadIdx.x * CPT;
+  const int cend = item.col0 + item.ncols;
+  float qv[CPT][RP];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    if (c0 + c < cend)
+      load_row<RP>(Q + td.q_off + (long long)(c0 + c) * RP, qv[c]);
+    else
+#pragma unroll
+      for (int k = 0; k < RP; ++k) qv[c][k] = 0.f;
+  }
+  for (int sb = 0; sb < item.nrows; sb += kPStage) {
+    const int rows = min(kPStage, item.nrows - sb);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * RP; idx += kThreads)
+      ps[idx / RP][idx % RP] = P[td.p_off + (long long)(item.row0 + sb) * RP + idx];
+    __syncthreads();
+    if (c0 >= cend) continue;
+#pragma unroll 4
+    for (int i = 0; i < rows; ++i) {
+      const long long row = item.row0 + sb + i;
+      float pr[RP];
+#pragma unroll
+      for (int k = 0; k < RP; ++k) pr[k] = ps[i][k];
+      float o[CPT];
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) o[c] = dot_chain<RP>(pr, qv[c]);
+      if constexpr (NC == CPT && CPT == 4) {
+        if constexpr (MODE == 0) {
+          store_f<4>(a.out + td.g_off + row * m + c0, o);
+        } else if constexpr (MODE == 1) {
+          float s[4];
+          load_f<4>(store + td.c_off + row * m + c0, s, true);
+          float e[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) e[c] = s[c] - o[c];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) a.eio[td.e_off + row * m + c0 + c] = e[c];
+        } else if constexpr (MODE == 2) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) store[td.c_off + row * m + c0 + c] = a.eio[td.e_off + row * m + c0 + c] + o[c];
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) store[td.c_off + row * m + c0 + c] -= o[c];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          if (c0 + c >= cend) continue;
+          const long long idx = row * m + c0 + c;
+          if constexpr (MODE == 0) {
+            st_stream1(a.out + td.g_off + idx, o[c]);
+          } else if constexpr (MODE == 1) {
+            a.eio[td.e_off + idx] = store[td.c_off + idx] - o[c];
+          } else if constexpr (MODE == 2) {
+            store[td.c_off + idx] = a.eio[td.e_off + idx] + o[c];
+          } else {
+            store[td.c_off + idx] -= o[c];
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int RP, int MODE>
+__global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
+  __shared__ __align__(16) float ps[kPStage][RP];
+  if (MODE == 0 && a.ctrl->flag) return;
+  // MODE 0 reads the factors just computed (next half); the error views read
+  // the committed half.
+  const int half = (MODE == 0) ? (a.ctrl->cur ^ 1) : a.ctrl->cur;
+  const float* P = a.Pf + (long long)half * a.p_total;
+  const float* Q = a.Qf + (long long)half * a.q_total;
+  float* store = nullptr;
+  if (MODE != 0) store = a.estore + ((long long)a.ctrl->cur * a.W + a.replica) * a.nc_pad;
+  constexpr int CPT = cpt_for(RP);
+  for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+    const Item item = a.items[it];
+    const TensorDesc td = a.tensors[item.t];
+    const bool vec = (MODE == 0) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
+    if (vec && CPT == 4)
+      pass3_tile<RP, MODE, CPT>(a, td, item, P, Q, ps, store);
+    else
+      pass3_tile<RP, MODE, 1>(a, td, item, P, Q, ps, store);
+  }
+}
+
+}  // namespace psgd

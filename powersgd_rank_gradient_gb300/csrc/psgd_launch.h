@@ -1,0 +1,27 @@
+// Host-side launchers of the kernels (one translation unit per padded rank).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "psgd_internal.h"
+
+namespace psgd {
+
+struct StepArgs;
+
+template <int RP> void launch_pass1(const StepArgs& a, int grid, cudaStream_t s);
+template <int RP> void launch_gram(const StepArgs& a, const float* src, float* dense_out, int is_q,
+                                   int from_parts, double* gram, int grid, cudaStream_t s);
+template <int RP> void launch_solve(const StepArgs& a, const double* gram, int is_q, cudaStream_t s);
+template <int RP> void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q,
+                                    int dst_half, int grid, cudaStream_t s);
+template <int RP> void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s);
+template <int RP> void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s);
+template <int RP> void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s);
+
+void launch_mean(const StepArgs& a, const Segment* segs, int nsegs, int grid, cudaStream_t s);
+void launch_commit(Ctrl* ctrl, int compressed, int* status, cudaStream_t s);
+void launch_randn(const StepArgs& a, const int* mask, unsigned long long seed,
+                  unsigned long long counter, int rp, int grid, cudaStream_t s);
+
+}  // namespace psgd

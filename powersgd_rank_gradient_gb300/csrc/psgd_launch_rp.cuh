@@ -1,0 +1,89 @@
+// Definitions of the per-rank launchers; included once per padded rank RP by
+// kern_rp<RP>.cu, which instantiates them.
+#pragma once
+
+#include "psgd_kernels.cuh"
+#include "psgd_launch.h"
+
+namespace psgd {
+
+template <int RP>
+void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
+  constexpr int RW = RP <= 8 ? 2 : 1;
+  if (a.f16) {
+    switch (a.W) {
+      case 1: k_pass1<RP, 1, __half, RW><<<grid, kThreads, 0, s>>>(a); break;
+      case 2: k_pass1<RP, 2, __half, RW><<<grid, kThreads, 0, s>>>(a); break;
+      case 4: k_pass1<RP, 4, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 8: k_pass1<RP, 8, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
+      default: k_pass1<RP, 0, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
+    }
+  } else {
+    switch (a.W) {
+      case 1: k_pass1<RP, 1, float, RW><<<grid, kThreads, 0, s>>>(a); break;
+      case 2: k_pass1<RP, 2, float, RW><<<grid, kThreads, 0, s>>>(a); break;
+      case 4: k_pass1<RP, 4, float, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 8: k_pass1<RP, 8, float, 1><<<grid, kThreads, 0, s>>>(a); break;
+      default: k_pass1<RP, 0, float, 1><<<grid, kThreads, 0, s>>>(a); break;
+    }
+  }
+}
+
+template <int RP>
+void launch_gram(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts,
+                 double* gram, int grid, cudaStream_t s) {
+  k_gram<RP><<<grid, kThreads, 0, s>>>(a, src, dense_out, is_q, from_parts, gram);
+}
+
+template <int RP>
+void launch_solve(const StepArgs& a, const double* gram, int is_q, cudaStream_t s) {
+  k_solve<RP><<<a.n_tensors, 32, 0, s>>>(a, gram, is_q, 0);
+}
+
+template <int RP>
+void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q, int dst_half, int grid,
+                  cudaStream_t s) {
+  k_apply<RP><<<grid, kThreads, 0, s>>>(a, src, dst, is_q, dst_half);
+}
+
+template <int RP>
+void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s) {
+  if (src_mode == 0)
+    k_pass2<RP, 0, float><<<grid, kThreads, 0, s>>>(a);
+  else if (src_mode == 1)
+    k_pass2<RP, 1, float><<<grid, kThreads, 0, s>>>(a);
+  else if (a.f16)
+    k_pass2<RP, 2, __half><<<grid, kThreads, 0, s>>>(a);
+  else
+    k_pass2<RP, 2, float><<<grid, kThreads, 0, s>>>(a);
+}
+
+template <int RP>
+void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s) {
+  k_qreduce<RP><<<grid, kThreads, 0, s>>>(a);
+}
+
+template <int RP>
+void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
+  if (mode == 0)
+    k_pass3<RP, 0><<<grid, kThreads, 0, s>>>(a);
+  else if (mode == 1)
+    k_pass3<RP, 1><<<grid, kThreads, 0, s>>>(a);
+  else if (mode == 2)
+    k_pass3<RP, 2><<<grid, kThreads, 0, s>>>(a);
+  else
+    k_pass3<RP, 3><<<grid, kThreads, 0, s>>>(a);
+}
+
+#define PSGD_INSTANTIATE(RPV)                                                                   \
+  template void launch_pass1<RPV>(const StepArgs&, int, cudaStream_t);                          \
+  template void launch_gram<RPV>(const StepArgs&, const float*, float*, int, int, double*, int, \
+                                 cudaStream_t);                                                 \
+  template void launch_solve<RPV>(const StepArgs&, const double*, int, cudaStream_t);           \
+  template void launch_apply<RPV>(const StepArgs&, const float*, float*, int, int, int,         \
+                                  cudaStream_t);                                                \
+  template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
+  template void launch_qreduce<RPV>(const StepArgs&, int, cudaStream_t);                        \
+  template void launch_pass3<RPV>(const StepArgs&, int, int, cudaStream_t);
+
+}  // namespace psgd

@@ -1,0 +1,164 @@
+// Rank-independent kernels: the replica mean of uncompressed elements, the
+// end-of-step commit, and the standard-normal draw of a fresh Q.
+#include <math.h>
+
+#include "psgd_kernels.cuh"
+#include "psgd_launch.h"
+
+namespace psgd {
+
+// out[e] = (1/W) sum_w g_w[e] * s over the listed segments.
+// "DDP Communication Hooks", "PowerSGD Hooks" step 2 (uncompressed tensors
+// are allreduced as a batch, without compression) and the vanilla-allreduce
+// note (every element before start_powerSGD_iter); "Default Communication
+// Hooks", allreduce_hook: the allreduce result is the mean over workers.
+template <int WT, typename GT>
+__global__ void __launch_bounds__(kThreads) k_mean(const StepArgs a, const Segment* __restrict__ segs,
+                                                   int nsegs) {
+  const int W = WT > 0 ? WT : a.W;
+  int bad = 0;
+  for (int it = blockIdx.x; it < nsegs; it += gridDim.x) {
+    const Segment sg = segs[it];
+    int start = 0;
+    if (a.vec_ok && (sg.off % 4 == 0)) {
+      const int n4 = sg.len / 4;
+      for (int j = threadIdx.x; j < n4; j += kThreads) {
+        const long long o = sg.off + 4LL * j;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll(WT > 0 ? WT : 1)
+        for (int w = 0; w < W; ++w) {
+          float v[4];
+          load_grad<4, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + o, v);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float x = v[c] * a.scale;
+            bad |= !isfinite(x);
+            acc[c] += x;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] *= a.invW;
+        store_f<4>(a.out + o, acc);
+      }
+      start = n4 * 4;
+    }
+    for (int j = start + threadIdx.x; j < sg.len; j += kThreads) {
+      const long long o = sg.off + j;
+      float acc = 0.f;
+      for (int w = 0; w < W; ++w) {
+        float v[1];
+        load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + o, v);
+        const float x = v[0] * a.scale;
+        bad |= !isfinite(x);
+        acc += x;
+      }
+      a.out[o] = acc * a.invW;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
+}
+
+void launch_mean(const StepArgs& a, const Segment* segs, int nsegs, int grid, cudaStream_t s) {
+  if (nsegs == 0) return;
+  if (a.f16) {
+    switch (a.W) {
+      case 1: k_mean<1, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 2: k_mean<2, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 4: k_mean<4, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 8: k_mean<8, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      default: k_mean<0, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+    }
+  } else {
+    switch (a.W) {
+      case 1: k_mean<1, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 2: k_mean<2, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 4: k_mean<4, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 8: k_mean<8, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      default: k_mean<0, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+    }
+  }
+}
+
+// End of a step: a step that saw no inf/NaN makes the next half of the
+// double-buffered state current; a skipped step leaves everything as it was
+// (torch.cuda.amp GradScaler: a step with inf/NaN gradients is skipped).
+__global__ void k_commit(Ctrl* ctrl, int compressed, int* status) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    const int bad = ctrl->flag;
+    if (!bad && compressed) {
+      ctrl->cur ^= 1;
+      ctrl->warm_valid = 1;
+    }
+    *status = bad ? 1 : 0;
+  }
+}
+
+void launch_commit(Ctrl* ctrl, int compressed, int* status, cudaStream_t s) {
+  k_commit<<<1, 32, 0, s>>>(ctrl, compressed, status);
+}
+
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror and Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011): each round multiplies counter
+// words 0 and 2 by the round constants, swaps the halves crosswise and mixes
+// in the key, which is bumped by the Weyl constants between rounds.
+struct Philox4 {
+  unsigned int v[4];
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(Philox4 c, unsigned int k0, unsigned int k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const unsigned int lo0 = 0xD2511F53u * c.v[0];
+    const unsigned int hi0 = __umulhi(0xD2511F53u, c.v[0]);
+    const unsigned int lo1 = 0xCD9E8D57u * c.v[2];
+    const unsigned int hi1 = __umulhi(0xCD9E8D57u, c.v[2]);
+    Philox4 n;
+    n.v[0] = hi1 ^ c.v[1] ^ k0;
+    n.v[1] = lo1;
+    n.v[2] = hi0 ^ c.v[3] ^ k1;
+    n.v[3] = lo0;
+    c = n;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Standard-normal draw of Q for the tensors whose mask is set ("PowerSGD
+// Hooks" step 3.1: Q is initialised from a standard normal distribution).
+// Element (j, k) of tensor t uses counter (j * RP + k, t, counter_lo,
+// counter_hi) and key = random_seed; Box-Muller on the first two words.
+__global__ void __launch_bounds__(kThreads) k_randn(const StepArgs a, const int* __restrict__ mask,
+                                                    unsigned long long seed, unsigned long long counter,
+                                                    int rp) {
+  for (int it = blockIdx.x; it < a.n_gsq; it += gridDim.x) {
+    const GsItem gi = a.gsq_items[it];
+    if (!mask[gi.t]) continue;
+    const TensorDesc td = a.tensors[gi.t];
+    for (int idx = threadIdx.x; idx < gi.nrows * rp; idx += kThreads) {
+      const long long j = gi.row0 + idx / rp;
+      const int k = idx % rp;
+      float z = 0.f;
+      if (k < td.r) {
+        Philox4 c;
+        const unsigned long long e = (unsigned long long)j * rp + k;
+        c.v[0] = (unsigned int)e;
+        c.v[1] = (unsigned int)(e >> 32) ^ ((unsigned int)gi.t << 8);
+        c.v[2] = (unsigned int)counter;
+        c.v[3] = (unsigned int)(counter >> 32);
+        const Philox4 o = philox4x32_10(c, (unsigned int)seed, (unsigned int)(seed >> 32));
+        const float u1 = ((float)o.v[0] + 1.0f) * 2.3283064365386963e-10f;  // (0, 1]
+        const float u2 = (float)o.v[1] * 2.3283064365386963e-10f;           // [0, 1)
+        z = sqrtf(-2.0f * logf(u1)) * cosf(6.283185307179586f * u2);
+      }
+      a.qdraw[td.q_off + j * rp + k] = z;
+    }
+  }
+}
+
+void launch_randn(const StepArgs& a, const int* mask, unsigned long long seed,
+                  unsigned long long counter, int rp, int grid, cudaStream_t s) {
+  k_randn<<<grid, kThreads, 0, s>>>(a, mask, seed, counter, rp);
+}
+
+}  // namespace psgd

@@ -1,0 +1,186 @@
+"""Python face of the library: ``PowerSGDState`` and ``powerSGD_hook``.
+
+Names and defaults follow "DDP Communication Hooks" (PyTorch 1.11 docs),
+"PowerSGD State": ``PowerSGDState(process_group, matrix_approximation_rank=1,
+start_powerSGD_iter=1000, min_compression_rate=2, use_error_feedback=True,
+warm_start=True, orthogonalization_epsilon=0, random_seed=0, ...)`` plus
+``batch_tensors_with_same_shape`` from the later page.  The process group is
+replaced by ``world_size`` simulated replicas on one GPU.  torch is used only
+for device memory and streams; every step of the method runs in the CUDA
+kernels of libpsgd.so.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import PSGD_F16, PSGD_F32, PSGD_SKIPPED_NONFINITE, check
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class PowerSGDState:
+    """Hyper-parameters and device state of the hook for one bucket layout."""
+
+    def __init__(self, shapes, world_size, matrix_approximation_rank=1, start_powerSGD_iter=1000,
+                 min_compression_rate=2, use_error_feedback=True, warm_start=True,
+                 orthogonalization_epsilon=0.0, random_seed=0, batch_tensors_with_same_shape=False,
+                 grad_dtype=torch.float32, device=None):
+        if device is None:
+            device = torch.cuda.current_device()
+        device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        if grad_dtype not in (torch.float32, torch.float16):
+            raise ValueError("grad_dtype must be torch.float32 or torch.float16")
+        self.shapes = [tuple(int(d) for d in s) for s in shapes]
+        self.world_size = int(world_size)
+        self.matrix_approximation_rank = int(matrix_approximation_rank)
+        self.start_powerSGD_iter = int(start_powerSGD_iter)
+        self.min_compression_rate = float(min_compression_rate)
+        self.use_error_feedback = bool(use_error_feedback)
+        self.warm_start = bool(warm_start)
+        self.orthogonalization_epsilon = float(orthogonalization_epsilon)
+        self.random_seed = int(random_seed)
+        self.batch_tensors_with_same_shape = bool(batch_tensors_with_same_shape)
+        self.grad_dtype = grad_dtype
+        self.device = device
+        self.numel = sum(_numel(s) for s in self.shapes)
+        L = _lib.lib()
+        d, n = _lib.shape_arrays(self.shapes)
+        handle = ctypes.c_void_p()
+        check(L.psgd_state_create(
+            d, n, len(self.shapes), self.world_size, self.matrix_approximation_rank,
+            self.start_powerSGD_iter, self.min_compression_rate, int(self.use_error_feedback),
+            int(self.warm_start), self.orthogonalization_epsilon, self.random_seed & (2**64 - 1),
+            int(self.batch_tensors_with_same_shape),
+            PSGD_F16 if grad_dtype == torch.float16 else PSGD_F32, device.index or 0,
+            ctypes.byref(handle)))
+        self._h = handle
+        self._lib = L
+
+    # -- lifetime -------------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            self._lib.psgd_state_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- the hook -------------------------------------------------------------
+    def step(self, grads, out=None, inv_loss_scale=1.0, stream=None):
+        """Enqueue one hook call on the W replica buckets; returns ``out``."""
+        if len(grads) != self.world_size:
+            raise ValueError(f"expected {self.world_size} replica buckets, got {len(grads)}")
+        for g in grads:
+            if not (g.is_cuda and g.dtype == self.grad_dtype and g.is_contiguous() and g.numel() == self.numel):
+                raise ValueError("each replica bucket must be a contiguous CUDA tensor of "
+                                 f"{self.numel} {self.grad_dtype} elements")
+        if out is None:
+            out = torch.empty(self.numel, dtype=torch.float32, device=self.device)
+        if not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous() and out.numel() == self.numel):
+            raise ValueError("out must be a contiguous CUDA float32 tensor of the bucket's size")
+        ptrs = (ctypes.c_void_p * self.world_size)(*[g.data_ptr() for g in grads])
+        check(self._lib.psgd_step(self._h, ptrs, ctypes.c_void_p(out.data_ptr()), float(inv_loss_scale),
+                                  _stream_ptr(stream)))
+        return out
+
+    def step_host(self, host_grads, host_out, inv_loss_scale=1.0, stream=None):
+        """psgd_step_host: host (ideally pinned) CPU tensors in and out."""
+        ptrs = (ctypes.c_void_p * self.world_size)(*[g.data_ptr() for g in host_grads])
+        check(self._lib.psgd_step_host(self._h, ptrs, ctypes.c_void_p(host_out.data_ptr()),
+                                       float(inv_loss_scale), _stream_ptr(stream)))
+        return host_out
+
+    def status(self, stream=None):
+        """Synchronises and returns True when the last step was skipped (inf/NaN)."""
+        rc = check(self._lib.psgd_step_status(self._h, _stream_ptr(stream)))
+        return rc == PSGD_SKIPPED_NONFINITE
+
+    # -- introspection ----------------------------------------------------------
+    def stats(self):
+        b, a, it = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        check(self._lib.psgd_get_stats(self._h, ctypes.byref(b), ctypes.byref(a), ctypes.byref(it)))
+        return b.value, a.value, it.value
+
+    def tensor_info(self, t):
+        c, r, k = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+        rows, cols, boff, poff = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        check(self._lib.psgd_tensor_info(self._h, int(t), ctypes.byref(c), ctypes.byref(rows),
+                                         ctypes.byref(cols), ctypes.byref(r), ctypes.byref(boff),
+                                         ctypes.byref(poff)))
+        return dict(compressed=bool(c.value), rows=rows.value, cols=cols.value, rank=r.value,
+                    bucket_offset=boff.value, packed_offset=poff.value)
+
+    def error_numel(self):
+        return int(self._lib.psgd_error_numel(self._h))
+
+    def workspace_bytes(self):
+        return int(self._lib.psgd_workspace_bytes(self._h))
+
+    def set_q(self, t, q, is_draw=True):
+        q = torch.as_tensor(q, dtype=torch.float32).contiguous().cpu()
+        check(self._lib.psgd_set_q(self._h, int(t), ctypes.c_void_p(q.data_ptr()), int(is_draw)))
+
+    def get_q(self, t):
+        info = self.tensor_info(t)
+        out = torch.empty(info["cols"], info["rank"], dtype=torch.float32)
+        check(self._lib.psgd_get_q(self._h, int(t), ctypes.c_void_p(out.data_ptr())))
+        return out
+
+    def get_p(self, t):
+        info = self.tensor_info(t)
+        out = torch.empty(info["rows"], info["rank"], dtype=torch.float32)
+        check(self._lib.psgd_get_p(self._h, int(t), ctypes.c_void_p(out.data_ptr())))
+        return out
+
+    def get_error(self, replica, out=None, stream=None):
+        n = self.error_numel()
+        if out is None:
+            out = torch.empty(max(1, n), dtype=torch.float32, device=self.device)
+        check(self._lib.psgd_get_error(self._h, int(replica), ctypes.c_void_p(out.data_ptr()),
+                                       _stream_ptr(stream)))
+        return out[:n]
+
+    def set_error(self, replica, e, stream=None):
+        e = e.to(device=self.device, dtype=torch.float32).contiguous()
+        check(self._lib.psgd_set_error(self._h, int(replica), ctypes.c_void_p(e.data_ptr()),
+                                       _stream_ptr(stream)))
+
+    # -- measurement ------------------------------------------------------------
+    def profile(self, enable=True):
+        check(self._lib.psgd_profile(self._h, int(enable)))
+
+    def profile_read(self):
+        """{kind: (launches, total_ms, algorithmic bytes per launch)} since the last read."""
+        res = {}
+        for k in range(self._lib.psgd_profile_kinds()):
+            name = ctypes.c_char_p()
+            n = ctypes.c_int64()
+            ms = ctypes.c_double()
+            by = ctypes.c_double()
+            check(self._lib.psgd_profile_read(self._h, k, ctypes.byref(name), ctypes.byref(n),
+                                              ctypes.byref(ms), ctypes.byref(by)))
+            res[name.value.decode()] = (n.value, ms.value, by.value)
+        return res
+
+
+def powerSGD_hook(state, grads, out=None, inv_loss_scale=1.0, stream=None):
+    """One hook call ("PowerSGD Hooks", powerSGD_hook) on the W replica buckets."""
+    return state.step(grads, out=out, inv_loss_scale=inv_loss_scale, stream=stream)
+
+
+def _numel(shape):
+    n = 1
+    for d in shape:
+        n *= int(d)
+    return n

@@ -1,0 +1,305 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, every step, tensor by tensor.
+
+Sizes are ones the oracle finishes in seconds but that still span several
+column tiles and row blocks with ragged tails, unaligned tensors (odd column
+counts, odd bucket offsets), every padded rank and several replica counts.
+"""
+
+import numpy as np
+import pytest
+
+from parity_util import Pair, grads_for, rel
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+# A bucket with: multiple column tiles (1100, 2100 > 1024 columns), multiple
+# row blocks with a ragged tail (1030 > 2 * 512 rows), an odd-sized vector in
+# front of a matrix (unaligned bucket offset), an odd column count (147), a
+# 4-D conv view and vectors.
+MIXED = [(700, 1100), (1100,), (3,), (1030, 64), (64, 3, 7, 7), (256,),
+         (33, 8, 3, 3), (5,), (40, 2100), (17, 16)]
+
+
+def _run(shapes, world, rank, steps, heavy=0.0, std=1.0, label="", **kw):
+    kw.setdefault("start_powerSGD_iter", 0)
+    kw.setdefault("min_compression_rate", 1.0)
+    pair = Pair(shapes, world, rank, DEV, **kw)
+    worst = {"out": 0.0, "err": 0.0, "orth": 0.0}
+    for step in range(steps):
+        g = grads_for(shapes, world, step, std=std, heavy=heavy)
+        skipped, status, out, exp = pair.step(g)
+        assert not skipped
+        w = pair.compare(out, exp, label=f"{label} step {step}")
+        worst = {k: max(worst[k], w[k]) for k in worst}
+    pair.close()
+    return worst
+
+
+def test_config1_256x512_rank1_two_steps():
+    """256x512, N(0,1) from seed 0, W=1, r=1, zero error buffer, Q drawn
+    N(0,1) from seed 1, eps=0, 2 warm-started steps on the same gradient."""
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+    import oracle
+
+    shapes = [(256, 512)]
+    g = np.random.default_rng(0).standard_normal(256 * 512).astype(np.float32)
+    q = np.random.default_rng(1).standard_normal((512, 1)).astype(np.float32)
+    st = PowerSGDState(shapes, 1, matrix_approximation_rank=1, start_powerSGD_iter=0, device=DEV)
+    ref = oracle.PowerSGDOracle(shapes=shapes, world_size=1, matrix_approximation_rank=1,
+                                start_powerSGD_iter=0)
+    st.set_q(0, q, is_draw=True)
+    ref.set_q_draw(0, q.astype(np.float64))
+    for step in range(2):
+        out = st.step([torch.from_numpy(g).to(DEV)])
+        assert not st.status()
+        _, exp = ref.step([g.astype(np.float64)])
+        assert rel(out.double().cpu().numpy(), exp) <= 1e-4
+        e = st.get_error(0).double().cpu().numpy()
+        assert rel(e, ref.error_of(0, 0).reshape(-1)) <= 1e-4
+        p = st.get_p(0).double().numpy()
+        assert abs(float(p.T @ p) - 1.0) <= 1e-4
+        assert rel(p[:, 0], ref.last_p[0][:, 0]) <= 1e-4
+        assert rel(st.get_q(0).double().numpy(), ref.q[0]) <= 1e-4
+    st.close()
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 8])
+def test_mixed_bucket_worlds(world):
+    _run(MIXED, world, 4, 3, label=f"W={world}")
+
+
+@pytest.mark.parametrize("rank", [1, 2, 3, 5, 8, 16, 32])
+def test_mixed_bucket_ranks(rank):
+    _run(MIXED, 2, rank, 3, min_compression_rate=0.25, label=f"r={rank}")
+
+
+def test_heavy_rows_batched():
+    _run(MIXED, 8, 4, 4, heavy=0.01, std=1e-3, batch_tensors_with_same_shape=True, label="heavy")
+
+
+def test_vanilla_phase_then_compression():
+    _run(MIXED, 3, 2, 4, start_powerSGD_iter=2, label="start=2")
+
+
+def test_no_error_feedback():
+    for world in (1, 2, 5):
+        _run(MIXED, world, 4, 3, use_error_feedback=False, label=f"noEF W={world}")
+
+
+def test_no_warm_start_fresh_draw_each_step():
+    shapes = MIXED
+    pair = Pair(shapes, 2, 4, DEV, start_powerSGD_iter=0, min_compression_rate=1.0,
+                warm_start=False)
+    for step in range(3):
+        if step > 0:
+            pair.inject_draws(seed=10 + step)
+        skipped, status, out, exp = pair.step(grads_for(shapes, 2, step))
+        pair.compare(out, exp, label=f"cold step {step}")
+    pair.close()
+
+
+def test_epsilon_positive():
+    _run(MIXED, 2, 4, 3, orthogonalization_epsilon=1e-8, label="eps")
+
+
+def test_zero_columns_with_epsilon():
+    """4096x1024 gradient, r=8, eps=1e-8: the first three columns of Q live on
+    coordinates where the gradient is zero, so three columns of P are exactly
+    zero.  They must stay zero with no NaN, and P^T P = diag(0,0,0,1,...)."""
+    import oracle
+
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    n, m, r = 4096, 1024, 8
+    rng = np.random.default_rng(5)
+    zero_cols = np.sort(rng.permutation(m)[:3])
+    g = rng.standard_normal((n, m)).astype(np.float32)
+    g[:, zero_cols] = 0.0
+    draw = rng.standard_normal((m, r)).astype(np.float32)
+    draw[:, :3] = 0.0
+    draw[zero_cols, np.arange(3)] = 1.0
+    st = PowerSGDState([(n, m)], 1, matrix_approximation_rank=r, start_powerSGD_iter=0,
+                       orthogonalization_epsilon=1e-8, device=DEV)
+    ref = oracle.PowerSGDOracle(shapes=[(n, m)], world_size=1, matrix_approximation_rank=r,
+                                start_powerSGD_iter=0, orthogonalization_epsilon=1e-8)
+    st.set_q(0, draw, is_draw=True)
+    ref.set_q_draw(0, draw.astype(np.float64))
+    for step in range(2):
+        out = st.step([torch.from_numpy(g.reshape(-1)).to(DEV)])
+        _, exp = ref.step([g.reshape(-1).astype(np.float64)])
+        got = out.double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        assert rel(got, exp) <= 1e-4
+        p = st.get_p(0).double().numpy()
+        assert np.all(np.isfinite(p))
+        assert np.all(p[:, :3] == 0.0)
+        assert np.abs(p.T @ p - np.diag([0, 0, 0, 1, 1, 1, 1, 1])).max() <= 1e-4
+        e = st.get_error(0).double().cpu().numpy()
+        assert rel(e, ref.error_of(0, 0).reshape(-1)) <= 1e-4
+    st.close()
+
+
+def test_fp16_scaled_with_inf_is_skipped():
+    """fp16 gradients pre-scaled by 65536 and unscaled in pass 1; a step with
+    one +inf is skipped with the state left bit for bit, the next clean step
+    matches the oracle."""
+    shapes = [(512, 768), (768,), (256, 256)]
+    world = 2
+    pair = Pair(shapes, world, 4, DEV, grad_dtype=torch.float16, start_powerSGD_iter=0,
+                min_compression_rate=1.0)
+    s = 1.0 / 65536.0
+    g0 = grads_for(shapes, world, 0, std=1e-3, dtype=np.float16, scale=65536.0)
+    skipped, status, out, exp = pair.step(g0, inv_loss_scale=s)
+    assert not skipped
+    pair.compare(out, exp, label="fp16 step 0")
+    before = ([pair.gpu.get_error(w).cpu().clone() for w in range(world)],
+              [pair.gpu.get_q(t).clone() for t in (0, 2)], [pair.gpu.get_p(t).clone() for t in (0, 2)])
+    g1 = grads_for(shapes, world, 1, std=1e-3, dtype=np.float16, scale=65536.0)
+    idx = np.random.default_rng(9).integers(g1[1].size)
+    g1[1][idx] = np.float16(np.inf)
+    skipped, status, out, exp = pair.step(g1, inv_loss_scale=s)
+    assert skipped and status == "skipped"
+    after = ([pair.gpu.get_error(w).cpu() for w in range(world)],
+             [pair.gpu.get_q(t) for t in (0, 2)], [pair.gpu.get_p(t) for t in (0, 2)])
+    for xs, ys in zip(before, after):
+        for x, y in zip(xs, ys):
+            assert torch.equal(x, y)
+    g2 = grads_for(shapes, world, 2, std=1e-3, dtype=np.float16, scale=65536.0)
+    skipped, status, out, exp = pair.step(g2, inv_loss_scale=s)
+    assert not skipped
+    pair.compare(out, exp, label="fp16 step 2")
+    pair.close()
+
+
+def test_nan_in_fp32_is_skipped():
+    shapes = [(300, 200), (7,)]
+    pair = Pair(shapes, 2, 2, DEV, start_powerSGD_iter=0, min_compression_rate=1.0)
+    skipped, _, out, exp = pair.step(grads_for(shapes, 2, 0))
+    pair.compare(out, exp)
+    g = grads_for(shapes, 2, 1)
+    g[0][300 * 200 + 3] = np.nan      # in the uncompressed vector
+    skipped, status, _, _ = pair.step(g)
+    assert skipped and status == "skipped"
+    skipped, _, out, exp = pair.step(grads_for(shapes, 2, 2))
+    assert not skipped
+    pair.compare(out, exp)
+    pair.close()
+
+
+def test_batch_flag_bit_identical():
+    outs = []
+    for flag in (False, True):
+        from powersgd_rank_gradient_gb300 import PowerSGDState
+
+        shapes = [(300, 200), (300, 200), (9,), (300, 200), (128, 64)]
+        st = PowerSGDState(shapes, 2, matrix_approximation_rank=4, start_powerSGD_iter=0,
+                           min_compression_rate=1.0, batch_tensors_with_same_shape=flag,
+                           random_seed=7, device=DEV)
+        res = []
+        for step in range(3):
+            g = [torch.from_numpy(x).to(DEV) for x in grads_for(shapes, 2, step)]
+            res.append(st.step(g).cpu().clone())
+        res.append(st.get_error(1).cpu().clone())
+        outs.append(res)
+        st.close()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_deterministic_and_out_aliases_grads0():
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = MIXED
+    runs = []
+    for alias in (False, True):
+        st = PowerSGDState(shapes, 2, matrix_approximation_rank=4, start_powerSGD_iter=0,
+                           min_compression_rate=1.0, random_seed=3, device=DEV)
+        res = []
+        for step in range(3):
+            g = [torch.from_numpy(x).to(DEV) for x in grads_for(shapes, 2, step)]
+            out = st.step(g, out=g[0] if alias else None)
+            res.append(out.cpu().clone())
+        runs.append(res)
+        st.close()
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)
+
+
+def test_error_set_get_roundtrip_and_warm_q_restore():
+    """Checkpoint: copy the residuals and the warm Q of one state into a fresh
+    one; both then produce the same next step (to fp32 rounding)."""
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = [(400, 300), (11,), (129, 64)]
+    kw = dict(matrix_approximation_rank=3, start_powerSGD_iter=0, min_compression_rate=1.0,
+              device=DEV)
+    a = PowerSGDState(shapes, 2, random_seed=1, **kw)
+    for step in range(2):
+        a.step([torch.from_numpy(x).to(DEV) for x in grads_for(shapes, 2, step)])
+    b = PowerSGDState(shapes, 2, random_seed=99, **kw)
+    for w in range(2):
+        b.set_error(w, a.get_error(w))
+    for t in (0, 2):
+        b.set_q(t, a.get_q(t), is_draw=False)
+    for w in range(2):
+        assert rel(b.get_error(w).double().cpu().numpy(), a.get_error(w).double().cpu().numpy()) < 1e-6
+    g = [torch.from_numpy(x).to(DEV) for x in grads_for(shapes, 2, 5)]
+    oa = a.step(g).double().cpu().numpy()
+    ob = b.step(g).double().cpu().numpy()
+    assert rel(ob, oa) < 1e-5
+    a.close()
+    b.close()
+
+
+def test_library_draw_statistics():
+    """The library's own standard-normal draw (no injected Q): after the first
+    step P is orthonormal and the stats counters match the plan."""
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = [(2048, 1024)]
+    st = PowerSGDState(shapes, 1, matrix_approximation_rank=8, start_powerSGD_iter=0, device=DEV,
+                       random_seed=1234)
+    st.step([torch.from_numpy(grads_for(shapes, 1, 0)[0]).to(DEV)])
+    assert not st.status()
+    p = st.get_p(0).double().numpy()
+    assert np.abs(p.T @ p - np.eye(8)).max() < 1e-4
+    before, after, it = st.stats()
+    assert (before, after, it) == (2048 * 1024, (2048 + 1024) * 8, 1)
+    st.close()
+
+
+def test_invalid_arguments_are_rejected():
+    from powersgd_rank_gradient_gb300 import PowerSGDState, _lib
+
+    with pytest.raises(_lib.PsgdError):
+        PowerSGDState([(4, 4)], 1, matrix_approximation_rank=0, device=DEV)
+    with pytest.raises(_lib.PsgdError):
+        PowerSGDState([(4, 4)], 65, device=DEV)
+    st = PowerSGDState([(64, 64), (8,)], 2, matrix_approximation_rank=2, start_powerSGD_iter=0,
+                       min_compression_rate=1.0, device=DEV)
+    g = [torch.zeros(64 * 64 + 8, device=DEV) for _ in range(2)]
+    with pytest.raises(_lib.PsgdError):
+        st.step(g, out=g[1])          # out may alias only replica 0
+    with pytest.raises(_lib.PsgdError):
+        st.set_q(1, np.zeros((1, 1), np.float32))   # vector tensor is not compressed
+    st.close()
+
+
+def test_empty_and_vector_only_buckets():
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    st = PowerSGDState([(7,), (0, 5), (3,)], 2, start_powerSGD_iter=0, device=DEV)
+    g = [torch.arange(10, dtype=torch.float32, device=DEV) * (w + 1) for w in range(2)]
+    out = st.step(g)
+    assert torch.allclose(out, (g[0] + g[1]) / 2)
+    st.close()
+
+
+@pytest.mark.parametrize("rank", [1, 2, 4, 8, 16, 32])
+def test_rank_sweep_8192(rank):
+    """8192 x 8192, W=1, N(0,1): two warm-started steps per rank."""
+    _run([(8192, 8192)], 1, rank, 2, min_compression_rate=2.0, label=f"8192 r={rank}")
