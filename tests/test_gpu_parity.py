@@ -61,7 +61,7 @@ def test_config1_256x512_rank1_two_steps():
         e = st.get_error(0).double().cpu().numpy()
         assert rel(e, ref.error_of(0, 0).reshape(-1)) <= 1e-4
         p = st.get_p(0).double().numpy()
-        assert abs(float(p.T @ p) - 1.0) <= 1e-4
+        assert abs(float((p.T @ p)[0, 0]) - 1.0) <= 1e-4
         assert rel(p[:, 0], ref.last_p[0][:, 0]) <= 1e-4
         assert rel(st.get_q(0).double().numpy(), ref.q[0]) <= 1e-4
     st.close()
