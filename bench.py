@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark of the PowerSGD hook step on GB300.
+
+Metric: PowerSGD step throughput as gradient GB/s (W replica buckets of N
+fp32 elements consumed per step, W * N * 4 bytes / step time), with the HBM
+roofline fraction of the dominant kernel.  One step = one psgd_step call in
+the compressed phase (warm-started Q): error feedback + unscale + replica
+mean + P = M Q, Gram-Schmidt, Q = M^T P, decompression, on every tensor of
+the bucket.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Multi-GPU: the path simulates its W data-parallel replicas inside one GPU and
+does not shard, so N GPUs run N independent replicas of the workload
+(weak scaling); the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PowerSGD step throughput, gradient GB/s and % of HBM roofline (1 GB300)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bert-large",
+                    choices=["bert-large", "gpt2-xl", "resnet50", "rank-sweep"])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--extra", default="gpt2-xl",
+                    help="comma-separated workloads also measured and reported under 'workloads'")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling cases: only this many transformer layers, no embeddings")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def workload_spec(name, rank_override=None, layers=None):
+    from powersgd_rank_gradient_gb300 import workloads as wl
+
+    if name == "rank-sweep":
+        return dict(name="rank-sweep-8192", shapes=[(8192, 8192)], world_size=1,
+                    rank=rank_override or 8, mcr=2.0, std=1.0, heavy=0.0, batch_same_shape=False)
+    w = wl.WORKLOADS[name]
+    if layers is not None and name in ("bert-large", "gpt2-xl"):
+        shapes = w["shapes"](layers=layers, embeddings=False)
+        name = f"{name}-{layers}layers"
+    else:
+        shapes = w["shapes"]()
+    return dict(name=name, shapes=shapes, world_size=w["world_size"], rank=w["rank"],
+                mcr=w["mcr"], std=w["std"], heavy=w["heavy"], batch_same_shape=w["batch_same_shape"])
+
+
+def plan_counts(spec):
+    from powersgd_rank_gradient_gb300 import _lib
+
+    comp, ranks, rows, cols = _lib.plan(spec["shapes"], spec["rank"], spec["mcr"])
+    numels = []
+    for s in spec["shapes"]:
+        n = 1
+        for d in s:
+            n *= d
+        numels.append(n)
+    nc = sum(n for n, c in zip(numels, comp) if c)
+    return dict(N=sum(numels), Nc=nc, Nunc=sum(numels) - nc, compressed=sum(comp),
+                tensors=len(numels),
+                pq=sum((r + c) * k for r, c, k, cc in zip(rows, cols, ranks, comp) if cc))
+
+
+def step_bytes(spec, counts, gsz=4):
+    """Bytes one step must move.  'design' is this implementation's
+    three-pass schedule with the factored residual; 'survey_min' is the
+    explicit-residual minimum min(6W+1, 5W+3) * 4 bytes per compressed element
+    (the bound the targets are quoted against)."""
+    W = spec["world_size"]
+    nc, nu = counts["Nc"], counts["Nunc"]
+    mbar = W * 4 > 8
+    p1 = W * (gsz + 8) + (4 if mbar else 0)
+    p2 = 4 if mbar else 4 * W
+    design = nc * (p1 + p2 + 4) + nu * (W * gsz + 4)
+    survey = nc * min(6 * W + 1, 5 * W + 3) * 4 + nu * (W * gsz + 4) + (W + 1) * counts["pq"] * 4
+    return dict(design=design, survey_min=survey)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_src_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "powersgd_rank_gradient_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("src_hash") != kernel_src_hash():
+        return None
+    ent = d.get("workloads", {}).get(workload, {}).get(kernel)
+    return None if ent is None else float(ent)
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            if r["hw"].lower().startswith("active"):
+                reasons.add("hw_slowdown")
+            if r["hwt"].lower().startswith("active"):
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"].lower().startswith("active"):
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"].lower().startswith("active"):
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+def run_native(spec, args, dist, rank_id, world, device):
+    import torch
+
+    from powersgd_rank_gradient_gb300 import PowerSGDState, workloads as wl
+
+    W = spec["world_size"]
+    counts = plan_counts(spec)
+    N = counts["N"]
+    st = PowerSGDState(spec["shapes"], W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
+                       min_compression_rate=spec["mcr"], use_error_feedback=True, warm_start=True,
+                       batch_tensors_with_same_shape=spec["batch_same_shape"], random_seed=0,
+                       device=device)
+    # two resident input sets (W replica buckets each), alternated step to step
+    sets = []
+    for k in range(2):
+        sets.append([wl.gaussian_bucket_torch(spec["shapes"], spec["std"], wl.replica_seed(w, k), device,
+                                              heavy_fraction=spec["heavy"]) for w in range(W)])
+    out = torch.empty(N, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    # the clock sampler runs from the warm-up through the timed region
+    clocks = Clocks(device.index)
+    if rank_id == 0:
+        clocks.start()
+    for i in range(args.warmup):
+        st.step(sets[i % 2], out=out)
+    if st.status():
+        raise RuntimeError("warm-up step was skipped (non-finite input)")
+    torch.cuda.synchronize(device)
+    st.profile_read()  # discard warm-up records
+    st.profile(True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        st.step(sets[i % 2], out=out)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if rank_id == 0 else None
+    st.profile(False)
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if st.status():
+        raise RuntimeError("timed step was skipped (non-finite input)")
+    prof = st.profile_read()
+    ms_step = ms / args.steps
+    grad_bytes = W * N * 4
+    value = grad_bytes * args.steps * world / (ms / 1e3) / 1e9
+    launches = sum(v[0] for v in prof.values())
+    # dominant kernel by device time
+    kern = max((k for k in prof if prof[k][0] > 0), key=lambda k: prof[k][1])
+    n_l, tot_ms, bpl = prof[kern]
+    peak, peak_kind = load_peaks()
+    achieved = bpl / (tot_ms / n_l / 1e3) / 1e9 if n_l and bpl else None
+    kernels = {k: {"launches": v[0], "avg_us": (v[1] / v[0] * 1e3) if v[0] else None,
+                   "share": v[1] / max(1e-12, sum(x[1] for x in prof.values())),
+                   "algo_bytes_per_launch": v[2] or None,
+                   "gbs": (v[2] / (v[1] / v[0] / 1e3) / 1e9) if v[0] and v[2] else None}
+               for k, v in prof.items() if v[0]}
+    sb = step_bytes(spec, counts)
+    res = dict(
+        value=value, ms_per_step=ms_step, grad_bytes=grad_bytes, launches=launches, clocks=clk,
+        roofline={"bound": "hbm", "kernel": kern, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                  "frac": (achieved / peak) if achieved else None, "peak_source": peak_kind,
+                  "traffic": ncu_traffic(spec["name"], kern)},
+        step_roofline={"design_bytes": sb["design"], "design_gbs": sb["design"] / (ms_step / 1e3) / 1e9,
+                       "design_frac_of_measured": sb["design"] / (ms_step / 1e3) / 1e9 / peak,
+                       "survey_min_bytes": sb["survey_min"],
+                       "survey_min_frac_of_nominal_8tbs": sb["survey_min"] / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                       "survey_min_frac_of_measured": sb["survey_min"] / (ms_step / 1e3) / 1e9 / peak},
+        kernels=kernels, counts=counts)
+    del sets
+    torch.cuda.empty_cache()
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(st, spec, args, dist, device, N, W)
+    st.close()
+    return res
+
+
+def run_e2e(st, spec, args, dist, device, N, W):
+    """Same metric through psgd_step_host: every step copies the W pinned host
+    buckets to the device and reads the result back."""
+    import torch
+
+    from powersgd_rank_gradient_gb300 import workloads as wl
+
+    host = []
+    for w in range(W):
+        g = wl.gaussian_bucket_torch(spec["shapes"], spec["std"], wl.replica_seed(w, 7), device,
+                                     heavy_fraction=spec["heavy"])
+        h = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        h.copy_(g)
+        host.append(h)
+        del g
+    host_out = torch.empty(N, dtype=torch.float32, pin_memory=True)
+    stream = torch.cuda.current_stream(device)
+    st.step_host(host, host_out)  # allocates the staging buffers
+    torch.cuda.synchronize(device)
+    k = max(3, min(args.steps, 10))
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k):
+        st.step_host(host, host_out)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        ws = dist.get_world_size()
+    else:
+        ws = 1
+    return {"value": W * N * 4 * k * ws / (ms / 1e3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": W * N * 4, "d2h_bytes_per_step": N * 4, "ms_per_step": ms / k}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(spec, budget):
+    """A window of the bucket's tensors (skipping any tensor larger than the
+    budget) with at most `budget` elements."""
+    sel = []
+    tot = 0
+    for s in spec["shapes"]:
+        n = 1
+        for d in s:
+            n *= d
+        if n > budget:
+            continue
+        if tot + n > budget:
+            break
+        sel.append(s)
+        tot += n
+    return sel, tot
+
+
+def time_oracle(spec, steps, budget=None, target_s=None, warmup=1):
+    import numpy as np
+
+    import oracle
+    from powersgd_rank_gradient_gb300 import workloads as wl
+
+    W = spec["world_size"]
+    if budget is None:
+        budget = 2_000_000 if W >= 8 else 6_000_000
+    shapes, n = oracle_sample(spec, budget)
+    if not shapes:
+        shapes, n = spec["shapes"][:1], 1
+        for d in spec["shapes"][0]:
+            n *= d
+    o = oracle.PowerSGDOracle(shapes=shapes, world_size=W, matrix_approximation_rank=spec["rank"],
+                              start_powerSGD_iter=0, min_compression_rate=spec["mcr"])
+    grads = [wl.gaussian_bucket_np(shapes, spec["std"], wl.replica_seed(w, 0),
+                                   heavy_fraction=spec["heavy"]) for w in range(W)]
+    for _ in range(max(1, warmup)):
+        o.step(grads)  # untimed (the first one draws Q)
+    times = []
+    t_start = time.perf_counter()
+    for i in range(steps):
+        t0 = time.perf_counter()
+        o.step(grads)
+        times.append(time.perf_counter() - t0)
+        if target_s is not None and time.perf_counter() - t_start > target_s:
+            break
+    t = statistics.median(times)
+    return dict(value=W * n * 4 / t / 1e9, unit=UNIT, cores=os.cpu_count(), kind="oracle",
+                sample=f"{len(shapes)} tensors ({n} elements per replica, W={W}) of the {spec['name']} "
+                       f"bucket, fp64 NumPy, median of {len(times)} steps",
+                s_per_step=t)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank_id = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = workload_spec(args.workload, layers=args.layers)
+    base_cfg = {"workload": spec["name"], "world_size_W": spec["world_size"],
+                "matrix_approximation_rank": spec["rank"], "min_compression_rate": spec["mcr"],
+                "start_powerSGD_iter": 0, "use_error_feedback": True, "warm_start": True,
+                "batch_tensors_with_same_shape": spec["batch_same_shape"],
+                "gradients": f"N(0,{spec['std']}) fp32" + (f", {spec['heavy']:.0%} heavy rows x100" if spec["heavy"] else ""),
+                "l2": "inputs larger than L2 (each step reads >10 GB)" if spec["name"] != "resnet50" else "inputs larger than L2",
+                "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank_id != 0:
+            return
+        cb = time_oracle(spec, args.steps, warmup=args.warmup, target_s=120.0)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["s_per_step"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": base_cfg,
+                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl")
+        dist = tdist
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from powersgd_rank_gradient_gb300 import _lib
+
+    _lib.lib()
+
+    res = run_native(spec, args, dist, rank_id, world, device)
+    extras = {}
+    for name in [x for x in args.extra.split(",") if x and x not in ("none", args.workload)]:
+        sp = workload_spec(name, layers=args.layers)
+        r = run_native(sp, args, dist, rank_id, world, device)
+        extras[sp["name"]] = {"value": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
+                              "step_roofline": r["step_roofline"], "e2e": r.get("e2e"), "clocks": r["clocks"],
+                              "kernels": r["kernels"]}
+    cpu = None
+    if rank_id == 0 and world == 1 and not args.no_cpu:
+        cb = time_oracle(spec, 50, target_s=15.0)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if dist is not None:
+        dist.barrier()
+    if rank_id == 0:
+        line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": base_cfg, "clocks": res["clocks"], "gpu_launches": res["launches"],
+                "roofline": res["roofline"], "step_roofline": res["step_roofline"],
+                "e2e": res.get("e2e"), "cpu_baseline": cpu, "kernels": res["kernels"],
+                "workloads": extras}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

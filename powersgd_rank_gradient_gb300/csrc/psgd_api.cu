@@ -125,7 +125,9 @@ struct psgd_state {
   // plan
   std::vector<HostTensor> tensors;
   std::vector<TensorDesc> cdesc;
-  std::vector<Item> items;
+  std::vector<Item> items;    // pass 2
+  std::vector<Item> fitems;   // pass 1, pass 3, error views
+  std::vector<GsItem> qr;     // Q partial reduction chunks
   std::vector<GsItem> gsp, gsq;
   std::vector<int> gsp_first, gsp_count, gsq_first, gsq_count;
   std::vector<Segment> unc_segs, all_segs;
@@ -135,6 +137,8 @@ struct psgd_state {
   // device memory
   TensorDesc* d_tensors = nullptr;
   Item* d_items = nullptr;
+  Item* d_fitems = nullptr;
+  GsItem* d_qr = nullptr;
   GsItem* d_gsp = nullptr;
   GsItem* d_gsq = nullptr;
   int* d_gs_index = nullptr;  // gsp_first | gsp_count | gsq_first | gsq_count
@@ -230,6 +234,8 @@ void build_plan(psgd_state* s) {
   const int CT = ctile_for(RP);
   s->cdesc.clear();
   s->items.clear();
+  s->fitems.clear();
+  s->qr.clear();
   s->gsp.clear();
   s->gsq.clear();
   s->gsp_first.clear();
@@ -265,10 +271,11 @@ void build_plan(psgd_state* s) {
       h.e_off = e_off;
       s->cdesc.push_back(td);
       c_off += (h.numel + 31) / 32 * 32;
+      auto r32 = [](long long x) { return (x + 31) / 32 * 32; };
       p_off += h.rows * RP;
-      q_off += h.cols * RP;
+      q_off += r32(h.cols * RP);
       pp_off += (long long)td.ctiles * h.rows * RP;
-      qp_off += (long long)td.rblocks * h.cols * RP;
+      qp_off += r32((long long)td.rblocks * h.cols * RP);
       e_off += h.numel;
     } else {
       unc += h.numel;
@@ -301,29 +308,38 @@ void build_plan(psgd_state* s) {
       if (it == shapes.end()) shapes.push_back(sh);
     }
   }
+  auto make_items = [&](std::vector<Item>* out, int rows_per_item) {
+    for (size_t c = 0; c < s->cdesc.size(); ++c) {
+      const TensorDesc& td = s->cdesc[c];
+      for (int r0 = 0; r0 < td.n; r0 += rows_per_item)
+        for (int ct = 0; ct < td.ctiles; ++ct) {
+          Item it;
+          it.t = (int)c;
+          it.row0 = r0;
+          it.nrows = std::min(rows_per_item, td.n - r0);
+          it.col0 = ct * CT;
+          it.ncols = std::min(CT, td.m - it.col0);
+          it.rb = r0 / kRowBlock;
+          it.ct = ct;
+          it.pad = group_of[c];
+          out->push_back(it);
+        }
+    }
+    // largest items first (static round-robin over a persistent grid); with
+    // batching, same-shape groups stay together.
+    std::stable_sort(out->begin(), out->end(), [&](const Item& x, const Item& y) {
+      if (s->batch && x.pad != y.pad) return x.pad < y.pad;
+      return (long long)x.nrows * x.ncols > (long long)y.nrows * y.ncols;
+    });
+    for (auto& it : *out) it.pad = 0;
+  };
+  make_items(&s->items, kRowBlock);
+  make_items(&s->fitems, kFineRows);
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
-    const TensorDesc& td = s->cdesc[c];
-    for (int b = 0; b < td.rblocks; ++b)
-      for (int ct = 0; ct < td.ctiles; ++ct) {
-        Item it;
-        it.t = (int)c;
-        it.row0 = b * kRowBlock;
-        it.nrows = std::min(kRowBlock, td.n - it.row0);
-        it.col0 = ct * CT;
-        it.ncols = std::min(CT, td.m - it.col0);
-        it.rb = b;
-        it.ct = ct;
-        it.pad = group_of[c];
-        s->items.push_back(it);
-      }
+    const long long len = (long long)s->cdesc[c].m * RP;
+    for (long long f = 0; f < len; f += 1024)
+      s->qr.push_back({(int)c, (int)f, (int)std::min<long long>(1024, len - f), 0});
   }
-  // largest items first (static round-robin over a persistent grid); with
-  // batching, same-shape groups stay together.
-  std::stable_sort(s->items.begin(), s->items.end(), [&](const Item& x, const Item& y) {
-    if (s->batch && x.pad != y.pad) return x.pad < y.pad;
-    return (long long)x.nrows * x.ncols > (long long)y.nrows * y.ncols;
-  });
-  for (auto& it : s->items) it.pad = 0;
 
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const TensorDesc& td = s->cdesc[c];
@@ -361,6 +377,10 @@ StepArgs make_args(psgd_state* s) {
   a.tensors = s->d_tensors;
   a.items = s->d_items;
   a.n_items = (int)s->items.size();
+  a.fitems = s->d_fitems;
+  a.n_fitems = (int)s->fitems.size();
+  a.qr_items = s->d_qr;
+  a.n_qr = (int)s->qr.size();
   a.gsp_items = s->d_gsp;
   a.n_gsp = (int)s->gsp.size();
   a.gsq_items = s->d_gsq;
@@ -440,8 +460,10 @@ struct Ops {
 
   static void compressed(psgd_state* s, const StepArgs& a, Launcher& L, bool need_fresh,
                          const std::vector<int>& mask) {
-    const int grid_items = std::max(1, std::min(a.n_items, s->sms * 2));
+    const int grid_items = std::max(1, std::min(a.n_items, s->sms * 3));
+    const int grid_fine = std::max(1, std::min(a.n_fitems, s->sms * 2));
     const int grid_q = std::max(1, std::min(a.n_gsq, s->sms * 4));
+    const int grid_qr = std::max(1, std::min(a.n_qr, s->sms * 8));
     if (need_fresh) {
       cudaMemcpyAsync(s->d_mask, mask.data(), mask.size() * sizeof(int), cudaMemcpyHostToDevice, L.st);
       L.begin(K_RANDN);
@@ -450,23 +472,23 @@ struct Ops {
       gs(s, a, L, 1);
     }
     L.begin(K_PASS1);
-    launch_pass1<RP>(a, grid_items, L.st);
+    launch_pass1<RP>(a, grid_fine, L.st);
     L.end();
     gs(s, a, L, 0);
     L.begin(K_PASS2);
     launch_pass2<RP>(a, s->pass2_src, grid_items, L.st);
     L.end();
     L.begin(K_QREDUCE);
-    launch_qreduce<RP>(a, grid_q, L.st);
+    launch_qreduce<RP>(a, grid_qr, L.st);
     L.end();
     L.begin(K_PASS3);
-    launch_pass3<RP>(a, 0, grid_items, L.st);
+    launch_pass3<RP>(a, 0, grid_fine, L.st);
     L.end();
   }
 
   static void errview(psgd_state* s, const StepArgs& a, int mode, cudaStream_t st) {
-    const int grid_items = std::max(1, std::min(a.n_items, s->sms * 2));
-    launch_pass3<RP>(a, mode, grid_items, st);
+    const int grid_fine = std::max(1, std::min(a.n_fitems, s->sms * 2));
+    launch_pass3<RP>(a, mode, grid_fine, st);
   }
 };
 
@@ -601,6 +623,8 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
   } while (0)
   TRY(dupload(s, &s->d_tensors, s->cdesc));
   TRY(dupload(s, &s->d_items, s->items));
+  TRY(dupload(s, &s->d_fitems, s->fitems));
+  TRY(dupload(s, &s->d_qr, s->qr));
   TRY(dupload(s, &s->d_gsp, s->gsp));
   TRY(dupload(s, &s->d_gsq, s->gsq));
   TRY(dupload(s, &s->d_gs_index, gs_index));
@@ -818,9 +842,10 @@ int psgd_set_q(psgd_state* s, int32_t t, const float* host_in, int32_t is_draw) 
   DeviceGuard g(s->device);
   PSGD_CUDA_TRY(cudaDeviceSynchronize());
   const TensorDesc& td = s->cdesc[h->cidx];
+  // k-major device layout: element (j, k) at k * cols + j
   std::vector<float> buf((size_t)td.m * s->RP, 0.f);
   for (long long j = 0; j < td.m; ++j)
-    for (int k = 0; k < td.r; ++k) buf[j * s->RP + k] = host_in[j * td.r + k];
+    for (int k = 0; k < td.r; ++k) buf[(size_t)k * td.m + j] = host_in[j * td.r + k];
   if (is_draw) {
     PSGD_CUDA_TRY(cudaMemcpy(s->qdraw + td.q_off, buf.data(), buf.size() * 4, cudaMemcpyHostToDevice));
     s->pending_draw[h->cidx] = 1;
@@ -866,7 +891,8 @@ static int get_factor(psgd_state* s, int t, float* host_out, bool is_q) {
   const float* src = is_q ? s->Qf + (size_t)cur * s->q_total + td.q_off : s->Pf + (size_t)cur * s->p_total + td.p_off;
   PSGD_CUDA_TRY(cudaMemcpy(buf.data(), src, buf.size() * 4, cudaMemcpyDeviceToHost));
   for (long long j = 0; j < rows; ++j)
-    for (int k = 0; k < td.r; ++k) host_out[j * td.r + k] = buf[j * s->RP + k];
+    for (int k = 0; k < td.r; ++k)
+      host_out[j * td.r + k] = is_q ? buf[(size_t)k * rows + j] : buf[j * s->RP + k];
   return PSGD_OK;
 }
 

@@ -6,11 +6,13 @@
 //                  holds M_w of the last committed step; the residual is kept
 //                  in factored form, e_w = store_w - P Q^T, with (P, Q) the
 //                  factors of that step (see Pf/Qf).
-//   Pf[2], Qf[2] : the committed factors (rows x RP, cols x RP per tensor,
-//                  rank padded to RP = next power of two, unused columns 0).
+//   Pf[2], Qf[2] : the committed factors, rank padded to RP = next power of
+//                  two (unused columns 0): P row-major (rows x RP), Q k-major
+//                  (element (j, k) at k * cols + j, so a warp reading 4
+//                  consecutive columns per lane makes one coalesced access).
 //                  Qf[cur] is also the warm-start projection of the next step.
 //   praw_part    : pass-1 partial P = Mbar Q, one slice per column tile.
-//   qpart        : pass-2 partial Q = Mbar^T P, one slice per row block.
+//   qpart        : pass-2 partial Q = Mbar^T P, one k-major slice per row block.
 //   mbar         : optional scratch holding the replica mean of M (W >= 3).
 //   ctrl         : device integers: cur, warm_valid, nonfinite flag.
 #pragma once
@@ -20,7 +22,8 @@
 namespace psgd {
 
 constexpr int kThreads = 256;      // threads per CTA of the streaming passes
-constexpr int kRowBlock = 512;     // rows per work item of the three passes
+constexpr int kRowBlock = 512;     // rows per work item of pass 2 (one Q partial each)
+constexpr int kFineRows = 64;      // rows per work item of pass 1 and pass 3
 constexpr int kGsRows = 1024;      // rows per work item of the Gram-Schmidt kernels
 
 // Columns per thread (CPT) and column-tile width of the streaming passes for
@@ -32,9 +35,9 @@ struct TensorDesc {
   long long g_off;   // first element in the bucket
   long long c_off;   // first element in the packed error store / mbar
   long long p_off;   // first element of the tensor's P (rows x RP)
-  long long q_off;   // first element of the tensor's Q (cols x RP)
+  long long q_off;   // first element of the tensor's Q (RP x cols, k-major; 32-aligned)
   long long pp_off;  // first element of praw_part (ctiles x rows x RP)
-  long long qp_off;  // first element of qpart (rblocks x cols x RP)
+  long long qp_off;  // first element of qpart (rblocks x RP x cols; 32-aligned)
   long long e_off;   // first element in the user-visible packed error (no padding)
   int n, m, r;       // rows, cols, effective rank
   int ctiles;        // column tiles

@@ -51,8 +51,12 @@ struct StepArgs {
   double* gram;       // per Gram-Schmidt item RP x RP
   float* tmat;        // per tensor RP x RP transform
   const TensorDesc* tensors;
-  const Item* items;
+  const Item* items;         // tall (row block) x (column tile) items: pass 2
   int n_items;
+  const Item* fitems;        // short items: pass 1, pass 3 and the error views
+  int n_fitems;
+  const GsItem* qr_items;    // chunks of each tensor's Q for the partial reduction
+  int n_qr;
   const GsItem* gsp_items;   // rows of P
   int n_gsp;
   const GsItem* gsq_items;   // rows of Q
@@ -185,6 +189,24 @@ __device__ __forceinline__ void load_row(const float* __restrict__ p, float (&v)
   }
 }
 
+// Columns c .. c+NC-1 of a k-major factor (element (j, k) at base + k * ld + j):
+// v[cc][k].  One coalesced access per k across the warp.
+template <int RP, int NC>
+__device__ __forceinline__ void load_qcols(const float* __restrict__ base, long long ld, long long c,
+                                           float (&v)[NC][RP]) {
+#pragma unroll
+  for (int k = 0; k < RP; ++k) {
+    const float* p = base + (long long)k * ld + c;
+    if constexpr (NC == 4) {
+      float4 x = __ldg(reinterpret_cast<const float4*>(p));
+      v[0][k] = x.x; v[1][k] = x.y; v[2][k] = x.z; v[3][k] = x.w;
+    } else {
+#pragma unroll
+      for (int cc = 0; cc < NC; ++cc) v[cc][k] = __ldg(p + cc);
+    }
+  }
+}
+
 // sum_k a[k] * b[k] as one fused multiply-add chain in increasing k.  Pass 3
 // (out) and pass 1 (the lazy residual) both use it, so they agree bit for bit.
 template <int RP>
@@ -233,13 +255,12 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
       // residual correction P_old[i,:] . Q_old[c,:]
       float corr[RW][NC];
       if (a.ef) {
+        float qo[NC][RP];
+        load_qcols<RP, NC>(Qc + td.q_off, m, c, qo);
 #pragma unroll
-        for (int cc = 0; cc < NC; ++cc) {
-          float qo[RP];
-          load_row<RP>(Qc + td.q_off + (long long)(c + cc) * RP, qo);
+        for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
-          for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qo);
-        }
+          for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qo[cc]);
       }
       float mb[RW][NC];
 #pragma unroll
@@ -276,14 +297,15 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
         for (int cc = 0; cc < NC; ++cc) mb[q][cc] *= a.invW;
         if (a.mbar && rv[q]) store_f<NC>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * m + c, mb[q]);
       }
+      {
+        float qv[NC][RP];
+        load_qcols<RP, NC>(Qp + td.q_off, m, c, qv);
 #pragma unroll
-      for (int cc = 0; cc < NC; ++cc) {
-        float qv[RP];
-        load_row<RP>(Qp + td.q_off + (long long)(c + cc) * RP, qv);
+        for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
-        for (int q = 0; q < RW; ++q)
+          for (int q = 0; q < RW; ++q)
 #pragma unroll
-          for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[k], pacc[q][k]);
+            for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[cc][k], pacc[q][k]);
       }
     }
 #pragma unroll
@@ -300,6 +322,206 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pass 1, staged: the same arithmetic as pass1_tile, but each lane copies the
+// 16 bytes it will consume of every source row segment into its own slot of
+// shared memory with cp.async, S units ahead ("unit" = RW rows x 128 columns).
+// Bytes in flight then cost shared memory instead of registers, so a warp
+// keeps (S - 1) units of HBM traffic outstanding.  Warps are independent: no
+// CTA barrier, each warp owns rows warp*RW + g*8*RW of the item.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int RP, int WT, typename GT, int RW>
+struct Pass1Stage {
+  static constexpr int GB = 4 * (int)sizeof(GT);                 // gradient bytes per lane per unit row
+  static constexpr int GSEG = 32 * GB;                            // one gradient row segment (warp)
+  static constexpr int ESEG = 32 * 16;                            // one store row segment (warp)
+  static constexpr int UNIT_BYTES = RW * WT * (GSEG + ESEG);      // per warp per unit
+  static constexpr int S_RAW = (200 * 1024) / (8 * UNIT_BYTES);
+  static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
+  static constexpr int SMEM = 8 * S * UNIT_BYTES;                 // per CTA
+};
+
+template <int RP, int WT, typename GT, int RW>
+__device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const TensorDesc& td, const Item& item,
+                                                  const float* __restrict__ Qp, const float* __restrict__ Qc,
+                                                  const float* __restrict__ Pc, int cur, int& bad,
+                                                  char* __restrict__ wsm) {
+  using St = Pass1Stage<RP, WT, GT, RW>;
+  constexpr int S = St::S;
+  constexpr int GB = St::GB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nxt = cur ^ 1;
+  const long long m = td.m;
+  const int cend = item.col0 + item.ncols;
+  const int nchunks = (item.ncols + 127) / 128;
+  const int first = warp * RW;
+  const int ngroups = first < item.nrows ? (item.nrows - first + 8 * RW - 1) / (8 * RW) : 0;
+  const int units = ngroups * nchunks;
+  const bool same_q = (Qp == Qc);
+  // slot layout: [q][w] gradient segments, then [q][w] store segments; inside
+  // a segment lane l owns bytes [l * width, (l + 1) * width), so a warp's
+  // accesses to one segment are contiguous and free of bank conflicts.
+
+  auto issue = [&](int u) {
+    const int g = u / nchunks, ch = u - (u / nchunks) * nchunks;
+    const int rr = first + g * 8 * RW;
+    const int c = item.col0 + ch * 128 + lane * 4;
+    char* slot = wsm + (u % S) * St::UNIT_BYTES;
+#pragma unroll
+    for (int q = 0; q < RW; ++q) {
+      if (rr + q >= item.nrows || c >= cend) continue;
+      const long long row = item.row0 + rr + q;
+#pragma unroll
+      for (int w = 0; w < WT; ++w) {
+        const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c;
+        char* gdst = slot + (q * WT + w) * St::GSEG + lane * GB;
+        if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+        if (a.ef) {
+          const float* esrc = a.estore + ((long long)cur * a.W + w) * a.nc_pad + td.c_off + row * m + c;
+          cp_async16(slot + RW * WT * St::GSEG + (q * WT + w) * St::ESEG + lane * 16, esrc);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int u = 0; u < S - 1; ++u) {
+    if (u < units) issue(u); else cp_async_commit();
+  }
+  float po[RW][RP];
+  float pacc[RW][RP];
+  for (int u = 0; u < units; ++u) {
+    cp_async_wait<S - 2>();
+    if (u + S - 1 < units) issue(u + S - 1); else cp_async_commit();
+    const int g = u / nchunks, ch = u - (u / nchunks) * nchunks;
+    const int rr = first + g * 8 * RW;
+    const int c = item.col0 + ch * 128 + lane * 4;
+    bool rv[RW];
+#pragma unroll
+    for (int q = 0; q < RW; ++q) rv[q] = (rr + q) < item.nrows;
+    if (ch == 0) {
+#pragma unroll
+      for (int q = 0; q < RW; ++q) {
+        const int i = item.row0 + (rv[q] ? rr + q : rr);
+#pragma unroll
+        for (int k = 0; k < RP; ++k) { pacc[q][k] = 0.f; po[q][k] = 0.f; }
+        if (a.ef) load_row<RP>(Pc + td.p_off + (long long)i * RP, po[q]);
+      }
+    }
+    if (c < cend) {
+      const char* slot = wsm + (u % S) * St::UNIT_BYTES;
+      float qv[4][RP];
+      float corr[RW][4];
+      if (a.ef) {
+        load_qcols<RP, 4>(Qc + td.q_off, m, c, qv);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qv[cc]);
+      }
+      float mb[RW][4];
+#pragma unroll
+      for (int q = 0; q < RW; ++q)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) mb[q][cc] = 0.f;
+#pragma unroll
+      for (int w = 0; w < WT; ++w) {
+        float* enxt = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off;
+#pragma unroll
+        for (int q = 0; q < RW; ++q) {
+          if (!rv[q]) continue;
+          const long long i = item.row0 + rr + q;
+          float gv[4];
+          if constexpr (GB == 16) {
+            const float4 x = *reinterpret_cast<const float4*>(slot + (q * WT + w) * St::GSEG + lane * GB);
+            gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
+          } else {
+            const uint2 raw = *reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB);
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+            gv[0] = fa.x; gv[1] = fa.y; gv[2] = fb.x; gv[3] = fb.y;
+          }
+          float ev[4] = {0.f, 0.f, 0.f, 0.f};
+          if (a.ef) {
+            const float4 x = *reinterpret_cast<const float4*>(slot + RW * WT * St::GSEG + (q * WT + w) * St::ESEG + lane * 16);
+            ev[0] = x.x; ev[1] = x.y; ev[2] = x.z; ev[3] = x.w;
+          }
+          float mv[4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const float v = gv[cc] * a.scale;
+            bad |= !isfinite(v);
+            mv[cc] = a.ef ? v + (ev[cc] - corr[q][cc]) : v;
+            mb[q][cc] += mv[cc];
+          }
+          if (a.ef) store_f<4>(enxt + i * m + c, mv);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < RW; ++q) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) mb[q][cc] *= a.invW;
+        if (a.mbar && rv[q]) store_f<4>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * m + c, mb[q]);
+      }
+      if (!(a.ef && same_q)) load_qcols<RP, 4>(Qp + td.q_off, m, c, qv);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int q = 0; q < RW; ++q)
+#pragma unroll
+          for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[cc][k], pacc[q][k]);
+    }
+    if (ch == nchunks - 1) {
+#pragma unroll
+      for (int q = 0; q < RW; ++q) {
+#pragma unroll
+        for (int k = 0; k < RP; ++k) pacc[q][k] = warp_sum(pacc[q][k]);
+        if (rv[q] && lane == 0) {
+          float* dst = a.praw_part + td.pp_off + ((long long)item.ct * td.n + item.row0 + rr + q) * RP;
+#pragma unroll
+          for (int k = 0; k < RP; ++k) dst[k] = pacc[q][k];
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+template <int RP, int WT, typename GT, int RW>
+__global__ void __launch_bounds__(kThreads) k_pass1_staged(const StepArgs a) {
+  extern __shared__ __align__(16) char p1smem[];
+  using St = Pass1Stage<RP, WT, GT, RW>;
+  const int cur = a.ctrl->cur;
+  const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
+  const float* Qc = a.Qf + (long long)cur * a.q_total;
+  const float* Pc = a.Pf + (long long)cur * a.p_total;
+  const float* Qp = use_init ? a.qinit : Qc;
+  char* wsm = p1smem + (threadIdx.x >> 5) * (St::S * St::UNIT_BYTES);
+  int bad = 0;
+  for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
+    const Item item = a.fitems[it];
+    const TensorDesc td = a.tensors[item.t];
+    if (td.vec && a.vec_ok)
+      pass1_tile_staged<RP, WT, GT, RW>(a, td, item, Qp, Qc, Pc, cur, bad, wsm);
+    else
+      pass1_tile<RP, WT, GT, RW, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
+}
+
 template <int RP, int WT, typename GT, int RW>
 __global__ void __launch_bounds__(kThreads) k_pass1(const StepArgs a) {
   const int cur = a.ctrl->cur;
@@ -308,8 +530,8 @@ __global__ void __launch_bounds__(kThreads) k_pass1(const StepArgs a) {
   const float* Pc = a.Pf + (long long)cur * a.p_total;
   const float* Qp = use_init ? a.qinit : Qc;
   int bad = 0;
-  for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
-    const Item item = a.items[it];
+  for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
+    const Item item = a.fitems[it];
     const TensorDesc td = a.tensors[item.t];
     if (td.vec && a.vec_ok)
       pass1_tile<RP, WT, GT, RW, 4>(a, td, item, Qp, Qc, Pc, cur, bad);
@@ -366,6 +588,8 @@ __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float
         if (from_parts) {
           v = 0.f;
           for (int c = 0; c < td.ctiles; ++c) v += src[td.pp_off + ((long long)c * td.n + row) * RP + k];
+        } else if (is_q) {
+          v = src[base + (long long)k * td.m + row];
         } else {
           v = src[base + row * RP + k];
         }
@@ -491,14 +715,17 @@ __global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const floa
     for (int rr = threadIdx.x; rr < gi.nrows; rr += kThreads) {
       const long long row = gi.row0 + rr;
       float x[RP], y[RP];
+      // P is row-major (rows x RP); Q is k-major (element (j, k) at k * m + j)
+      const long long rs = is_q ? 1 : RP;
+      const long long ks = is_q ? td.m : 1;
 #pragma unroll
-      for (int k = 0; k < RP; ++k) { x[k] = src[base + row * RP + k]; y[k] = 0.f; }
+      for (int k = 0; k < RP; ++k) { x[k] = src[base + row * rs + k * ks]; y[k] = 0.f; }
 #pragma unroll
       for (int l = 0; l < RP; ++l)
 #pragma unroll
         for (int k = 0; k < RP; ++k) y[k] = fmaf(x[l], T[l * RP + k], y[k]);
 #pragma unroll
-      for (int k = 0; k < RP; ++k) dst[half_off + base + row * RP + k] = y[k];
+      for (int k = 0; k < RP; ++k) dst[half_off + base + row * rs + k * ks] = y[k];
     }
   }
 }
@@ -507,23 +734,79 @@ __global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const floa
 // Pass 2: partial Q' = Mbar^T P over one (row block, column tile); each thread
 // owns CPT columns and accumulates CPT x RP sums over the block's rows.
 // SRC 0: Mbar scratch; 1: mean of the W store halves just written; 2: mean of
-// the W unscaled gradients (error feedback off).
+// the W unscaled gradients (error feedback off).  Partials are k-major:
+// qpart[rb][k][j].
 // ---------------------------------------------------------------------------
 constexpr int kPStage = 64;
+constexpr int kRowBatch = 8;
 
-template <int RP, int SRC, typename GT, int NC>
+// NC values of Mbar at (row, c0 ..) from the selected source; VEC: one
+// 16-byte access per source (NC == 4, aligned rows), else element by element
+// with bounds checks.
+template <int SRC, typename GT, int WT, int NC, bool VEC>
+__device__ __forceinline__ void load_mbar(const StepArgs& a, const TensorDesc& td, long long row, int c0,
+                                          int cend, int nxt, float (&mv)[NC]) {
+  const long long m = td.m;
+  static_assert(!VEC || NC == 4, "vector path is 4 wide");
+  if constexpr (SRC == 0) {
+    if constexpr (VEC) {
+      load_f<4>(a.mbar + td.c_off + row * m + c0, mv, true);
+    } else {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) mv[c] = (c0 + c < cend) ? ld_stream1(a.mbar + td.c_off + row * m + c0 + c) : 0.f;
+    }
+  } else {
+    const int W = WT > 0 ? WT : a.W;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) mv[c] = 0.f;
+#pragma unroll(WT > 0 ? WT : 1)
+    for (int w = 0; w < W; ++w) {
+      float v[NC];
+      if constexpr (SRC == 1) {
+        const float* src = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * m + c0;
+        if constexpr (VEC) {
+          load_f<4>(src, v, true);
+        } else {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) v[c] = (c0 + c < cend) ? ld_stream1(src + c) : 0.f;
+        }
+      } else {
+        const GT* src = reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c0;
+        if constexpr (VEC) {
+          load_grad<4, GT>(src, v);
+        } else {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            float t[1] = {0.f};
+            if (c0 + c < cend) load_grad<1, GT>(src + c, t);
+            v[c] = t[0];
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < NC; ++c) v[c] *= a.scale;
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c) mv[c] += v[c];
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) mv[c] *= a.invW;
+  }
+}
+
+template <int RP, int SRC, typename GT, int WT, int NC>
 __device__ __forceinline__ void pass2_tile(const StepArgs& a, const TensorDesc& td, const Item& item,
                                            const float* __restrict__ P, float (*ps)[RP]) {
   constexpr int CPT = cpt_for(RP);
-  const long long m = td.m;
+  static_assert(NC == CPT || NC == 1, "columns per access");
+  constexpr int NA = CPT;  // columns accumulated per thread
   const int c0 = item.col0 + threadIdx.x * CPT;
   const int nxt = a.ctrl->cur ^ 1;
-  float acc[CPT][RP];
+  const int cend = item.col0 + item.ncols;
+  float acc[NA][RP];
 #pragma unroll
-  for (int c = 0; c < CPT; ++c)
+  for (int c = 0; c < NA; ++c)
 #pragma unroll
     for (int k = 0; k < RP; ++k) acc[c][k] = 0.f;
-  const int cend = item.col0 + item.ncols;
   for (int sb = 0; sb < item.nrows; sb += kPStage) {
     const int rows = min(kPStage, item.nrows - sb);
     __syncthreads();
@@ -531,71 +814,47 @@ __device__ __forceinline__ void pass2_tile(const StepArgs& a, const TensorDesc& 
       ps[idx / RP][idx % RP] = P[td.p_off + (long long)(item.row0 + sb) * RP + idx];
     __syncthreads();
     if (c0 >= cend) continue;
-#pragma unroll 4
-    for (int i = 0; i < rows; ++i) {
-      const long long row = item.row0 + sb + i;
-      float mv[CPT];
+    int i = 0;
+    for (; i + kRowBatch <= rows; i += kRowBatch) {
+      float mv[kRowBatch][NA];
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) mv[c] = 0.f;
-      if constexpr (NC == CPT) {
-        if constexpr (SRC == 0) {
-          load_f<NC>(a.mbar + td.c_off + row * m + c0, mv, true);
-        } else {
-          for (int w = 0; w < a.W; ++w) {
-            float v[NC];
-            if constexpr (SRC == 1) {
-              load_f<NC>(a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * m + c0, v, true);
-            } else {
-              load_grad<NC, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c0, v);
+      for (int u = 0; u < kRowBatch; ++u)
+        load_mbar<SRC, GT, WT, NA, (NC == 4)>(a, td, item.row0 + sb + i + u, c0, cend, nxt, mv[u]);
 #pragma unroll
-              for (int c = 0; c < NC; ++c) v[c] *= a.scale;
-            }
+      for (int u = 0; u < kRowBatch; ++u)
 #pragma unroll
-            for (int c = 0; c < NC; ++c) mv[c] += v[c];
-          }
+        for (int c = 0; c < NA; ++c)
 #pragma unroll
-          for (int c = 0; c < CPT; ++c) mv[c] *= a.invW;
-        }
-      } else {
-        // unaligned tensor: element by element
+          for (int k = 0; k < RP; ++k) acc[c][k] = fmaf(mv[u][c], ps[i + u][k], acc[c][k]);
+    }
+    for (; i < rows; ++i) {
+      float mv[NA];
+      load_mbar<SRC, GT, WT, NA, (NC == 4)>(a, td, item.row0 + sb + i, c0, cend, nxt, mv);
 #pragma unroll
-        for (int c = 0; c < CPT; ++c) {
-          if (c0 + c >= cend) continue;
-          if constexpr (SRC == 0) {
-            mv[c] = ld_stream1(a.mbar + td.c_off + row * m + c0 + c);
-          } else {
-            float s = 0.f;
-            for (int w = 0; w < a.W; ++w) {
-              float v[1];
-              if constexpr (SRC == 1) {
-                v[0] = ld_stream1(a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * m + c0 + c);
-              } else {
-                load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c0 + c, v);
-                v[0] *= a.scale;
-              }
-              s += v[0];
-            }
-            mv[c] = s * a.invW;
-          }
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < CPT; ++c)
+      for (int c = 0; c < NA; ++c)
 #pragma unroll
         for (int k = 0; k < RP; ++k) acc[c][k] = fmaf(mv[c], ps[i][k], acc[c][k]);
     }
   }
-  // columns of this thread
+  if (c0 >= cend) return;
+  float* dst = a.qpart + td.qp_off + (long long)item.rb * RP * td.m;
 #pragma unroll
-  for (int c = 0; c < CPT; ++c) {
-    if (c0 + c >= cend) continue;
-    float* dst = a.qpart + td.qp_off + ((long long)item.rb * td.m + c0 + c) * RP;
+  for (int k = 0; k < RP; ++k) {
+    float* d = dst + (long long)k * td.m + c0;
+    if constexpr (NA == 4 && NC == 4) {
+      *reinterpret_cast<float4*>(d) = make_float4(acc[0][k], acc[1][k], acc[2][k], acc[3][k]);
+    } else {
 #pragma unroll
-    for (int k = 0; k < RP; ++k) dst[k] = acc[c][k];
+      for (int c = 0; c < NA; ++c)
+        if (c0 + c < cend) d[c] = acc[c][k];
+    }
   }
 }
 
-template <int RP, int SRC, typename GT>
+// The vector path needs 16-byte aligned rows of the source; unaligned tensors
+// take the element-wise path (NC = 1): same CPT columns per thread, one access
+// per element.
+template <int RP, int SRC, typename GT, int WT>
 __global__ void __launch_bounds__(kThreads) k_pass2(const StepArgs a) {
   __shared__ __align__(16) float ps[kPStage][RP];
   if (a.ctrl->flag) return;
@@ -604,31 +863,49 @@ __global__ void __launch_bounds__(kThreads) k_pass2(const StepArgs a) {
   for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
     const Item item = a.items[it];
     const TensorDesc td = a.tensors[item.t];
-    // CPT-wide vector accesses need rows aligned to CPT elements; the store and
-    // mbar are, the gradient rows are when the tensor is marked vec.
     const bool vec = (SRC == 2) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
-    if (vec)
-      pass2_tile<RP, SRC, GT, CPT>(a, td, item, P, ps);
+    if (vec && CPT == 4)
+      pass2_tile<RP, SRC, GT, WT, CPT>(a, td, item, P, ps);
     else
-      pass2_tile<RP, SRC, GT, 1>(a, td, item, P, ps);
+      pass2_tile<RP, SRC, GT, WT, 1>(a, td, item, P, ps);
   }
 }
 
-// Q'[j] = sum over row blocks of the partials, in row-block order; written
-// into the next half of Qf.
+// Q'(j, k) = sum over row blocks of the partials, in row-block order, written
+// k-major into the next half of Qf.  Each work item is a chunk of one
+// tensor's RP * m values, four per thread.
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
   if (a.ctrl->flag) return;
   float* Q = a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
-  for (int it = blockIdx.x; it < a.n_gsq; it += gridDim.x) {
-    const GsItem gi = a.gsq_items[it];
+  for (int it = blockIdx.x; it < a.n_qr; it += gridDim.x) {
+    const GsItem gi = a.qr_items[it];
     const TensorDesc td = a.tensors[gi.t];
-    for (int idx = threadIdx.x; idx < gi.nrows * RP; idx += kThreads) {
-      const long long j = gi.row0 + idx / RP;
-      const int k = idx % RP;
-      float s = 0.f;
-      for (int b = 0; b < td.rblocks; ++b) s += a.qpart[td.qp_off + ((long long)b * td.m + j) * RP + k];
-      Q[td.q_off + j * RP + k] = s;
+    const long long len = (long long)RP * td.m;
+    const float* src = a.qpart + td.qp_off;
+    const int f = gi.row0 + threadIdx.x * 4;
+    if (f >= gi.row0 + gi.nrows) continue;
+    if (len % 4 == 0) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      int b = 0;
+      for (; b + 4 <= td.rblocks; b += 4) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = ld_stream4(src + (long long)(b + u) * len + f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) { s.x += x[u].x; s.y += x[u].y; s.z += x[u].z; s.w += x[u].w; }
+      }
+      for (; b < td.rblocks; ++b) {
+        float4 x = ld_stream4(src + (long long)b * len + f);
+        s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
+      }
+      *reinterpret_cast<float4*>(Q + td.q_off + f) = s;
+    } else {
+      for (int e = f; e < min(f + 4, gi.row0 + gi.nrows); ++e) {
+        float s = 0.f;
+        for (int b = 0; b < td.rblocks; ++b) s += src[(long long)b * len + e];
+        Q[td.q_off + e] = s;
+      }
     }
   }
 }
@@ -650,12 +927,19 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
   const int cend = item.col0 + item.ncols;
   float qv[CPT][RP];
 #pragma unroll
-  for (int c = 0; c < CPT; ++c) {
-    if (c0 + c < cend)
-      load_row<RP>(Q + td.q_off + (long long)(c0 + c) * RP, qv[c]);
-    else
+  for (int k = 0; k < RP; ++k) {
+    const float* q = Q + td.q_off + (long long)k * m + c0;
+    if constexpr (NC == 4 && CPT == 4) {
+      if (c0 < cend) {
+        float4 x = __ldg(reinterpret_cast<const float4*>(q));
+        qv[0][k] = x.x; qv[1][k] = x.y; qv[2][k] = x.z; qv[3][k] = x.w;
+      } else {
+        qv[0][k] = qv[1][k] = qv[2][k] = qv[3][k] = 0.f;
+      }
+    } else {
 #pragma unroll
-      for (int k = 0; k < RP; ++k) qv[c][k] = 0.f;
+      for (int c = 0; c < CPT; ++c) qv[c][k] = (c0 + c < cend) ? __ldg(q + c) : 0.f;
+    }
   }
   for (int sb = 0; sb < item.nrows; sb += kPStage) {
     const int rows = min(kPStage, item.nrows - sb);
@@ -677,13 +961,10 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
         if constexpr (MODE == 0) {
           store_f<4>(a.out + td.g_off + row * m + c0, o);
         } else if constexpr (MODE == 1) {
-          float s[4];
-          load_f<4>(store + td.c_off + row * m + c0, s, true);
-          float e[4];
+          float sv[4];
+          load_f<4>(store + td.c_off + row * m + c0, sv, true);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) e[c] = s[c] - o[c];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) a.eio[td.e_off + row * m + c0 + c] = e[c];
+          for (int c = 0; c < 4; ++c) a.eio[td.e_off + row * m + c0 + c] = sv[c] - o[c];
         } else if constexpr (MODE == 2) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) store[td.c_off + row * m + c0 + c] = a.eio[td.e_off + row * m + c0 + c] + o[c];
@@ -723,8 +1004,8 @@ __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
   float* store = nullptr;
   if (MODE != 0) store = a.estore + ((long long)a.ctrl->cur * a.W + a.replica) * a.nc_pad;
   constexpr int CPT = cpt_for(RP);
-  for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
-    const Item item = a.items[it];
+  for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
+    const Item item = a.fitems[it];
     const TensorDesc td = a.tensors[item.t];
     const bool vec = (MODE == 0) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
     if (vec && CPT == 4)

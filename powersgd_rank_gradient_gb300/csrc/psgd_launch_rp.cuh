@@ -7,23 +7,34 @@
 
 namespace psgd {
 
+template <int RP, int WT, typename GT, int RW>
+void launch_pass1_staged(const StepArgs& a, int grid, cudaStream_t s) {
+  using St = Pass1Stage<RP, WT, GT, RW>;
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(k_pass1_staged<RP, WT, GT, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize, St::SMEM);
+    configured = true;
+  }
+  k_pass1_staged<RP, WT, GT, RW><<<grid, kThreads, St::SMEM, s>>>(a);
+}
+
 template <int RP>
 void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
   constexpr int RW = RP <= 8 ? 2 : 1;
   if (a.f16) {
     switch (a.W) {
-      case 1: k_pass1<RP, 1, __half, RW><<<grid, kThreads, 0, s>>>(a); break;
-      case 2: k_pass1<RP, 2, __half, RW><<<grid, kThreads, 0, s>>>(a); break;
-      case 4: k_pass1<RP, 4, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
-      case 8: k_pass1<RP, 8, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 1: launch_pass1_staged<RP, 1, __half, RW>(a, grid, s); break;
+      case 2: launch_pass1_staged<RP, 2, __half, RW>(a, grid, s); break;
+      case 4: launch_pass1_staged<RP, 4, __half, 1>(a, grid, s); break;
+      case 8: launch_pass1_staged<RP, 8, __half, 1>(a, grid, s); break;
       default: k_pass1<RP, 0, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
     }
   } else {
     switch (a.W) {
-      case 1: k_pass1<RP, 1, float, RW><<<grid, kThreads, 0, s>>>(a); break;
-      case 2: k_pass1<RP, 2, float, RW><<<grid, kThreads, 0, s>>>(a); break;
-      case 4: k_pass1<RP, 4, float, 1><<<grid, kThreads, 0, s>>>(a); break;
-      case 8: k_pass1<RP, 8, float, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 1: launch_pass1_staged<RP, 1, float, RW>(a, grid, s); break;
+      case 2: launch_pass1_staged<RP, 2, float, RW>(a, grid, s); break;
+      case 4: launch_pass1_staged<RP, 4, float, 1>(a, grid, s); break;
+      case 8: launch_pass1_staged<RP, 8, float, 1>(a, grid, s); break;
       default: k_pass1<RP, 0, float, 1><<<grid, kThreads, 0, s>>>(a); break;
     }
   }
@@ -48,14 +59,29 @@ void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q, int
 
 template <int RP>
 void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s) {
-  if (src_mode == 0)
-    k_pass2<RP, 0, float><<<grid, kThreads, 0, s>>>(a);
-  else if (src_mode == 1)
-    k_pass2<RP, 1, float><<<grid, kThreads, 0, s>>>(a);
-  else if (a.f16)
-    k_pass2<RP, 2, __half><<<grid, kThreads, 0, s>>>(a);
-  else
-    k_pass2<RP, 2, float><<<grid, kThreads, 0, s>>>(a);
+  if (src_mode == 0) {
+    k_pass2<RP, 0, float, 0><<<grid, kThreads, 0, s>>>(a);
+  } else if (src_mode == 1) {
+    if (a.W == 1)
+      k_pass2<RP, 1, float, 1><<<grid, kThreads, 0, s>>>(a);
+    else if (a.W == 2)
+      k_pass2<RP, 1, float, 2><<<grid, kThreads, 0, s>>>(a);
+    else
+      k_pass2<RP, 1, float, 0><<<grid, kThreads, 0, s>>>(a);
+  } else if (a.f16) {
+    switch (a.W) {
+      case 1: k_pass2<RP, 2, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 2: k_pass2<RP, 2, __half, 2><<<grid, kThreads, 0, s>>>(a); break;
+      case 4: k_pass2<RP, 2, __half, 4><<<grid, kThreads, 0, s>>>(a); break;
+      default: k_pass2<RP, 2, __half, 0><<<grid, kThreads, 0, s>>>(a); break;
+    }
+  } else {
+    switch (a.W) {
+      case 1: k_pass2<RP, 2, float, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 2: k_pass2<RP, 2, float, 2><<<grid, kThreads, 0, s>>>(a); break;
+      default: k_pass2<RP, 2, float, 0><<<grid, kThreads, 0, s>>>(a); break;
+    }
+  }
 }
 
 template <int RP>

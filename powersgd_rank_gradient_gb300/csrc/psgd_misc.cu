@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) k_randn(const StepArgs a, const int*
         const float u2 = (float)o.v[1] * 2.3283064365386963e-10f;           // [0, 1)
         z = sqrtf(-2.0f * logf(u1)) * cosf(6.283185307179586f * u2);
       }
-      a.qdraw[td.q_off + j * rp + k] = z;
+      a.qdraw[td.q_off + (long long)k * td.m + j] = z;  // k-major
     }
   }
 }

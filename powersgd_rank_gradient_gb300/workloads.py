@@ -40,21 +40,22 @@ def resnet50_shapes():
     return shapes
 
 
-def bert_large_shapes():
-    shapes = [(30522, 1024), (512, 1024), (1024,), (1024,)]
-    for _ in range(24):
+def bert_large_shapes(layers=24, embeddings=True):
+    shapes = [(30522, 1024), (512, 1024), (1024,), (1024,)] if embeddings else []
+    for _ in range(layers):
         shapes += [(1024, 1024), (1024,)] * 4
         shapes += [(1024,), (1024,), (4096, 1024), (4096,), (1024, 4096), (1024,),
                    (1024,), (1024,)]
     return shapes
 
 
-def gpt2_xl_shapes():
-    shapes = [(50257, 1600)]
-    for _ in range(48):
+def gpt2_xl_shapes(layers=48, embeddings=True):
+    shapes = [(50257, 1600)] if embeddings else []
+    for _ in range(layers):
         shapes += [(1600,), (1600,), (1600, 4800), (4800,), (1600, 1600), (1600,),
                    (1600,), (1600,), (1600, 6400), (6400,), (6400, 1600), (1600,)]
-    shapes += [(1600,), (1600,)]
+    if embeddings:
+        shapes += [(1600,), (1600,)]
     return shapes
 
 
