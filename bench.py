@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--extra", default="gpt2-xl",
                     help="comma-separated workloads also measured and reported under 'workloads'")
+    ap.add_argument("--rank", type=int, default=None, help="rank of the rank-sweep workload")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling cases: only this many transformer layers, no embeddings")
     ap.add_argument("--no-e2e", action="store_true")
@@ -60,7 +61,7 @@ def workload_spec(name, rank_override=None, layers=None):
     from powersgd_rank_gradient_gb300 import workloads as wl
 
     if name == "rank-sweep":
-        return dict(name="rank-sweep-8192", shapes=[(8192, 8192)], world_size=1,
+        return dict(name=f"rank-sweep-8192-r{rank_override or 8}", shapes=[(8192, 8192)], world_size=1,
                     rank=rank_override or 8, mcr=2.0, std=1.0, heavy=0.0, batch_same_shape=False)
     w = wl.WORKLOADS[name]
     if layers is not None and name in ("bert-large", "gpt2-xl"):
@@ -392,7 +393,7 @@ def main():
     rank_id = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    spec = workload_spec(args.workload, layers=args.layers)
+    spec = workload_spec(args.workload, rank_override=args.rank, layers=args.layers)
     base_cfg = {"workload": spec["name"], "world_size_W": spec["world_size"],
                 "matrix_approximation_rank": spec["rank"], "min_compression_rate": spec["mcr"],
                 "start_powerSGD_iter": 0, "use_error_feedback": True, "warm_start": True,

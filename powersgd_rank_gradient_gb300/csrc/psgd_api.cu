@@ -462,6 +462,7 @@ struct Ops {
                          const std::vector<int>& mask) {
     const int grid_items = std::max(1, std::min(a.n_items, s->sms * 3));
     const int grid_fine = std::max(1, std::min(a.n_fitems, s->sms * 2));
+    const int grid_p1 = std::max(1, std::min(a.n_fitems, s->sms));   // x CTAs per SM inside
     const int grid_q = std::max(1, std::min(a.n_gsq, s->sms * 4));
     const int grid_qr = std::max(1, std::min(a.n_qr, s->sms * 8));
     if (need_fresh) {
@@ -472,7 +473,7 @@ struct Ops {
       gs(s, a, L, 1);
     }
     L.begin(K_PASS1);
-    launch_pass1<RP>(a, grid_fine, L.st);
+    launch_pass1<RP>(a, grid_p1, L.st);
     L.end();
     gs(s, a, L, 0);
     L.begin(K_PASS2);

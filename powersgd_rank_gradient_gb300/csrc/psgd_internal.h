@@ -24,7 +24,7 @@ namespace psgd {
 constexpr int kThreads = 256;      // threads per CTA of the streaming passes
 constexpr int kRowBlock = 512;     // rows per work item of pass 2 (one Q partial each)
 constexpr int kFineRows = 64;      // rows per work item of pass 1 and pass 3
-constexpr int kGsRows = 1024;      // rows per work item of the Gram-Schmidt kernels
+constexpr int kGsRows = 256;       // rows per work item of the Gram-Schmidt kernels
 
 // Columns per thread (CPT) and column-tile width of the streaming passes for
 // a padded rank RP: the per-thread accumulators hold CPT x RP floats.

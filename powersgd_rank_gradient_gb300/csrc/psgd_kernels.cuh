@@ -342,23 +342,23 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int RP, int WT, typename GT, int RW>
+template <int RP, int WT, typename GT, int RW, int MINB>
 struct Pass1Stage {
   static constexpr int GB = 4 * (int)sizeof(GT);                 // gradient bytes per lane per unit row
   static constexpr int GSEG = 32 * GB;                            // one gradient row segment (warp)
   static constexpr int ESEG = 32 * 16;                            // one store row segment (warp)
   static constexpr int UNIT_BYTES = RW * WT * (GSEG + ESEG);      // per warp per unit
-  static constexpr int S_RAW = (200 * 1024) / (8 * UNIT_BYTES);
+  static constexpr int S_RAW = (200 * 1024 / MINB) / (8 * UNIT_BYTES);
   static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
   static constexpr int SMEM = 8 * S * UNIT_BYTES;                 // per CTA
 };
 
-template <int RP, int WT, typename GT, int RW>
+template <int RP, int WT, typename GT, int RW, int MINB>
 __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const TensorDesc& td, const Item& item,
                                                   const float* __restrict__ Qp, const float* __restrict__ Qc,
-                                                  const float* __restrict__ Pc, int cur, int& bad,
+                                                  const float* __restrict__ Pc, int cur, float& chk,
                                                   char* __restrict__ wsm) {
-  using St = Pass1Stage<RP, WT, GT, RW>;
+  using St = Pass1Stage<RP, WT, GT, RW, MINB>;
   constexpr int S = St::S;
   constexpr int GB = St::GB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -374,11 +374,15 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
   // a segment lane l owns bytes [l * width, (l + 1) * width), so a warp's
   // accesses to one segment are contiguous and free of bank conflicts.
 
-  auto issue = [&](int u) {
-    const int g = u / nchunks, ch = u - (u / nchunks) * nchunks;
-    const int rr = first + g * 8 * RW;
-    const int c = item.col0 + ch * 128 + lane * 4;
-    char* slot = wsm + (u % S) * St::UNIT_BYTES;
+  // unit u = (row group g, chunk ch); the issuer runs S - 1 units ahead of
+  // the consumer, each with its own counters.
+  int ig = 0, ich = 0, islot = 0;
+  auto issue = [&]() {
+    const int rr = first + ig * 8 * RW;
+    const int c = item.col0 + ich * 128 + lane * 4;
+    char* slot = wsm + islot * St::UNIT_BYTES;
+    if (++ich == nchunks) { ich = 0; ++ig; }
+    if (++islot == S) islot = 0;
 #pragma unroll
     for (int q = 0; q < RW; ++q) {
       if (rr + q >= item.nrows || c >= cend) continue;
@@ -399,14 +403,14 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 
 #pragma unroll
   for (int u = 0; u < S - 1; ++u) {
-    if (u < units) issue(u); else cp_async_commit();
+    if (u < units) issue(); else cp_async_commit();
   }
   float po[RW][RP];
   float pacc[RW][RP];
+  int g = 0, ch = 0, cslot = 0;
   for (int u = 0; u < units; ++u) {
     cp_async_wait<S - 2>();
-    if (u + S - 1 < units) issue(u + S - 1); else cp_async_commit();
-    const int g = u / nchunks, ch = u - (u / nchunks) * nchunks;
+    if (u + S - 1 < units) issue(); else cp_async_commit();
     const int rr = first + g * 8 * RW;
     const int c = item.col0 + ch * 128 + lane * 4;
     bool rv[RW];
@@ -422,15 +426,28 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
       }
     }
     if (c < cend) {
-      const char* slot = wsm + (u % S) * St::UNIT_BYTES;
-      float qv[4][RP];
+      const char* slot = wsm + cslot * St::UNIT_BYTES;
+      // Q columns c .. c+3: as one 4 x RP block for small RP, one column at a
+      // time (RP registers) for RP >= 16.
+      constexpr int QB = RP <= 8 ? 4 : 1;
+      float qv[QB][RP];
       float corr[RW][4];
       if (a.ef) {
-        load_qcols<RP, 4>(Qc + td.q_off, m, c, qv);
+        if constexpr (QB == 4) {
+          load_qcols<RP, 4>(Qc + td.q_off, m, c, qv);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-          for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qv[cc]);
+            for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qv[cc]);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+            for (int k = 0; k < RP; ++k) qv[0][k] = __ldg(Qc + td.q_off + (long long)k * m + c + cc);
+#pragma unroll
+            for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qv[0]);
+          }
+        }
       }
       float mb[RW][4];
 #pragma unroll
@@ -463,7 +480,7 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             const float v = gv[cc] * a.scale;
-            bad |= !isfinite(v);
+            chk = fmaf(v, 0.f, chk);   // stays 0 unless v is inf or NaN
             mv[cc] = a.ef ? v + (ev[cc] - corr[q][cc]) : v;
             mb[q][cc] += mv[cc];
           }
@@ -476,13 +493,25 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
         for (int cc = 0; cc < 4; ++cc) mb[q][cc] *= a.invW;
         if (a.mbar && rv[q]) store_f<4>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * m + c, mb[q]);
       }
-      if (!(a.ef && same_q)) load_qcols<RP, 4>(Qp + td.q_off, m, c, qv);
+      if constexpr (QB == 4) {
+        if (!(a.ef && same_q)) load_qcols<RP, 4>(Qp + td.q_off, m, c, qv);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int q = 0; q < RW; ++q)
+          for (int q = 0; q < RW; ++q)
 #pragma unroll
-          for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[cc][k], pacc[q][k]);
+            for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[cc][k], pacc[q][k]);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+          for (int k = 0; k < RP; ++k) qv[0][k] = __ldg(Qp + td.q_off + (long long)k * m + c + cc);
+#pragma unroll
+          for (int q = 0; q < RW; ++q)
+#pragma unroll
+            for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[0][k], pacc[q][k]);
+        }
+      }
     }
     if (ch == nchunks - 1) {
 #pragma unroll
@@ -496,14 +525,16 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
         }
       }
     }
+    if (++ch == nchunks) { ch = 0; ++g; }
+    if (++cslot == S) cslot = 0;
   }
   cp_async_wait<0>();
 }
 
-template <int RP, int WT, typename GT, int RW>
-__global__ void __launch_bounds__(kThreads) k_pass1_staged(const StepArgs a) {
+template <int RP, int WT, typename GT, int RW, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) k_pass1_staged(const StepArgs a) {
   extern __shared__ __align__(16) char p1smem[];
-  using St = Pass1Stage<RP, WT, GT, RW>;
+  using St = Pass1Stage<RP, WT, GT, RW, MINB>;
   const int cur = a.ctrl->cur;
   const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
   const float* Qc = a.Qf + (long long)cur * a.q_total;
@@ -511,14 +542,16 @@ __global__ void __launch_bounds__(kThreads) k_pass1_staged(const StepArgs a) {
   const float* Qp = use_init ? a.qinit : Qc;
   char* wsm = p1smem + (threadIdx.x >> 5) * (St::S * St::UNIT_BYTES);
   int bad = 0;
+  float chk = 0.f;
   for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
     const Item item = a.fitems[it];
     const TensorDesc td = a.tensors[item.t];
     if (td.vec && a.vec_ok)
-      pass1_tile_staged<RP, WT, GT, RW>(a, td, item, Qp, Qc, Pc, cur, bad, wsm);
+      pass1_tile_staged<RP, WT, GT, RW, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm);
     else
       pass1_tile<RP, WT, GT, RW, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
   }
+  bad |= !(chk == 0.f);
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
 }
 
@@ -737,7 +770,7 @@ __global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const floa
 // the W unscaled gradients (error feedback off).  Partials are k-major:
 // qpart[rb][k][j].
 // ---------------------------------------------------------------------------
-constexpr int kPStage = 64;
+constexpr int kPStage = 128;
 constexpr int kRowBatch = 8;
 
 // NC values of Mbar at (row, c0 ..) from the selected source; VEC: one

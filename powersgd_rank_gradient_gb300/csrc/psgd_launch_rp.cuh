@@ -7,35 +7,39 @@
 
 namespace psgd {
 
-template <int RP, int WT, typename GT, int RW>
+template <int RP, int WT, typename GT, int RW, int MINB>
 void launch_pass1_staged(const StepArgs& a, int grid, cudaStream_t s) {
-  using St = Pass1Stage<RP, WT, GT, RW>;
+  using St = Pass1Stage<RP, WT, GT, RW, MINB>;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(k_pass1_staged<RP, WT, GT, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize, St::SMEM);
+    cudaFuncSetAttribute(k_pass1_staged<RP, WT, GT, RW, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         St::SMEM);
     configured = true;
   }
-  k_pass1_staged<RP, WT, GT, RW><<<grid, kThreads, St::SMEM, s>>>(a);
+  k_pass1_staged<RP, WT, GT, RW, MINB><<<grid * MINB, kThreads, St::SMEM, s>>>(a);
 }
 
+// grid = one CTA per SM; the staged kernels run MINB CTAs per SM: two for
+// W <= 2 and RP <= 8, where a unit is small enough that two CTAs' stages and
+// registers fit, else one.
 template <int RP>
 void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
-  constexpr int RW = RP <= 8 ? 2 : 1;
+  constexpr int MB = RP <= 8 ? 2 : 1;
   if (a.f16) {
     switch (a.W) {
-      case 1: launch_pass1_staged<RP, 1, __half, RW>(a, grid, s); break;
-      case 2: launch_pass1_staged<RP, 2, __half, RW>(a, grid, s); break;
-      case 4: launch_pass1_staged<RP, 4, __half, 1>(a, grid, s); break;
-      case 8: launch_pass1_staged<RP, 8, __half, 1>(a, grid, s); break;
-      default: k_pass1<RP, 0, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 1: launch_pass1_staged<RP, 1, __half, 1, MB>(a, grid, s); break;
+      case 2: launch_pass1_staged<RP, 2, __half, 1, MB>(a, grid, s); break;
+      case 4: launch_pass1_staged<RP, 4, __half, 1, 1>(a, grid, s); break;
+      case 8: launch_pass1_staged<RP, 8, __half, 1, 1>(a, grid, s); break;
+      default: k_pass1<RP, 0, __half, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
     }
   } else {
     switch (a.W) {
-      case 1: launch_pass1_staged<RP, 1, float, RW>(a, grid, s); break;
-      case 2: launch_pass1_staged<RP, 2, float, RW>(a, grid, s); break;
-      case 4: launch_pass1_staged<RP, 4, float, 1>(a, grid, s); break;
-      case 8: launch_pass1_staged<RP, 8, float, 1>(a, grid, s); break;
-      default: k_pass1<RP, 0, float, 1><<<grid, kThreads, 0, s>>>(a); break;
+      case 1: launch_pass1_staged<RP, 1, float, 1, MB>(a, grid, s); break;
+      case 2: launch_pass1_staged<RP, 2, float, 1, MB>(a, grid, s); break;
+      case 4: launch_pass1_staged<RP, 4, float, 1, 1>(a, grid, s); break;
+      case 8: launch_pass1_staged<RP, 8, float, 1, 1>(a, grid, s); break;
+      default: k_pass1<RP, 0, float, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
     }
   }
 }
