@@ -227,6 +227,35 @@ int32_t psgd_profile_kinds(void);
 int psgd_profile_read(psgd_state* s, int32_t kind, const char** name, int64_t* launches,
                       double* total_ms, double* bytes_per_launch);
 
+/*
+ * psgd_project_q_static -- Q = M^T P for one matrix, allocating nothing.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot call cudaMalloc -- a job that reserved nearly all device memory up
+ * front, code whose device memory must come from a framework's own
+ * allocator, or latency-sensitive code that cannot afford cudaMalloc's
+ * implicit synchronisation.  It computes what pass 2 of psgd_step computes
+ * for one replica (Q(j, k) = sum_i M(i, j) P(i, k)), summing per block of
+ * 512 rows in row order and then over the blocks in block order, with those
+ * partial sums kept in a file-scope __device__ array of 2 Mi floats (8 MiB)
+ * that every GPU loading this library holds until the process exits.
+ *
+ *   dev_m  : device pointer, rows x cols floats, row-major.
+ *   dev_p  : device pointer, rows x rank floats, row-major.
+ *   dev_q  : device pointer, cols x rank floats, row-major (output).
+ *   rank   : 1 .. 32.
+ *   stream : cudaStream_t; the work is enqueued on it.
+ * Runs on the calling thread's current CUDA device; the first call on a
+ * device looks up the array's device address (make that first call before
+ * any stream capture).  Sizes with ceil(rows / 512) * next_pow2(rank) * cols
+ * above 2 Mi return PSGD_EINVAL.  Every call overwrites the whole part of the
+ * array it uses, so nothing carries over between calls, but calls that
+ * overlap on the GPU (other streams, other threads) race on the array.
+ * Errors: PSGD_EINVAL (NULL pointer, sizes), PSGD_ECUDA.
+ */
+int psgd_project_q_static(const float* dev_m, const float* dev_p, float* dev_q, int64_t rows,
+                          int64_t cols, int32_t rank, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* psgd_last_error(void);
 

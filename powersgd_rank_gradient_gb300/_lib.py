@@ -28,6 +28,7 @@ EXPORTS = [
     "psgd_step_status", "psgd_get_stats", "psgd_tensor_info", "psgd_error_numel", "psgd_set_q",
     "psgd_get_q", "psgd_get_p", "psgd_get_error", "psgd_set_error", "psgd_workspace_bytes",
     "psgd_profile", "psgd_profile_kinds", "psgd_profile_read", "psgd_last_error",
+    "psgd_project_q_static",
 ]
 
 _lib = None
@@ -91,6 +92,8 @@ def lib():
     L.psgd_profile_read.argtypes = [P, c_i32, ctypes.POINTER(ctypes.c_char_p), pi64,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
     L.psgd_profile_read.restype = ctypes.c_int
+    L.psgd_project_q_static.argtypes = [P, P, P, c_i64, c_i64, c_i32, P]
+    L.psgd_project_q_static.restype = ctypes.c_int
     L.psgd_last_error.argtypes = []
     L.psgd_last_error.restype = ctypes.c_char_p
     _lib = L

@@ -17,8 +17,17 @@
 using namespace psgd;
 
 namespace {
-
 thread_local std::string g_last_error;
+}  // namespace
+
+// Records the message psgd_last_error returns (also used by psgd_static.cu).
+int psgd_internal_set_error(int code, const char* msg) {
+  g_last_error = msg ? msg : "";
+  return code;
+}
+
+namespace {
+
 
 int fail(int code, const std::string& msg) {
   g_last_error = msg;
