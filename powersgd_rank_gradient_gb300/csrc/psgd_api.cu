@@ -107,9 +107,10 @@ int plan_tensors(const int64_t* dims, const int32_t* ndims, int32_t n, int32_t r
   return PSGD_OK;
 }
 
-enum Kind { K_MEAN = 0, K_PASS1, K_GRAM, K_SOLVE, K_APPLY, K_PASS2, K_QREDUCE, K_PASS3, K_COMMIT, K_RANDN, K_COUNT };
+enum Kind { K_MEAN = 0, K_PASS1, K_GRAM, K_SOLVE, K_APPLY, K_PASS2, K_QREDUCE, K_PASS3, K_COMMIT, K_RANDN,
+            K_PSUM, K_COUNT };
 const char* kKindNames[K_COUNT] = {"mean", "pass1", "gs_gram", "gs_solve", "gs_apply",
-                                   "pass2", "qreduce", "pass3", "commit", "randn"};
+                                   "pass2", "qreduce", "pass3", "commit", "randn", "psum"};
 
 struct EventPair {
   cudaEvent_t a, b;
@@ -135,7 +136,9 @@ struct psgd_state {
   std::vector<HostTensor> tensors;
   std::vector<TensorDesc> cdesc;
   std::vector<Item> items;    // pass 2
-  std::vector<Item> fitems;   // pass 1, pass 3, error views
+  std::vector<Item> fitems;   // pass 3, error views
+  std::vector<Item> p1items;  // pass 1
+  std::vector<GsItem> ps;     // P partial reduction chunks
   std::vector<GsItem> qr;     // Q partial reduction chunks
   std::vector<GsItem> gsp, gsq;
   std::vector<int> gsp_first, gsp_count, gsq_first, gsq_count;
@@ -147,6 +150,8 @@ struct psgd_state {
   TensorDesc* d_tensors = nullptr;
   Item* d_items = nullptr;
   Item* d_fitems = nullptr;
+  Item* d_p1items = nullptr;
+  GsItem* d_ps = nullptr;
   GsItem* d_qr = nullptr;
   GsItem* d_gsp = nullptr;
   GsItem* d_gsq = nullptr;
@@ -241,10 +246,13 @@ struct DeviceGuard {
 void build_plan(psgd_state* s) {
   const int RP = s->RP;
   const int CT = ctile_for(RP);
+  const int CT1 = ctile1_for(RP);
   s->cdesc.clear();
   s->items.clear();
   s->fitems.clear();
+  s->p1items.clear();
   s->qr.clear();
+  s->ps.clear();
   s->gsp.clear();
   s->gsq.clear();
   s->gsp_first.clear();
@@ -271,6 +279,7 @@ void build_plan(psgd_state* s) {
       td.m = (int)h.cols;
       td.r = h.rank;
       td.ctiles = (int)((h.cols + CT - 1) / CT);
+      td.ctiles1 = (int)((h.cols + CT1 - 1) / CT1);
       td.rblocks = (int)((h.rows + kRowBlock - 1) / kRowBlock);
       td.pp_off = pp_off;
       td.qp_off = qp_off;
@@ -283,7 +292,7 @@ void build_plan(psgd_state* s) {
       auto r32 = [](long long x) { return (x + 31) / 32 * 32; };
       p_off += h.rows * RP;
       q_off += r32(h.cols * RP);
-      pp_off += (long long)td.ctiles * h.rows * RP;
+      pp_off += (long long)td.ctiles1 * h.rows * RP;
       qp_off += r32((long long)td.rblocks * h.cols * RP);
       e_off += h.numel;
     } else {
@@ -317,17 +326,18 @@ void build_plan(psgd_state* s) {
       if (it == shapes.end()) shapes.push_back(sh);
     }
   }
-  auto make_items = [&](std::vector<Item>* out, int rows_per_item) {
+  auto make_items = [&](std::vector<Item>* out, int rows_per_item, int ctw) {
     for (size_t c = 0; c < s->cdesc.size(); ++c) {
       const TensorDesc& td = s->cdesc[c];
+      const int nct = (td.m + ctw - 1) / ctw;
       for (int r0 = 0; r0 < td.n; r0 += rows_per_item)
-        for (int ct = 0; ct < td.ctiles; ++ct) {
+        for (int ct = 0; ct < nct; ++ct) {
           Item it;
           it.t = (int)c;
           it.row0 = r0;
           it.nrows = std::min(rows_per_item, td.n - r0);
-          it.col0 = ct * CT;
-          it.ncols = std::min(CT, td.m - it.col0);
+          it.col0 = ct * ctw;
+          it.ncols = std::min(ctw, td.m - it.col0);
           it.rb = r0 / kRowBlock;
           it.ct = ct;
           it.pad = group_of[c];
@@ -342,12 +352,16 @@ void build_plan(psgd_state* s) {
     });
     for (auto& it : *out) it.pad = 0;
   };
-  make_items(&s->items, kRowBlock);
-  make_items(&s->fitems, kFineRows);
+  make_items(&s->items, kRowBlock, CT);
+  make_items(&s->fitems, kFineRows3, CT);
+  make_items(&s->p1items, kFineRows, CT1);
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const long long len = (long long)s->cdesc[c].m * RP;
     for (long long f = 0; f < len; f += 1024)
       s->qr.push_back({(int)c, (int)f, (int)std::min<long long>(1024, len - f), 0});
+    const long long plen = (long long)s->cdesc[c].n * RP;
+    for (long long f = 0; f < plen; f += 1024)
+      s->ps.push_back({(int)c, (int)f, (int)std::min<long long>(1024, plen - f), 0});
   }
 
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
@@ -388,6 +402,10 @@ StepArgs make_args(psgd_state* s) {
   a.n_items = (int)s->items.size();
   a.fitems = s->d_fitems;
   a.n_fitems = (int)s->fitems.size();
+  a.p1items = s->d_p1items;
+  a.n_p1items = (int)s->p1items.size();
+  a.ps_items = s->d_ps;
+  a.n_ps = (int)s->ps.size();
   a.qr_items = s->d_qr;
   a.n_qr = (int)s->qr.size();
   a.gsp_items = s->d_gsp;
@@ -441,11 +459,15 @@ struct Ops {
   static void gs(psgd_state* s, const StepArgs& a, Launcher& L, int is_q) {
     const int n_items = is_q ? a.n_gsq : a.n_gsp;
     const int grid = std::max(1, std::min(n_items, s->sms * 4));
-    const float* src = is_q ? s->qdraw : s->praw_part;
-    float* dense = is_q ? nullptr : s->praw;
     const float* src_dense = is_q ? s->qdraw : s->praw;
+    if (!is_q) {
+      // P_raw = sum of pass 1's column-tile partials
+      L.begin(K_PSUM);
+      launch_psum<RP>(a, std::max(1, std::min(a.n_ps, s->sms * 8)), L.st);
+      L.end();
+    }
     L.begin(K_GRAM);
-    launch_gram<RP>(a, src, dense, is_q, is_q ? 0 : 1, s->gram, grid, L.st);
+    launch_gram<RP>(a, src_dense, nullptr, is_q, 0, s->gram, grid, L.st);
     L.end();
     L.begin(K_SOLVE);
     launch_solve<RP>(a, s->gram, is_q, L.st);
@@ -471,7 +493,8 @@ struct Ops {
                          const std::vector<int>& mask) {
     const int grid_items = std::max(1, std::min(a.n_items, s->sms * 3));
     const int grid_fine = std::max(1, std::min(a.n_fitems, s->sms * 2));
-    const int grid_p1 = std::max(1, std::min(a.n_fitems, s->sms));   // x CTAs per SM inside
+    const int grid_p1 = std::max(1, std::min(a.n_p1items, s->sms));  // x CTAs per SM inside
+    const int grid_ps = std::max(1, std::min(a.n_ps, s->sms * 8));
     const int grid_q = std::max(1, std::min(a.n_gsq, s->sms * 4));
     const int grid_qr = std::max(1, std::min(a.n_qr, s->sms * 8));
     if (need_fresh) {
@@ -634,6 +657,8 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
   TRY(dupload(s, &s->d_tensors, s->cdesc));
   TRY(dupload(s, &s->d_items, s->items));
   TRY(dupload(s, &s->d_fitems, s->fitems));
+  TRY(dupload(s, &s->d_p1items, s->p1items));
+  TRY(dupload(s, &s->d_ps, s->ps));
   TRY(dupload(s, &s->d_qr, s->qr));
   TRY(dupload(s, &s->d_gsp, s->gsp));
   TRY(dupload(s, &s->d_gsq, s->gsq));

@@ -23,24 +23,30 @@ namespace psgd {
 
 constexpr int kThreads = 256;      // threads per CTA of the streaming passes
 constexpr int kRowBlock = 512;     // rows per work item of pass 2 (one Q partial each)
-constexpr int kFineRows = 64;      // rows per work item of pass 1 and pass 3
+constexpr int kFineRows = 64;      // rows per work item of pass 1
+constexpr int kFineRows3 = 32;     // rows per work item of pass 3 and the error views
 constexpr int kGsRows = 256;       // rows per work item of the Gram-Schmidt kernels
 
 // Columns per thread (CPT) and column-tile width of the streaming passes for
 // a padded rank RP: the per-thread accumulators hold CPT x RP floats.
 __host__ __device__ constexpr int cpt_for(int rp) { return rp <= 8 ? 4 : (rp == 16 ? 2 : 1); }
 __host__ __device__ constexpr int ctile_for(int rp) { return kThreads * cpt_for(rp); }
+// Column tile of pass 1: the tile's slice of Q (ctile1 x RP floats) stays at
+// or below 16 KB so that the Q slices of the CTAs sharing an SM stay in L1
+// next to their shared-memory stages.
+__host__ __device__ constexpr int ctile1_for(int rp) { return 4096 / rp < 1024 ? 4096 / rp : 1024; }
 
 struct TensorDesc {
   long long g_off;   // first element in the bucket
   long long c_off;   // first element in the packed error store / mbar
   long long p_off;   // first element of the tensor's P (rows x RP)
   long long q_off;   // first element of the tensor's Q (RP x cols, k-major; 32-aligned)
-  long long pp_off;  // first element of praw_part (ctiles x rows x RP)
+  long long pp_off;  // first element of praw_part (ctiles1 x rows x RP)
   long long qp_off;  // first element of qpart (rblocks x RP x cols; 32-aligned)
   long long e_off;   // first element in the user-visible packed error (no padding)
   int n, m, r;       // rows, cols, effective rank
-  int ctiles;        // column tiles
+  int ctiles;        // column tiles of passes 2 and 3
+  int ctiles1;       // column tiles of pass 1 (praw_part slices)
   int rblocks;       // row blocks
   int vec;           // rows are 16-byte aligned in the bucket (m % 4 == 0, g_off % 4 == 0)
 };

@@ -53,8 +53,12 @@ struct StepArgs {
   const TensorDesc* tensors;
   const Item* items;         // tall (row block) x (column tile) items: pass 2
   int n_items;
-  const Item* fitems;        // short items: pass 1, pass 3 and the error views
+  const Item* fitems;        // short items: pass 3 and the error views
   int n_fitems;
+  const Item* p1items;       // short items of pass 1 (its own column tiles)
+  int n_p1items;
+  const GsItem* ps_items;    // chunks of each tensor's P for the partial reduction
+  int n_ps;
   const GsItem* qr_items;    // chunks of each tensor's Q for the partial reduction
   int n_qr;
   const GsItem* gsp_items;   // rows of P
@@ -217,6 +221,37 @@ __device__ __forceinline__ float dot_chain(const float (&a)[RP], const float (&b
   return acc;
 }
 
+// Reduce RP per-lane values over the warp by recursive halving: each step
+// exchanges half of the remaining values with the lane `o` apart, so after
+// log2(RP) steps every lane holds one partial value, which the remaining
+// steps sum.  The total of value index (lane >> (5 - log2 RP)) ends in lane
+// `lane` (all 32 / RP lanes of a group hold the same total).
+template <int RP>
+__device__ __forceinline__ float warp_reduce_scatter(const float (&v)[RP]) {
+  float x[RP];
+#pragma unroll
+  for (int i = 0; i < RP; ++i) x[i] = v[i];
+  const int lane = threadIdx.x & 31;
+  int o = 16;
+#pragma unroll
+  for (int n = RP; n > 1; n >>= 1, o >>= 1) {
+    const int half = n >> 1;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? x[i] : x[i + half];
+      const float keep = up ? x[i + half] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float t = x[0];
+  for (; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+
+template <int RP>
+__host__ __device__ constexpr int log2_rp() { return RP >= 32 ? 5 : RP >= 16 ? 4 : RP >= 8 ? 3 : RP >= 4 ? 2 : RP >= 2 ? 1 : 0; }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -348,7 +383,11 @@ struct Pass1Stage {
   static constexpr int GSEG = 32 * GB;                            // one gradient row segment (warp)
   static constexpr int ESEG = 32 * 16;                            // one store row segment (warp)
   static constexpr int UNIT_BYTES = RW * WT * (GSEG + ESEG);      // per warp per unit
-  static constexpr int S_RAW = (200 * 1024 / MINB) / (8 * UNIT_BYTES);
+  // Shared-memory budget per CTA: 192 KB with one CTA per SM, 96 KB with two,
+  // 56 KB with three, so that the carve-out leaves L1 room for the CTAs' Q
+  // tiles next to the stages.
+  static constexpr int BUDGET = MINB == 1 ? 192 * 1024 : (MINB == 2 ? 96 * 1024 : (MINB == 3 ? 56 * 1024 : 40 * 1024));
+  static constexpr int S_RAW = BUDGET / (8 * UNIT_BYTES);
   static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
   static constexpr int SMEM = 8 * S * UNIT_BYTES;                 // per CTA
 };
@@ -370,30 +409,41 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
   const int ngroups = first < item.nrows ? (item.nrows - first + 8 * RW - 1) / (8 * RW) : 0;
   const int units = ngroups * nchunks;
   const bool same_q = (Qp == Qc);
+  const bool unit_scale = (a.scale == 1.0f);
   // slot layout: [q][w] gradient segments, then [q][w] store segments; inside
   // a segment lane l owns bytes [l * width, (l + 1) * width), so a warp's
   // accesses to one segment are contiguous and free of bank conflicts.
 
   // unit u = (row group g, chunk ch); the issuer runs S - 1 units ahead of
-  // the consumer, each with its own counters.
+  // the consumer, each with its own counters.  The issuer keeps the row start
+  // of every source (element offsets) and adds the chunk's column.
   int ig = 0, ich = 0, islot = 0;
+  long long grow[RW], erow[RW];
   auto issue = [&]() {
     const int rr = first + ig * 8 * RW;
+    if (ich == 0) {
+#pragma unroll
+      for (int q = 0; q < RW; ++q) {
+        const long long row = item.row0 + rr + q;
+        grow[q] = td.g_off + row * m;
+        erow[q] = (long long)cur * a.W * a.nc_pad + td.c_off + row * m;
+      }
+    }
     const int c = item.col0 + ich * 128 + lane * 4;
     char* slot = wsm + islot * St::UNIT_BYTES;
+    const bool cin = c < cend;
     if (++ich == nchunks) { ich = 0; ++ig; }
     if (++islot == S) islot = 0;
 #pragma unroll
     for (int q = 0; q < RW; ++q) {
-      if (rr + q >= item.nrows || c >= cend) continue;
-      const long long row = item.row0 + rr + q;
+      if (rr + q >= item.nrows || !cin) continue;
 #pragma unroll
       for (int w = 0; w < WT; ++w) {
-        const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c;
+        const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + grow[q] + c;
         char* gdst = slot + (q * WT + w) * St::GSEG + lane * GB;
         if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
         if (a.ef) {
-          const float* esrc = a.estore + ((long long)cur * a.W + w) * a.nc_pad + td.c_off + row * m + c;
+          const float* esrc = a.estore + erow[q] + (long long)w * a.nc_pad + c;
           cp_async16(slot + RW * WT * St::GSEG + (q * WT + w) * St::ESEG + lane * 16, esrc);
         }
       }
@@ -479,8 +529,7 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
           float mv[4];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
-            const float v = gv[cc] * a.scale;
-            chk = fmaf(v, 0.f, chk);   // stays 0 unless v is inf or NaN
+            const float v = unit_scale ? gv[cc] : gv[cc] * a.scale;
             mv[cc] = a.ef ? v + (ev[cc] - corr[q][cc]) : v;
             mb[q][cc] += mv[cc];
           }
@@ -516,12 +565,15 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
     if (ch == nchunks - 1) {
 #pragma unroll
       for (int q = 0; q < RW; ++q) {
-#pragma unroll
-        for (int k = 0; k < RP; ++k) pacc[q][k] = warp_sum(pacc[q][k]);
-        if (rv[q] && lane == 0) {
+        const float tot = warp_reduce_scatter<RP>(pacc[q]);
+        // An inf or NaN among the row's inputs reaches every sum it enters
+        // (inf * 0 is NaN), so the reduced partial is non-finite exactly when
+        // an input was (or the sums overflowed).
+        chk = fmaf(tot, 0.f, chk);
+        constexpr int SH = 5 - log2_rp<RP>();
+        if (rv[q] && (lane & ((1 << SH) - 1)) == 0) {
           float* dst = a.praw_part + td.pp_off + ((long long)item.ct * td.n + item.row0 + rr + q) * RP;
-#pragma unroll
-          for (int k = 0; k < RP; ++k) dst[k] = pacc[q][k];
+          dst[lane >> SH] = tot;
         }
       }
     }
@@ -529,6 +581,185 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
     if (++cslot == S) cslot = 0;
   }
   cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1, chunk-stationary (RP <= 8).  Warp w of the CTA owns chunk
+// (w % NCH) of the item's column tile (NCH = tile / 128 chunks of 128
+// columns) and every (8 / NCH)-th row of the item, so each lane loads the Q
+// values of its 4 columns once per item and keeps them in registers.  Its
+// source segments (one row x 128 columns of every replica's gradient and
+// store) are staged by cp.async S rows ahead, as in pass1_tile_staged.  Each
+// row's P partial over the chunk is reduced across the warp and parked in
+// shared memory; at the end of the item the CTA adds the chunk partials in
+// chunk order and writes one partial per (row, column tile).
+// ---------------------------------------------------------------------------
+template <int RP, int WT, typename GT, int MINB>
+struct Pass1CS {
+  static constexpr int NCH = ctile1_for(RP) / 128;                // chunks per column tile
+  static constexpr int WPC = 8 / NCH;                             // warps per chunk
+  static constexpr int GB = 4 * (int)sizeof(GT);
+  static constexpr int GSEG = 32 * GB;
+  static constexpr int ESEG = 32 * 16;
+  static constexpr int UNIT_BYTES = WT * (GSEG + ESEG);           // one row x 128 columns
+  static constexpr int RED_BYTES = kFineRows * NCH * RP * 4;
+  static constexpr int BUDGET = (MINB == 1 ? 200 * 1024 : 96 * 1024) - RED_BYTES;
+  static constexpr int S_RAW = BUDGET / (8 * UNIT_BYTES);
+  static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
+  static constexpr int SMEM = 8 * S * UNIT_BYTES + RED_BYTES;
+};
+
+template <int RP, int WT, typename GT, int MINB>
+__device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDesc& td, const Item& item,
+                                              const float* __restrict__ Qp, const float* __restrict__ Qc,
+                                              const float* __restrict__ Pc, int cur, float& chk,
+                                              char* __restrict__ wsm, float* __restrict__ red) {
+  using St = Pass1CS<RP, WT, GT, MINB>;
+  constexpr int S = St::S;
+  constexpr int GB = St::GB;
+  constexpr int NCH = St::NCH;
+  constexpr int WPC = St::WPC;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nxt = cur ^ 1;
+  const long long m = td.m;
+  const int cend = item.col0 + item.ncols;
+  const int nch = (item.ncols + 127) / 128;
+  const int ch = warp % NCH;
+  const int phase = warp / NCH;
+  const bool unit_scale = (a.scale == 1.0f);
+  const bool same_q = (Qp == Qc);
+  if (ch < nch) {
+    const int c = item.col0 + ch * 128 + lane * 4;
+    const bool cin = c < cend;
+    const int units = phase < item.nrows ? (item.nrows - phase + WPC - 1) / WPC : 0;
+    float qc[4][RP], qp[4][RP];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+      for (int k = 0; k < RP; ++k) { qc[cc][k] = 0.f; qp[cc][k] = 0.f; }
+    if (cin) {
+      if (a.ef) load_qcols<RP, 4>(Qc + td.q_off, m, c, qc);
+      if (!(a.ef && same_q)) load_qcols<RP, 4>(Qp + td.q_off, m, c, qp);
+    }
+    auto issue = [&](int u) {
+      char* slot = wsm + (u % S) * St::UNIT_BYTES;
+      if (cin) {
+        const long long row = item.row0 + phase + (long long)u * WPC;
+        const long long go = td.g_off + row * m + c;
+        const long long eo = (long long)cur * a.W * a.nc_pad + td.c_off + row * m + c;
+#pragma unroll
+        for (int w = 0; w < WT; ++w) {
+          const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
+          char* gdst = slot + w * St::GSEG + lane * GB;
+          if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+          if (a.ef) cp_async16(slot + WT * St::GSEG + w * St::ESEG + lane * 16, a.estore + eo + (long long)w * a.nc_pad);
+        }
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int u = 0; u < S - 1; ++u) {
+      if (u < units) issue(u); else cp_async_commit();
+    }
+    for (int u = 0; u < units; ++u) {
+      cp_async_wait<S - 2>();
+      if (u + S - 1 < units) issue(u + S - 1); else cp_async_commit();
+      const int rr = phase + u * WPC;
+      const long long i = item.row0 + rr;
+      float pacc[RP];
+#pragma unroll
+      for (int k = 0; k < RP; ++k) pacc[k] = 0.f;
+      if (cin) {
+        const char* slot = wsm + (u % S) * St::UNIT_BYTES;
+        float corr[4] = {0.f, 0.f, 0.f, 0.f};
+        if (a.ef) {
+          float po[RP];
+          load_row<RP>(Pc + td.p_off + i * RP, po);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) corr[cc] = dot_chain<RP>(po, qc[cc]);
+        }
+        float mb[4] = {0.f, 0.f, 0.f, 0.f};
+        float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + td.c_off + i * m + c;
+#pragma unroll
+        for (int w = 0; w < WT; ++w) {
+          float gv[4];
+          if constexpr (GB == 16) {
+            const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
+            gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
+          } else {
+            const uint2 raw = *reinterpret_cast<const uint2*>(slot + w * St::GSEG + lane * GB);
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+            gv[0] = fa.x; gv[1] = fa.y; gv[2] = fb.x; gv[3] = fb.y;
+          }
+          float mv[4];
+          if (a.ef) {
+            const float4 x = *reinterpret_cast<const float4*>(slot + WT * St::GSEG + w * St::ESEG + lane * 16);
+            const float ev[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const float v = unit_scale ? gv[cc] : gv[cc] * a.scale;
+              mv[cc] = v + (ev[cc] - corr[cc]);
+              mb[cc] += mv[cc];
+            }
+            store_f<4>(enxt + (long long)w * a.nc_pad, mv);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              mv[cc] = unit_scale ? gv[cc] : gv[cc] * a.scale;
+              mb[cc] += mv[cc];
+            }
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) mb[cc] *= a.invW;
+        if (a.mbar) store_f<4>(a.mbar + td.c_off + i * m + c, mb);
+        const float (*qq)[RP] = (a.ef && same_q) ? qc : qp;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int k = 0; k < RP; ++k) pacc[k] = fmaf(mb[cc], qq[cc][k], pacc[k]);
+      }
+      const float tot = warp_reduce_scatter<RP>(pacc);
+      chk = fmaf(tot, 0.f, chk);   // inf/NaN in the row's inputs reach the sums
+      constexpr int SH = 5 - log2_rp<RP>();
+      if ((lane & ((1 << SH) - 1)) == 0) red[(rr * NCH + ch) * RP + (lane >> SH)] = tot;
+    }
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < item.nrows * RP; e += kThreads) {
+    const int rr = e / RP, k = e - (e / RP) * RP;
+    float v = 0.f;
+    for (int h = 0; h < nch; ++h) v += red[(rr * NCH + h) * RP + k];
+    a.praw_part[td.pp_off + ((long long)item.ct * td.n + item.row0 + rr) * RP + k] = v;
+  }
+  __syncthreads();
+}
+
+template <int RP, int WT, typename GT, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
+  extern __shared__ __align__(16) char p1smem[];
+  using St = Pass1CS<RP, WT, GT, MINB>;
+  const int cur = a.ctrl->cur;
+  const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
+  const float* Qc = a.Qf + (long long)cur * a.q_total;
+  const float* Pc = a.Pf + (long long)cur * a.p_total;
+  const float* Qp = use_init ? a.qinit : Qc;
+  char* wsm = p1smem + (threadIdx.x >> 5) * (St::S * St::UNIT_BYTES);
+  float* red = reinterpret_cast<float*>(p1smem + 8 * St::S * St::UNIT_BYTES);
+  int bad = 0;
+  float chk = 0.f;
+  for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
+    const Item item = a.p1items[it];
+    const TensorDesc td = a.tensors[item.t];
+    if (td.vec && a.vec_ok)
+      pass1_tile_cs<RP, WT, GT, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+    else
+      pass1_tile<RP, WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
+  }
+  bad |= !(chk == 0.f);
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
 }
 
 template <int RP, int WT, typename GT, int RW, int MINB>
@@ -543,8 +774,8 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_staged(const StepArgs 
   char* wsm = p1smem + (threadIdx.x >> 5) * (St::S * St::UNIT_BYTES);
   int bad = 0;
   float chk = 0.f;
-  for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
-    const Item item = a.fitems[it];
+  for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
+    const Item item = a.p1items[it];
     const TensorDesc td = a.tensors[item.t];
     if (td.vec && a.vec_ok)
       pass1_tile_staged<RP, WT, GT, RW, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm);
@@ -563,8 +794,8 @@ __global__ void __launch_bounds__(kThreads) k_pass1(const StepArgs a) {
   const float* Pc = a.Pf + (long long)cur * a.p_total;
   const float* Qp = use_init ? a.qinit : Qc;
   int bad = 0;
-  for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
-    const Item item = a.fitems[it];
+  for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
+    const Item item = a.p1items[it];
     const TensorDesc td = a.tensors[item.t];
     if (td.vec && a.vec_ok)
       pass1_tile<RP, WT, GT, RW, 4>(a, td, item, Qp, Qc, Pc, cur, bad);
@@ -587,6 +818,44 @@ __global__ void __launch_bounds__(kThreads) k_pass1(const StepArgs a) {
 // re-orthogonalises the first sweep's output), which keeps P^T P = I to fp32
 // rounding even when X is ill conditioned.
 // ---------------------------------------------------------------------------
+// P_raw = sum of pass 1's column-tile partials, in tile order (the Gram stage
+// then reads dense rows).  Each work item is a chunk of one tensor's rows x RP
+// values, four per thread.
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
+  if (a.ctrl->flag) return;
+  for (int it = blockIdx.x; it < a.n_ps; it += gridDim.x) {
+    const GsItem gi = a.ps_items[it];
+    const TensorDesc td = a.tensors[gi.t];
+    const long long len = (long long)td.n * RP;
+    const float* src = a.praw_part + td.pp_off;
+    const int f = gi.row0 + threadIdx.x * 4;
+    if (f >= gi.row0 + gi.nrows) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (RP >= 4) {
+      int c = 0;
+      for (; c + 4 <= td.ctiles1; c += 4) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = *reinterpret_cast<const float4*>(src + (long long)(c + u) * len + f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) { acc.x += x[u].x; acc.y += x[u].y; acc.z += x[u].z; acc.w += x[u].w; }
+      }
+      for (; c < td.ctiles1; ++c) {
+        const float4 x = *reinterpret_cast<const float4*>(src + (long long)c * len + f);
+        acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+      }
+      *reinterpret_cast<float4*>(a.praw + td.p_off + f) = acc;
+    } else {
+      for (int e = f; e < min(f + 4, gi.row0 + gi.nrows); ++e) {
+        float v = 0.f;
+        for (int c = 0; c < td.ctiles1; ++c) v += src[(long long)c * len + e];
+        a.praw[td.p_off + e] = v;
+      }
+    }
+  }
+}
+
 constexpr int kGramTile = 128;
 
 // Rows of P live as column-tile partials (nparts > 1) or dense (nparts == 1).
@@ -620,7 +889,7 @@ __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float
         float v;
         if (from_parts) {
           v = 0.f;
-          for (int c = 0; c < td.ctiles; ++c) v += src[td.pp_off + ((long long)c * td.n + row) * RP + k];
+          for (int c = 0; c < td.ctiles1; ++c) v += src[td.pp_off + ((long long)c * td.n + row) * RP + k];
         } else if (is_q) {
           v = src[base + (long long)k * td.m + row];
         } else {

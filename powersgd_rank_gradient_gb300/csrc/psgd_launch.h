@@ -10,6 +10,7 @@ namespace psgd {
 struct StepArgs;
 
 template <int RP> void launch_pass1(const StepArgs& a, int grid, cudaStream_t s);
+template <int RP> void launch_psum(const StepArgs& a, int grid, cudaStream_t s);
 template <int RP> void launch_gram(const StepArgs& a, const float* src, float* dense_out, int is_q,
                                    int from_parts, double* gram, int grid, cudaStream_t s);
 template <int RP> void launch_solve(const StepArgs& a, const double* gram, int is_q, cudaStream_t s);

@@ -19,29 +19,64 @@ void launch_pass1_staged(const StepArgs& a, int grid, cudaStream_t s) {
   k_pass1_staged<RP, WT, GT, RW, MINB><<<grid * MINB, kThreads, St::SMEM, s>>>(a);
 }
 
-// grid = one CTA per SM; the staged kernels run MINB CTAs per SM: two for
-// W <= 2 and RP <= 8, where a unit is small enough that two CTAs' stages and
-// registers fit, else one.
+template <int RP, int WT, typename GT, int MINB>
+void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
+  using St = Pass1CS<RP, WT, GT, MINB>;
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, St::SMEM);
+    configured = true;
+  }
+  k_pass1_cs<RP, WT, GT, MINB><<<grid * MINB, kThreads, St::SMEM, s>>>(a);
+}
+
+// grid = one CTA per SM; the kernels run MINB CTAs per SM.  Ranks up to 8 use
+// the chunk-stationary kernel (two CTAs per SM for W <= 2, one above); ranks
+// 16 and 32 keep Q in L1 and use pass1_tile_staged (one CTA per SM).
 template <int RP>
 void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
-  constexpr int MB = RP <= 8 ? 2 : 1;
-  if (a.f16) {
-    switch (a.W) {
-      case 1: launch_pass1_staged<RP, 1, __half, 1, MB>(a, grid, s); break;
-      case 2: launch_pass1_staged<RP, 2, __half, 1, MB>(a, grid, s); break;
-      case 4: launch_pass1_staged<RP, 4, __half, 1, 1>(a, grid, s); break;
-      case 8: launch_pass1_staged<RP, 8, __half, 1, 1>(a, grid, s); break;
-      default: k_pass1<RP, 0, __half, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+  if constexpr (RP <= 8) {
+    if (a.f16) {
+      switch (a.W) {
+        case 1: launch_pass1_cs<RP, 1, __half, 2>(a, grid, s); break;
+        case 2: launch_pass1_cs<RP, 2, __half, 2>(a, grid, s); break;
+        case 4: launch_pass1_cs<RP, 4, __half, 1>(a, grid, s); break;
+        case 8: launch_pass1_cs<RP, 8, __half, 1>(a, grid, s); break;
+        default: k_pass1<RP, 0, __half, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+      }
+    } else {
+      switch (a.W) {
+        case 1: launch_pass1_cs<RP, 1, float, 2>(a, grid, s); break;
+        case 2: launch_pass1_cs<RP, 2, float, 2>(a, grid, s); break;
+        case 4: launch_pass1_cs<RP, 4, float, 1>(a, grid, s); break;
+        case 8: launch_pass1_cs<RP, 8, float, 1>(a, grid, s); break;
+        default: k_pass1<RP, 0, float, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+      }
     }
   } else {
-    switch (a.W) {
-      case 1: launch_pass1_staged<RP, 1, float, 1, MB>(a, grid, s); break;
-      case 2: launch_pass1_staged<RP, 2, float, 1, MB>(a, grid, s); break;
-      case 4: launch_pass1_staged<RP, 4, float, 1, 1>(a, grid, s); break;
-      case 8: launch_pass1_staged<RP, 8, float, 1, 1>(a, grid, s); break;
-      default: k_pass1<RP, 0, float, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+    if (a.f16) {
+      switch (a.W) {
+        case 1: launch_pass1_staged<RP, 1, __half, 1, 1>(a, grid, s); break;
+        case 2: launch_pass1_staged<RP, 2, __half, 1, 1>(a, grid, s); break;
+        case 4: launch_pass1_staged<RP, 4, __half, 1, 1>(a, grid, s); break;
+        case 8: launch_pass1_staged<RP, 8, __half, 1, 1>(a, grid, s); break;
+        default: k_pass1<RP, 0, __half, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+      }
+    } else {
+      switch (a.W) {
+        case 1: launch_pass1_staged<RP, 1, float, 1, 1>(a, grid, s); break;
+        case 2: launch_pass1_staged<RP, 2, float, 1, 1>(a, grid, s); break;
+        case 4: launch_pass1_staged<RP, 4, float, 1, 1>(a, grid, s); break;
+        case 8: launch_pass1_staged<RP, 8, float, 1, 1>(a, grid, s); break;
+        default: k_pass1<RP, 0, float, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+      }
     }
   }
+}
+
+template <int RP>
+void launch_psum(const StepArgs& a, int grid, cudaStream_t s) {
+  k_psum<RP><<<grid, kThreads, 0, s>>>(a);
 }
 
 template <int RP>
@@ -107,6 +142,7 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
 
 #define PSGD_INSTANTIATE(RPV)                                                                   \
   template void launch_pass1<RPV>(const StepArgs&, int, cudaStream_t);                          \
+  template void launch_psum<RPV>(const StepArgs&, int, cudaStream_t);                           \
   template void launch_gram<RPV>(const StepArgs&, const float*, float*, int, int, double*, int, \
                                  cudaStream_t);                                                 \
   template void launch_solve<RPV>(const StepArgs&, const double*, int, cudaStream_t);           \
