@@ -202,6 +202,27 @@ class Clocks:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (one independent replica of the workload per GPU)
+# ---------------------------------------------------------------------------
+def reduce_max(x, dist, device=None):
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step, steps, ranks, max_ms):
+    """Whole-job GB/s: every rank processed `steps` steps of
+    `bytes_per_rank_step` bytes; the job took the slowest rank's time."""
+    return bytes_per_rank_step * steps * ranks / (max_ms / 1e3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
 def run_native(spec, args, dist, rank_id, world, device):
@@ -248,17 +269,13 @@ def run_native(spec, args, dist, rank_id, world, device):
         dist.barrier()
     clk = clocks.stop() if rank_id == 0 else None
     st.profile(False)
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(e0.elapsed_time(e1), dist, device)
     if st.status():
         raise RuntimeError("timed step was skipped (non-finite input)")
     prof = st.profile_read()
     ms_step = ms / args.steps
     grad_bytes = W * N * 4
-    value = grad_bytes * args.steps * world / (ms / 1e3) / 1e9
+    value = job_throughput(grad_bytes, args.steps, world, ms)
     launches = sum(v[0] for v in prof.values())
     # dominant kernel by device time
     kern = max((k for k in prof if prof[k][0] > 0), key=lambda k: prof[k][1])
@@ -319,15 +336,9 @@ def run_e2e(st, spec, args, dist, device, N, W):
         st.step_host(host, host_out)
     e1.record(stream)
     torch.cuda.synchronize(device)
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        ws = dist.get_world_size()
-    else:
-        ws = 1
-    return {"value": W * N * 4 * k * ws / (ms / 1e3) / 1e9, "unit": UNIT,
+    ms = reduce_max(e0.elapsed_time(e1), dist, device)
+    ws = dist.get_world_size() if dist is not None else 1
+    return {"value": job_throughput(W * N * 4, k, ws, ms), "unit": UNIT,
             "h2d_bytes_per_step": W * N * 4, "d2h_bytes_per_step": N * 4, "ms_per_step": ms / k}
 
 
