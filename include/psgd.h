@@ -133,13 +133,19 @@ int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_los
 
 /*
  * psgd_step_host -- psgd_step on HOST buffers: copies the W host buckets to
- * the device (one cudaMemcpyAsync per replica; pinned memory makes them
- * asynchronous), runs the step and copies `out` back to host memory, all on
- * `stream`.  The device staging buffers are allocated on the first call (so
- * the first call may return PSGD_ENOMEM) and reused afterwards.
+ * the device (one cudaMemcpyAsync per replica), runs the step and copies
+ * `out` back to host memory.  Two device staging sets are allocated on the
+ * first call (so the first call may return PSGD_ENOMEM) and alternated call
+ * by call: the uploads run on an internal stream and wait only for the
+ * download that last used the same set, the step runs on `stream` after the
+ * uploads, and the download runs on a second internal stream after the step.
+ * `stream` then waits for the download, so host_out is valid once `stream`
+ * is synchronised, and consecutive calls overlap the next upload with the
+ * current step and download.  Pinned host memory makes the copies
+ * asynchronous; the host buffers must stay untouched until `stream` is
+ * synchronised.
  *   host_grads[W] : host pointers, N elements of grad_dtype each.
  *   host_out      : host pointer, N floats.
- * Returns after enqueueing; host_out is valid once the stream is synchronised.
  */
 int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out,
                    float inv_loss_scale, void* stream);

@@ -176,9 +176,14 @@ struct psgd_state {
   int* h_status = nullptr;  // pinned
   size_t bytes = 0;
   std::vector<void*> allocs;
-  // host staging for psgd_step_host
-  std::vector<void*> stage_grads;
-  float* stage_out = nullptr;
+  // host staging for psgd_step_host: two sets, alternated call by call, so
+  // that the next call's uploads overlap this call's compute and download
+  std::vector<void*> stage_grads[2];
+  float* stage_out[2] = {nullptr, nullptr};
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
+  int set_used[2] = {0, 0};
+  long long host_calls = 0;
   // counters
   long long iter = 0;
   long long compressed_launched = 0;
@@ -578,8 +583,15 @@ void psgd_state_destroy(psgd_state* s) {
   if (!s) return;
   DeviceGuard g(s->device);
   for (void* p : s->allocs) cudaFree(p);
-  for (void* p : s->stage_grads) cudaFree(p);
-  if (s->stage_out) cudaFree(s->stage_out);
+  for (int k = 0; k < 2; ++k) {
+    for (void* p : s->stage_grads[k]) cudaFree(p);
+    if (s->stage_out[k]) cudaFree(s->stage_out[k]);
+    if (s->ev_in[k]) cudaEventDestroy(s->ev_in[k]);
+    if (s->ev_comp[k]) cudaEventDestroy(s->ev_comp[k]);
+    if (s->ev_free[k]) cudaEventDestroy(s->ev_free[k]);
+  }
+  if (s->s_in) cudaStreamDestroy(s->s_in);
+  if (s->s_out) cudaStreamDestroy(s->s_out);
   if (s->h_status) cudaFreeHost(s->h_status);
   for (auto& v : s->ev)
     for (auto& e : v) {
@@ -782,38 +794,80 @@ int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_los
   return PSGD_OK;
 }
 
+namespace {
+// Allocates the two staging sets, the copy streams and their events.
+int host_staging_init(psgd_state* s) {
+  const size_t gsz = s->dtype == PSGD_F16 ? 2 : 4;
+  for (int k = 0; k < 2; ++k) {
+    s->stage_grads[k].assign(s->W, nullptr);
+    for (int w = 0; w < s->W; ++w)
+      if (cudaMalloc(&s->stage_grads[k][w], std::max<size_t>(16, s->N * gsz)) != cudaSuccess) goto oom;
+    if (cudaMalloc((void**)&s->stage_out[k], std::max<size_t>(16, s->N * 4)) != cudaSuccess) goto oom;
+    if (cudaEventCreateWithFlags(&s->ev_in[k], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s->ev_comp[k], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s->ev_free[k], cudaEventDisableTiming) != cudaSuccess)
+      goto cuda_err;
+  }
+  if (cudaStreamCreateWithFlags(&s->s_in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&s->s_out, cudaStreamNonBlocking) != cudaSuccess)
+    goto cuda_err;
+  return PSGD_OK;
+oom:
+  cudaGetLastError();
+  return fail(PSGD_ENOMEM, "psgd_step_host: staging buffers");
+cuda_err:
+  cudaGetLastError();
+  return fail(PSGD_ECUDA, "psgd_step_host: streams/events");
+}
+
+void host_staging_free(psgd_state* s) {
+  for (int k = 0; k < 2; ++k) {
+    for (void* p : s->stage_grads[k])
+      if (p) cudaFree(p);
+    s->stage_grads[k].clear();
+    if (s->stage_out[k]) cudaFree(s->stage_out[k]);
+    s->stage_out[k] = nullptr;
+  }
+}
+}  // namespace
+
+// Call k uses staging set k % 2.  Uploads run on an internal stream and wait
+// only for the download that last used the same set; the step runs on the
+// caller's stream after the uploads; the download runs on a second internal
+// stream after the step, and the caller's stream waits for it, so host_out
+// is valid once the caller's stream is synchronised.  Consecutive calls thus
+// overlap the next upload with the current compute and download.
 int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out, float inv_loss_scale,
                    void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
   if (!host_grads || !host_out) return fail(PSGD_EINVAL, "host_grads/host_out is NULL");
+  for (int w = 0; w < s->W; ++w)
+    if (!host_grads[w]) return fail(PSGD_EINVAL, "host_grads[w] is NULL");
   DeviceGuard g(s->device);
   const size_t gsz = s->dtype == PSGD_F16 ? 2 : 4;
-  if (s->stage_grads.empty()) {
-    s->stage_grads.assign(s->W, nullptr);
-    for (int w = 0; w < s->W; ++w) {
-      if (cudaMalloc(&s->stage_grads[w], std::max<size_t>(16, s->N * gsz)) != cudaSuccess) {
-        cudaGetLastError();
-        for (void* p : s->stage_grads)
-          if (p) cudaFree(p);
-        s->stage_grads.clear();
-        return fail(PSGD_ENOMEM, "staging buffers");
-      }
-    }
-    if (cudaMalloc((void**)&s->stage_out, std::max<size_t>(16, s->N * 4)) != cudaSuccess) {
-      cudaGetLastError();
-      for (void* p : s->stage_grads) cudaFree(p);
-      s->stage_grads.clear();
-      return fail(PSGD_ENOMEM, "staging buffers");
+  if (!s->s_in) {
+    int rc = host_staging_init(s);
+    if (rc) {
+      host_staging_free(s);
+      return rc;
     }
   }
   cudaStream_t st = (cudaStream_t)stream;
-  for (int w = 0; w < s->W; ++w) {
-    if (!host_grads[w]) return fail(PSGD_EINVAL, "host_grads[w] is NULL");
-    PSGD_CUDA_TRY(cudaMemcpyAsync(s->stage_grads[w], host_grads[w], s->N * gsz, cudaMemcpyHostToDevice, st));
-  }
-  int rc = psgd_step(s, (const void* const*)s->stage_grads.data(), s->stage_out, inv_loss_scale, stream);
+  const int k = (int)(s->host_calls & 1);
+  if (s->set_used[k]) PSGD_CUDA_TRY(cudaStreamWaitEvent(s->s_in, s->ev_free[k], 0));
+  for (int w = 0; w < s->W; ++w)
+    PSGD_CUDA_TRY(cudaMemcpyAsync(s->stage_grads[k][w], host_grads[w], s->N * gsz, cudaMemcpyHostToDevice, s->s_in));
+  PSGD_CUDA_TRY(cudaEventRecord(s->ev_in[k], s->s_in));
+  PSGD_CUDA_TRY(cudaStreamWaitEvent(st, s->ev_in[k], 0));
+  int rc = psgd_step(s, (const void* const*)s->stage_grads[k].data(), s->stage_out[k], inv_loss_scale, stream);
   if (rc) return rc;
-  PSGD_CUDA_TRY(cudaMemcpyAsync(host_out, s->stage_out, s->N * 4, cudaMemcpyDeviceToHost, st));
+  PSGD_CUDA_TRY(cudaEventRecord(s->ev_comp[k], st));
+  PSGD_CUDA_TRY(cudaStreamWaitEvent(s->s_out, s->ev_comp[k], 0));
+  PSGD_CUDA_TRY(cudaMemcpyAsync(host_out, s->stage_out[k], s->N * 4, cudaMemcpyDeviceToHost, s->s_out));
+  PSGD_CUDA_TRY(cudaEventRecord(s->ev_free[k], s->s_out));
+  PSGD_CUDA_TRY(cudaStreamWaitEvent(st, s->ev_free[k], 0));
+  s->set_used[k] = 1;
+  s->host_calls++;
   return PSGD_OK;
 }
 

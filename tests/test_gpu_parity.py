@@ -303,3 +303,27 @@ def test_empty_and_vector_only_buckets():
 def test_rank_sweep_8192(rank):
     """8192 x 8192, W=1, N(0,1): two warm-started steps per rank."""
     _run([(8192, 8192)], 1, rank, 2, min_compression_rate=2.0, label=f"8192 r={rank}")
+
+
+def test_step_host_matches_device_path():
+    """psgd_step_host (host buffers in and out, pipelined across calls) gives
+    the same bits as psgd_step on device buffers, call after call."""
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = MIXED
+    kw = dict(matrix_approximation_rank=4, start_powerSGD_iter=1, min_compression_rate=1.0,
+              random_seed=5, device=DEV)
+    dev_state = PowerSGDState(shapes, 3, **kw)
+    host_state = PowerSGDState(shapes, 3, **kw)
+    steps = 5
+    host_in = [[torch.from_numpy(x).pin_memory() for x in grads_for(shapes, 3, step)] for step in range(steps)]
+    host_out = [torch.empty(dev_state.numel, dtype=torch.float32).pin_memory() for _ in range(steps)]
+    # enqueue every host call back to back (the pipelined case), then compare
+    for step in range(steps):
+        host_state.step_host(host_in[step], host_out[step])
+    torch.cuda.synchronize()
+    for step in range(steps):
+        out = dev_state.step([h.to(DEV) for h in host_in[step]])
+        assert torch.equal(out.cpu(), host_out[step]), f"step {step}"
+    dev_state.close()
+    host_state.close()
