@@ -31,10 +31,10 @@ constexpr int kGsRows = 256;       // rows per work item of the Gram-Schmidt ker
 // a padded rank RP: the per-thread accumulators hold CPT x RP floats.
 __host__ __device__ constexpr int cpt_for(int rp) { return rp <= 8 ? 4 : (rp == 16 ? 2 : 1); }
 __host__ __device__ constexpr int ctile_for(int rp) { return kThreads * cpt_for(rp); }
-// Column tile of pass 1: the tile's slice of Q (ctile1 x RP floats) stays at
-// or below 16 KB so that the Q slices of the CTAs sharing an SM stay in L1
-// next to their shared-memory stages.
-__host__ __device__ constexpr int ctile1_for(int rp) { return 4096 / rp < 1024 ? 4096 / rp : 1024; }
+// Column tile of pass 1: 1024 columns (eight 128-column chunks, one per warp)
+// for ranks up to 8; for larger ranks the tile's slice of Q (ctile1 x RP
+// floats) stays at 32 KB so that it stays in L1 next to the stages.
+__host__ __device__ constexpr int ctile1_for(int rp) { return 8192 / rp < 1024 ? 8192 / rp : 1024; }
 
 struct TensorDesc {
   long long g_off;   // first element in the bucket

@@ -1157,7 +1157,7 @@ __device__ __forceinline__ void pass2_tile(const StepArgs& a, const TensorDesc& 
 // take the element-wise path (NC = 1): same CPT columns per thread, one access
 // per element.
 template <int RP, int SRC, typename GT, int WT>
-__global__ void __launch_bounds__(kThreads) k_pass2(const StepArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_pass2(const StepArgs a) {
   __shared__ __align__(16) float ps[kPStage][RP];
   if (a.ctrl->flag) return;
   const float* P = a.Pf + (long long)(a.ctrl->cur ^ 1) * a.p_total;
