@@ -371,11 +371,15 @@ void build_plan(psgd_state* s) {
 
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const TensorDesc& td = s->cdesc[c];
+    // Gram-Schmidt items (one Gram partial each): kGsRows rows, fewer for
+    // large ranks so that a single tall matrix still spreads over many CTAs
+    const int per_p = std::max(64, std::min(kGsRows, 2048 / RP));
+    const int per_q = per_p;
     s->gsp_first.push_back((int)s->gsp.size());
-    for (int r0 = 0; r0 < td.n; r0 += kGsRows) s->gsp.push_back({(int)c, r0, std::min(kGsRows, td.n - r0), 0});
+    for (int r0 = 0; r0 < td.n; r0 += per_p) s->gsp.push_back({(int)c, r0, std::min(per_p, td.n - r0), 0});
     s->gsp_count.push_back((int)s->gsp.size() - s->gsp_first.back());
     s->gsq_first.push_back((int)s->gsq.size());
-    for (int r0 = 0; r0 < td.m; r0 += kGsRows) s->gsq.push_back({(int)c, r0, std::min(kGsRows, td.m - r0), 0});
+    for (int r0 = 0; r0 < td.m; r0 += per_q) s->gsq.push_back({(int)c, r0, std::min(per_q, td.m - r0), 0});
     s->gsq_count.push_back((int)s->gsq.size() - s->gsq_first.back());
   }
 }

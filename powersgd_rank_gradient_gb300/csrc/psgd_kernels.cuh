@@ -386,17 +386,20 @@ struct Pass1Stage {
   // Shared-memory budget per CTA: 192 KB with one CTA per SM, 96 KB with two,
   // 56 KB with three, so that the carve-out leaves L1 room for the CTAs' Q
   // tiles next to the stages.
-  static constexpr int BUDGET = MINB == 1 ? 192 * 1024 : (MINB == 2 ? 96 * 1024 : (MINB == 3 ? 56 * 1024 : 40 * 1024));
+  // Ranks >= 16 also keep the item's Q tiles (projection and correction,
+  // ctile1 x RP floats each) in shared memory.
+  static constexpr int QTILE = RP >= 16 ? ctile1_for(RP) * RP * 4 : 0;
+  static constexpr int BUDGET = (MINB == 1 ? 192 * 1024 : (MINB == 2 ? 96 * 1024 : (MINB == 3 ? 56 * 1024 : 40 * 1024))) - 2 * QTILE;
   static constexpr int S_RAW = BUDGET / (8 * UNIT_BYTES);
   static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
-  static constexpr int SMEM = 8 * S * UNIT_BYTES;                 // per CTA
+  static constexpr int SMEM = 8 * S * UNIT_BYTES + 2 * QTILE;     // per CTA
 };
 
 template <int RP, int WT, typename GT, int RW, int MINB>
 __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const TensorDesc& td, const Item& item,
                                                   const float* __restrict__ Qp, const float* __restrict__ Qc,
                                                   const float* __restrict__ Pc, int cur, float& chk,
-                                                  char* __restrict__ wsm) {
+                                                  char* __restrict__ wsm, float* __restrict__ qtile) {
   using St = Pass1Stage<RP, WT, GT, RW, MINB>;
   constexpr int S = St::S;
   constexpr int GB = St::GB;
@@ -410,6 +413,24 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
   const int units = ngroups * nchunks;
   const bool same_q = (Qp == Qc);
   const bool unit_scale = (a.scale == 1.0f);
+  constexpr int CT1 = ctile1_for(RP);
+  // ranks >= 16: the item's Q tiles, k-major [k][column - col0], in shared
+  // memory (qtile: correction Q, then projection Q)
+  float* qts_c = qtile;
+  float* qts_p = qtile + CT1 * RP;
+  if constexpr (RP >= 16) {
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < RP * (CT1 / 4); idx += kThreads) {
+      const int k = idx / (CT1 / 4), c4 = (idx - k * (CT1 / 4)) * 4;
+      if (c4 < item.ncols) {
+        const long long src = td.q_off + (long long)k * m + item.col0 + c4;
+        if (a.ef) *reinterpret_cast<float4*>(qts_c + k * CT1 + c4) = __ldg(reinterpret_cast<const float4*>(Qc + src));
+        if (!(a.ef && same_q))
+          *reinterpret_cast<float4*>(qts_p + k * CT1 + c4) = __ldg(reinterpret_cast<const float4*>(Qp + src));
+      }
+    }
+    __syncthreads();
+  }
   // slot layout: [q][w] gradient segments, then [q][w] store segments; inside
   // a segment lane l owns bytes [l * width, (l + 1) * width), so a warp's
   // accesses to one segment are contiguous and free of bank conflicts.
@@ -490,12 +511,23 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 #pragma unroll
             for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qv[cc]);
         } else {
+          // one 16-byte shared-memory read per k; each correction is the
+          // increasing-k FMA chain of dot_chain (bit-identical to pass 3)
+          const float* qt = qts_c + (c - item.col0);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int q = 0; q < RW; ++q)
 #pragma unroll
-            for (int k = 0; k < RP; ++k) qv[0][k] = __ldg(Qc + td.q_off + (long long)k * m + c + cc);
+            for (int cc = 0; cc < 4; ++cc) corr[q][cc] = 0.f;
 #pragma unroll
-            for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qv[0]);
+          for (int k = 0; k < RP; ++k) {
+            const float4 x = *reinterpret_cast<const float4*>(qt + k * CT1);
+#pragma unroll
+            for (int q = 0; q < RW; ++q) {
+              corr[q][0] = fmaf(po[q][k], x.x, corr[q][0]);
+              corr[q][1] = fmaf(po[q][k], x.y, corr[q][1]);
+              corr[q][2] = fmaf(po[q][k], x.z, corr[q][2]);
+              corr[q][3] = fmaf(po[q][k], x.w, corr[q][3]);
+            }
           }
         }
       }
@@ -551,14 +583,19 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 #pragma unroll
             for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[cc][k], pacc[q][k]);
       } else {
+        const float* qt = ((a.ef && same_q) ? qts_c : qts_p) + (c - item.col0);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int k = 0; k < RP; ++k) {
+          const float4 x = *reinterpret_cast<const float4*>(qt + k * CT1);
 #pragma unroll
-          for (int k = 0; k < RP; ++k) qv[0][k] = __ldg(Qp + td.q_off + (long long)k * m + c + cc);
-#pragma unroll
-          for (int q = 0; q < RW; ++q)
-#pragma unroll
-            for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[0][k], pacc[q][k]);
+          for (int q = 0; q < RW; ++q) {
+            float t = pacc[q][k];
+            t = fmaf(mb[q][0], x.x, t);
+            t = fmaf(mb[q][1], x.y, t);
+            t = fmaf(mb[q][2], x.z, t);
+            t = fmaf(mb[q][3], x.w, t);
+            pacc[q][k] = t;
+          }
         }
       }
     }
@@ -772,13 +809,14 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_staged(const StepArgs 
   const float* Pc = a.Pf + (long long)cur * a.p_total;
   const float* Qp = use_init ? a.qinit : Qc;
   char* wsm = p1smem + (threadIdx.x >> 5) * (St::S * St::UNIT_BYTES);
+  float* qtile = reinterpret_cast<float*>(p1smem + 8 * St::S * St::UNIT_BYTES);
   int bad = 0;
   float chk = 0.f;
   for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
     const Item item = a.p1items[it];
     const TensorDesc td = a.tensors[item.t];
     if (td.vec && a.vec_ok)
-      pass1_tile_staged<RP, WT, GT, RW, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm);
+      pass1_tile_staged<RP, WT, GT, RW, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, qtile);
     else
       pass1_tile<RP, WT, GT, RW, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
   }
@@ -927,73 +965,113 @@ __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float
   }
 }
 
-// One warp per tensor: sum the item Gram matrices in item order, then modified
-// Gram-Schmidt with epsilon on the coefficient matrix.  Lane j holds column j
-// of T.
+// One CTA per tensor: the whole CTA adds up the item Gram matrices (each
+// entry split over SPLIT threads, four accumulators each, then combined in a
+// fixed order), then warp 0 runs modified Gram-Schmidt with epsilon on the
+// coefficient matrix T (X_out = X T), with G and T in shared memory.  Step i:
+// g = G t_i, ||x_i||^2 = t_i . g, scale column i by 1 / (||x_i|| + eps), then
+// every later column j (lane j) loses its projection (t_i^T G t_j) t_i.
+// fp64 throughout; the dot products keep four independent chains.
 template <int RP>
-__global__ void __launch_bounds__(32) k_solve(const StepArgs a, const double* __restrict__ gram_in,
-                                              int is_q, int only_init) {
-  __shared__ double G[RP * RP];
+__global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const double* __restrict__ gram_in,
+                                                    int is_q, int only_init) {
+  constexpr int ENT = RP * RP;
+  constexpr int SPLIT = ENT >= kThreads ? 1 : kThreads / ENT;
+  __shared__ double G[ENT];
+  __shared__ double T[ENT];   // T[k * RP + j] = row k of column j
+  __shared__ double gv[RP];
+  __shared__ double part[kThreads];
   const int t = blockIdx.x;
-  const int lane = threadIdx.x;
   if (a.ctrl->flag) return;
   const TensorDesc td = a.tensors[t];
   const int first = is_q ? a.gsq_first[t] : a.gsp_first[t];
   const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
   if (count == 0) return;
-  for (int idx = lane; idx < RP * RP; idx += 32) {
-    double s = 0.0;
-    for (int it = 0; it < count; ++it) s += gram_in[(long long)(first + it) * RP * RP + idx];
-    G[idx] = s;
+  for (int base = 0; base < ENT; base += kThreads / SPLIT) {
+    const int idx = base + threadIdx.x / SPLIT;
+    const int sp = threadIdx.x % SPLIT;
+    double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+    if (idx < ENT) {
+      int it = sp;
+      for (; it + 3 * SPLIT < count; it += 4 * SPLIT) {
+        s0 += gram_in[(long long)(first + it) * ENT + idx];
+        s1 += gram_in[(long long)(first + it + SPLIT) * ENT + idx];
+        s2 += gram_in[(long long)(first + it + 2 * SPLIT) * ENT + idx];
+        s3 += gram_in[(long long)(first + it + 3 * SPLIT) * ENT + idx];
+      }
+      for (; it < count; it += SPLIT) s0 += gram_in[(long long)(first + it) * ENT + idx];
+    }
+    part[threadIdx.x] = (s0 + s1) + (s2 + s3);
+    __syncthreads();
+    if (sp == 0 && idx < ENT) {
+      double v = 0.0;
+      for (int q = 0; q < SPLIT; ++q) v += part[threadIdx.x + q];
+      G[idx] = v;
+      const int k = idx / RP, j = idx % RP;
+      T[idx] = (k == j && j < td.r) ? 1.0 : 0.0;
+    }
+    __syncthreads();
   }
-  __syncwarp();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   const int r = td.r;
   const double eps = (double)a.eps;
-  double tj[RP];
-#pragma unroll
-  for (int k = 0; k < RP; ++k) tj[k] = (k == lane && lane < r) ? 1.0 : 0.0;
   for (int i = 0; i < r; ++i) {
-    double ti[RP];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) ti[k] = __shfl_sync(0xffffffffu, tj[k], i);
-    // lane k: (G t_i)[k]
-    double gk = 0.0;
     if (lane < r) {
-#pragma unroll
-      for (int l = 0; l < RP; ++l) gk += G[lane * RP + l] * ti[l];
+      double c0 = 0.0, c1 = 0.0, c2 = 0.0, c3 = 0.0;
+      int l = 0;
+      // G is symmetric: row `lane` is read as column `lane`, contiguous across
+      // the warp (no shared-memory bank conflicts)
+      for (; l + 4 <= r; l += 4) {
+        c0 += G[l * RP + lane] * T[l * RP + i];
+        c1 += G[(l + 1) * RP + lane] * T[(l + 1) * RP + i];
+        c2 += G[(l + 2) * RP + lane] * T[(l + 2) * RP + i];
+        c3 += G[(l + 3) * RP + lane] * T[(l + 3) * RP + i];
+      }
+      for (; l < r; ++l) c0 += G[l * RP + lane] * T[l * RP + i];
+      gv[lane] = (c0 + c1) + (c2 + c3);
     }
-    double tl = 0.0;
+    __syncwarp();
+    double nn = (lane < r) ? T[lane * RP + i] * gv[lane] : 0.0;
 #pragma unroll
-    for (int k = 0; k < RP; ++k)
-      if (k == lane) tl = ti[k];
-    double part = (lane < r) ? tl * gk : 0.0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    const double nrm = sqrt(fmax(part, 0.0));
-    const double sc = 1.0 / (nrm + eps);
-#pragma unroll
-    for (int k = 0; k < RP; ++k) ti[k] *= sc;
-    gk *= sc;
-    if (lane == i) {
-#pragma unroll
-      for (int k = 0; k < RP; ++k) tj[k] = ti[k];
+    for (int o = 16; o > 0; o >>= 1) nn += __shfl_xor_sync(0xffffffffu, nn, o);
+    // sc = 1 / (sqrt(nn) + eps).  For eps = 0 and nn > 0 it is 1 / sqrt(nn):
+    // an fp32 rsqrtf seed refined by one Newton-Raphson step for
+    // f(y) = 1 / y^2 - nn (y <- y (3 - nn y^2) / 2), which takes the seed's
+    // ~24 correct bits to ~48 with three dependent fp64 operations instead of
+    // an fp64 square root and division.  A zero or negative nn, and eps > 0,
+    // take the direct expression (eps = 0 with a zero column gives inf and
+    // then NaN, as the oracle).
+    double sc;
+    if (eps == 0.0 && nn > 0.0 && nn < 1e300) {
+      const double y = (double)rsqrtf((float)nn);
+      sc = y * (1.5 - 0.5 * nn * y * y);
+    } else {
+      sc = 1.0 / (sqrt(fmax(nn, 0.0)) + eps);
     }
-    double gall[RP];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) gall[k] = __shfl_sync(0xffffffffu, gk, k);
+    __syncwarp();
+    if (lane < r) {
+      T[lane * RP + i] *= sc;
+      gv[lane] *= sc;
+    }
+    __syncwarp();
     if (lane > i && lane < r) {
-      double d = 0.0;
-#pragma unroll
-      for (int k = 0; k < RP; ++k) d += gall[k] * tj[k];
-#pragma unroll
-      for (int k = 0; k < RP; ++k) tj[k] -= d * ti[k];
+      double d0 = 0.0, d1 = 0.0, d2 = 0.0, d3 = 0.0;
+      int k = 0;
+      for (; k + 4 <= r; k += 4) {
+        d0 += gv[k] * T[k * RP + lane];
+        d1 += gv[k + 1] * T[(k + 1) * RP + lane];
+        d2 += gv[k + 2] * T[(k + 2) * RP + lane];
+        d3 += gv[k + 3] * T[(k + 3) * RP + lane];
+      }
+      for (; k < r; ++k) d0 += gv[k] * T[k * RP + lane];
+      const double d = (d0 + d1) + (d2 + d3);
+      for (k = 0; k < r; ++k) T[k * RP + lane] -= d * T[k * RP + i];
     }
+    __syncwarp();
   }
-  if (lane < RP) {
-    float* T = a.tmat + (long long)t * RP * RP;
-#pragma unroll
-    for (int k = 0; k < RP; ++k) T[k * RP + lane] = (lane < r) ? (float)tj[k] : 0.f;
-  }
+  float* Tout = a.tmat + (long long)t * RP * RP;
+  for (int idx = lane; idx < ENT; idx += 32) Tout[idx] = (float)T[idx];
 }
 
 // dst rows = src rows x T (thread per row).
@@ -1040,7 +1118,8 @@ __global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const floa
 // qpart[rb][k][j].
 // ---------------------------------------------------------------------------
 constexpr int kPStage = 128;
-constexpr int kRowBatch = 8;
+// rows of loads issued together per thread: 32 bytes x batch per source
+__host__ __device__ constexpr int row_batch_for(int rp) { return 32 / cpt_for(rp); }
 
 // NC values of Mbar at (row, c0 ..) from the selected source; VEC: one
 // 16-byte access per source (NC == 4, aligned rows), else element by element
@@ -1101,6 +1180,7 @@ __device__ __forceinline__ void pass2_tile(const StepArgs& a, const TensorDesc& 
   constexpr int CPT = cpt_for(RP);
   static_assert(NC == CPT || NC == 1, "columns per access");
   constexpr int NA = CPT;  // columns accumulated per thread
+  constexpr int kRowBatch = row_batch_for(RP);
   const int c0 = item.col0 + threadIdx.x * CPT;
   const int nxt = a.ctrl->cur ^ 1;
   const int cend = item.col0 + item.ncols;

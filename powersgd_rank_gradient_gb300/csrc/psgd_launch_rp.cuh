@@ -87,7 +87,7 @@ void launch_gram(const StepArgs& a, const float* src, float* dense_out, int is_q
 
 template <int RP>
 void launch_solve(const StepArgs& a, const double* gram, int is_q, cudaStream_t s) {
-  k_solve<RP><<<a.n_tensors, 32, 0, s>>>(a, gram, is_q, 0);
+  k_solve<RP><<<a.n_tensors, kThreads, 0, s>>>(a, gram, is_q, 0);
 }
 
 template <int RP>
