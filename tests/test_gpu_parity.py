@@ -327,3 +327,33 @@ def test_step_host_matches_device_path():
         assert torch.equal(out.cpu(), host_out[step]), f"step {step}"
     dev_state.close()
     host_state.close()
+
+
+@pytest.mark.parametrize("warm", [True, False])
+def test_library_draw_matches_oracle_philox(warm):
+    """No injected draw: the library draws Q with its Philox4x32-10 stream;
+    the oracle is fed the same stream computed independently in float64."""
+    import oracle
+    from oracle.philox import library_draw
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = [(300, 200), (7,), (64, 3, 3, 3), (128, 96)]
+    rank, seed, world = 3, 0x1234567890AB, 2
+    st = PowerSGDState(shapes, world, matrix_approximation_rank=rank, start_powerSGD_iter=1,
+                       min_compression_rate=1.0, warm_start=warm, random_seed=seed, device=DEV)
+    ref = oracle.PowerSGDOracle(shapes=shapes, world_size=world, matrix_approximation_rank=rank,
+                                start_powerSGD_iter=1, min_compression_rate=1.0, warm_start=warm)
+    comp = [p for p in ref.plans if p.compressed]
+    rp = 4
+    for step in range(4):
+        if step >= 1 and (step == 1 or not warm):
+            for ci, p in enumerate(comp):
+                ref.set_q_draw(p.index, library_draw(p.cols, p.rank, rp, ci, step, seed))
+        g = grads_for(shapes, world, step)
+        out = st.step([torch.from_numpy(x).to(DEV) for x in g])
+        _, exp = ref.step(g)
+        got = out.double().cpu().numpy()
+        for p in ref.plans:
+            sl = slice(p.offset, p.offset + p.numel)
+            assert rel(got[sl], exp[sl]) <= 1e-4, (step, p.index)
+    st.close()

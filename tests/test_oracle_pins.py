@@ -465,3 +465,25 @@ def test_compression_stats():
     o = PowerSGDOracle(shapes=[(8, 6), (5,)], world_size=1, matrix_approximation_rank=2,
                        min_compression_rate=0.5)
     assert o.compression_stats() == (53, (8 + 6) * 2 + 5)
+
+
+# --------------------------------------------------------------------------
+# The oracle's counter-based generator (for the library's own Q draws)
+# --------------------------------------------------------------------------
+def test_philox_known_answers():
+    from oracle.philox import philox4x32_10
+
+    for case in _load("philox_kat.json")["cases"]:
+        c = [np.uint32(int(x, 16)) for x in case["counter"]]
+        k = [np.uint32(int(x, 16)) for x in case["key"]]
+        out = philox4x32_10(*c, *k)
+        assert ["%08x" % int(x) for x in out] == case["output"]
+
+
+def test_box_muller_moments():
+    from oracle.philox import library_draw
+
+    z = library_draw(4096, 8, 8, 3, 0, 1234).ravel()
+    assert abs(z.mean()) < 0.02
+    assert abs(z.var() - 1.0) < 0.03
+    assert abs(np.mean(z ** 4) - 3.0) < 0.15   # Gaussian kurtosis
