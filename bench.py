@@ -299,12 +299,66 @@ def run_native(spec, args, dist, rank_id, world, device):
                        "survey_min_frac_of_nominal_8tbs": sb["survey_min"] / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                        "survey_min_frac_of_measured": sb["survey_min"] / (ms_step / 1e3) / 1e9 / peak},
         kernels=kernels, counts=counts)
+    res["rows"] = run_rows(spec, args, dist, device, sets, out, W, N)
     del sets
     torch.cuda.empty_cache()
     if not args.no_e2e:
         res["e2e"] = run_e2e(st, spec, args, dist, device, N, W)
     st.close()
     return res
+
+
+def run_rows(spec, args, dist, device, sets, out, W, N):
+    """The survey's other hot-path rows on the same resident inputs:
+    A1, the vanilla phase (every call before start_powerSGD_iter is the plain
+    replica mean of the whole bucket), and A3, the first compressed call
+    (draw Q, orthogonalise it, then the step) against a warm-started one."""
+    import torch
+
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    stream = torch.cuda.current_stream(device)
+    rows = {}
+    van = PowerSGDState(spec["shapes"], W, matrix_approximation_rank=spec["rank"],
+                        start_powerSGD_iter=1 << 60, min_compression_rate=spec["mcr"],
+                        use_error_feedback=False, device=device)
+    for i in range(3):
+        van.step(sets[i % 2], out=out)
+    torch.cuda.synchronize(device)
+    van.profile(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        van.step(sets[i % 2], out=out)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
+    prof = van.profile_read()
+    n_l, tot_ms, _ = prof["mean"]
+    mean_bytes = N * (W * 4 + 4)
+    peak, _ = load_peaks()
+    rows["A1_vanilla_phase"] = {
+        "ms_per_step": ms, "gradient_gbs": W * N * 4 / (ms / 1e3) / 1e9,
+        "kernel": "mean", "algo_bytes_per_launch": mean_bytes,
+        "achieved_gbs": mean_bytes / (tot_ms / n_l / 1e3) / 1e9,
+        "frac_of_measured": mean_bytes / (tot_ms / n_l / 1e3) / 1e9 / peak}
+    van.close()
+    # A3: a fresh state's first compressed call (Q draw + orthogonalisation)
+    fresh = PowerSGDState(spec["shapes"], W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
+                          min_compression_rate=spec["mcr"],
+                          batch_tensors_with_same_shape=spec["batch_same_shape"], device=device)
+    times = []
+    for i in range(3):
+        e0.record(stream)
+        fresh.step(sets[i % 2], out=out)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        times.append(e0.elapsed_time(e1))
+    fresh.close()
+    rows["A3_first_compressed_call"] = {"ms": times[0], "next_calls_ms": times[1:],
+                                        "q_init_overhead_ms": times[0] - min(times[1:])}
+    return rows
 
 
 def run_e2e(st, spec, args, dist, device, N, W):
@@ -447,7 +501,7 @@ def main():
         r = run_native(sp, args, dist, rank_id, world, device)
         extras[sp["name"]] = {"value": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
                               "step_roofline": r["step_roofline"], "e2e": r.get("e2e"), "clocks": r["clocks"],
-                              "kernels": r["kernels"]}
+                              "kernels": r["kernels"], "rows": r.get("rows")}
     cpu = None
     if rank_id == 0 and world == 1 and not args.no_cpu:
         cb = time_oracle(spec, 50, target_s=15.0)
@@ -461,6 +515,7 @@ def main():
                 "config": base_cfg, "clocks": res["clocks"], "gpu_launches": res["launches"],
                 "roofline": res["roofline"], "step_roofline": res["step_roofline"],
                 "e2e": res.get("e2e"), "cpu_baseline": cpu, "kernels": res["kernels"],
+                "rows": res.get("rows"),
                 "workloads": extras}
         print(json.dumps(line))
     if dist is not None:
