@@ -146,6 +146,7 @@ struct psgd_state {
   long long N = 0, Nc = 0, Nc_pad = 0, Nunc = 0, Ne = 0;
   long long p_total = 0, q_total = 0, pp_total = 0, qp_total = 0;
   int pass2_src = 0;  // 0 mbar scratch, 1 error store, 2 gradients
+  int row_block = kRowBlock;  // rows per pass-2 item
   // device memory
   TensorDesc* d_tensors = nullptr;
   Item* d_items = nullptr;
@@ -268,6 +269,17 @@ void build_plan(psgd_state* s) {
   s->all_segs.clear();
   long long c_off = 0, p_off = 0, q_off = 0, pp_off = 0, qp_off = 0, e_off = 0;
   long long unc = 0;
+  // pass 2: row blocks of kRowBlock rows, shorter for small buckets so that
+  // there are several items per resident CTA (one Q partial per item)
+  {
+    long long nc = 0;
+    for (auto& h : s->tensors)
+      if (h.compressed) nc += h.numel;
+    const long long target = (long long)s->sms * 3 * 4;
+    int rb = kRowBlock;
+    while (rb > 64 && nc / ((long long)rb * CT) < target) rb >>= 1;
+    s->row_block = rb;
+  }
   // uncompressed ranges, merged
   long long run_start = -1, run_len = 0;
   for (auto& h : s->tensors) {
@@ -285,7 +297,7 @@ void build_plan(psgd_state* s) {
       td.r = h.rank;
       td.ctiles = (int)((h.cols + CT - 1) / CT);
       td.ctiles1 = (int)((h.cols + CT1 - 1) / CT1);
-      td.rblocks = (int)((h.rows + kRowBlock - 1) / kRowBlock);
+      td.rblocks = (int)((h.rows + s->row_block - 1) / s->row_block);
       td.pp_off = pp_off;
       td.qp_off = qp_off;
       td.e_off = e_off;
@@ -343,7 +355,7 @@ void build_plan(psgd_state* s) {
           it.nrows = std::min(rows_per_item, td.n - r0);
           it.col0 = ct * ctw;
           it.ncols = std::min(ctw, td.m - it.col0);
-          it.rb = r0 / kRowBlock;
+          it.rb = r0 / s->row_block;
           it.ct = ct;
           it.pad = group_of[c];
           out->push_back(it);
@@ -357,7 +369,7 @@ void build_plan(psgd_state* s) {
     });
     for (auto& it : *out) it.pad = 0;
   };
-  make_items(&s->items, kRowBlock, CT);
+  make_items(&s->items, s->row_block, CT);
   make_items(&s->fitems, kFineRows3, CT);
   make_items(&s->p1items, kFineRows, CT1);
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
@@ -645,8 +657,8 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
   s->batch = batch ? 1 : 0;
   s->dtype = grad_dtype;
   for (auto& h : s->tensors) s->N += h.numel;
-  build_plan(s);
   cudaDeviceGetAttribute(&s->sms, cudaDevAttrMultiProcessorCount, device);
+  build_plan(s);
   // Where pass 2 reads the replica mean: a scratch copy written by pass 1
   // costs 8 bytes per element; re-reading the W sources costs W * 4 (store)
   // or W * sizeof(grad) (no error feedback).  Take the cheaper.

@@ -622,9 +622,9 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 
 // ---------------------------------------------------------------------------
 // Pass 1, chunk-stationary (RP <= 8).  Warp w of the CTA owns chunk
-// (w % NCH) of the item's column tile (NCH = tile / 128 chunks of 128
-// columns) and every (8 / NCH)-th row of the item, so each lane loads the Q
-// values of its 4 columns once per item and keeps them in registers.  Its
+// (w % nch) of the item's column tile (nch <= 8 chunks of 128 columns) and
+// every (8 / nch)-th row of the item, so each lane loads the Q values of its
+// 4 columns once per item and keeps them in registers.  Its
 // source segments (one row x 128 columns of every replica's gradient and
 // store) are staged by cp.async S rows ahead, as in pass1_tile_staged.  Each
 // row's P partial over the chunk is reduced across the warp and parked in
@@ -634,7 +634,6 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 template <int RP, int WT, typename GT, int MINB>
 struct Pass1CS {
   static constexpr int NCH = ctile1_for(RP) / 128;                // chunks per column tile
-  static constexpr int WPC = 8 / NCH;                             // warps per chunk
   static constexpr int GB = 4 * (int)sizeof(GT);
   static constexpr int GSEG = 32 * GB;
   static constexpr int ESEG = 32 * 16;
@@ -655,20 +654,22 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
   constexpr int S = St::S;
   constexpr int GB = St::GB;
   constexpr int NCH = St::NCH;
-  constexpr int WPC = St::WPC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nxt = cur ^ 1;
   const long long m = td.m;
   const int cend = item.col0 + item.ncols;
   const int nch = (item.ncols + 127) / 128;
-  const int ch = warp % NCH;
-  const int phase = warp / NCH;
+  // wpc warps per chunk (rows interleaved among them): a full tile has one
+  // warp per chunk; a narrow one spreads the 8 warps over its chunks
+  const int wpc = 8 / nch;
+  const int ch = warp % nch;
+  const int phase = warp / nch;
   const bool unit_scale = (a.scale == 1.0f);
   const bool same_q = (Qp == Qc);
-  if (ch < nch) {
+  if (warp < nch * wpc) {
     const int c = item.col0 + ch * 128 + lane * 4;
     const bool cin = c < cend;
-    const int units = phase < item.nrows ? (item.nrows - phase + WPC - 1) / WPC : 0;
+    const int units = phase < item.nrows ? (item.nrows - phase + wpc - 1) / wpc : 0;
     float qc[4][RP], qp[4][RP];
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc)
@@ -681,7 +682,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
     auto issue = [&](int u) {
       char* slot = wsm + (u % S) * St::UNIT_BYTES;
       if (cin) {
-        const long long row = item.row0 + phase + (long long)u * WPC;
+        const long long row = item.row0 + phase + (long long)u * wpc;
         const long long go = td.g_off + row * m + c;
         const long long eo = (long long)cur * a.W * a.nc_pad + td.c_off + row * m + c;
 #pragma unroll
@@ -701,7 +702,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
     for (int u = 0; u < units; ++u) {
       cp_async_wait<S - 2>();
       if (u + S - 1 < units) issue(u + S - 1); else cp_async_commit();
-      const int rr = phase + u * WPC;
+      const int rr = phase + u * wpc;
       const long long i = item.row0 + rr;
       float pacc[RP];
 #pragma unroll
