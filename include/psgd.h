@@ -43,7 +43,12 @@ extern "C" {
 
 typedef struct psgd_state psgd_state; /* opaque, library-owned */
 
-typedef enum { PSGD_F32 = 0, PSGD_F16 = 1 } psgd_dtype;
+/* Type of the replica gradient buckets.  F16 / BF16: 16-bit gradients, as
+ * produced by GradScaler-scaled half-precision training or by the pages'
+ * fp16/bf16 compress wrappers ("Default Communication Hooks":
+ * fp16_compress_wrapper / bf16_compress_wrapper cast the bucket to 16 bits);
+ * the library computes in fp32 and returns fp32 (the cast back). */
+typedef enum { PSGD_F32 = 0, PSGD_F16 = 1, PSGD_BF16 = 2 } psgd_dtype;
 
 #define PSGD_OK 0
 #define PSGD_SKIPPED_NONFINITE 1 /* [AMP] inf/NaN seen: step skipped, state kept   */
@@ -83,7 +88,7 @@ int psgd_plan(const int64_t* dims, const int32_t* ndims, int32_t n_tensors,
  *
  * Hyper-parameters keep the pages' names and meaning ([DDP] items 1-4,
  * [DDP2] item 5).  world_size = W simulated replicas.  grad_dtype is the type
- * of the replica buckets passed to psgd_step (F16: GradScaler-scaled halves).
+ * of the replica buckets passed to psgd_step (F16 / BF16: 16-bit buckets).
  * Allocates on `device` everything a step needs: the per-replica error
  * feedback store, P/Q memory and all scratch; psgd_step allocates nothing.
  * The error store is kept twice (the current and the next step) so that a

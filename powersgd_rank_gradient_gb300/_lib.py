@@ -19,6 +19,7 @@ PSGD_ECUDA = -3
 PSGD_ETIMEOUT = -4
 PSGD_F32 = 0
 PSGD_F16 = 1
+PSGD_BF16 = 2
 PSGD_MAX_RANK = 32
 PSGD_MAX_WORLD = 64
 

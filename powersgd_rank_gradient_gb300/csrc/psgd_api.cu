@@ -400,7 +400,7 @@ StepArgs make_args(psgd_state* s) {
   StepArgs a;
   memset(&a, 0, sizeof(a));
   a.W = s->W;
-  a.f16 = s->dtype == PSGD_F16;
+  a.gtype = s->dtype == PSGD_F16 ? 1 : (s->dtype == PSGD_BF16 ? 2 : 0);
   a.scale = 1.f;
   a.invW = 1.f / (float)s->W;
   a.estore = s->estore;
@@ -630,7 +630,8 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
   if (world_size < 1 || world_size > PSGD_MAX_WORLD) return fail(PSGD_EINVAL, "world_size must be in [1, 64]");
   if (start_iter < 0) return fail(PSGD_EINVAL, "start_powerSGD_iter < 0");
   if (!(eps >= 0.f)) return fail(PSGD_EINVAL, "orthogonalization_epsilon must be >= 0");
-  if (grad_dtype != PSGD_F32 && grad_dtype != PSGD_F16) return fail(PSGD_EINVAL, "grad_dtype");
+  if (grad_dtype != PSGD_F32 && grad_dtype != PSGD_F16 && grad_dtype != PSGD_BF16)
+    return fail(PSGD_EINVAL, "grad_dtype");
   psgd_state* s = new psgd_state();
   int rc = plan_tensors(dims, ndims, n_tensors, rank, mcr, &s->tensors);
   if (rc) {
@@ -662,7 +663,7 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
   // Where pass 2 reads the replica mean: a scratch copy written by pass 1
   // costs 8 bytes per element; re-reading the W sources costs W * 4 (store)
   // or W * sizeof(grad) (no error feedback).  Take the cheaper.
-  const int gsz = grad_dtype == PSGD_F16 ? 2 : 4;
+  const int gsz = grad_dtype == PSGD_F32 ? 4 : 2;
   const int reread = s->W * (s->ef ? 4 : gsz);
   s->pass2_src = (reread <= 8) ? (s->ef ? 1 : 2) : 0;
   if (s->W == 1 && s->ef) s->pass2_src = 1;
@@ -752,7 +753,7 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
 int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_loss_scale, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
   if (!grads || !out) return fail(PSGD_EINVAL, "grads/out is NULL");
-  const size_t gsz = s->dtype == PSGD_F16 ? 2 : 4;
+  const size_t gsz = s->dtype == PSGD_F32 ? 4 : 2;
   for (int w = 0; w < s->W; ++w) {
     if (!grads[w]) return fail(PSGD_EINVAL, "grads[w] is NULL");
     const bool same = (grads[w] == (const void*)out);
@@ -768,7 +769,7 @@ int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_los
   a.out = out;
   a.scale = inv_loss_scale;
   int vec_ok = ((uintptr_t)out % 16 == 0);
-  for (int w = 0; w < s->W; ++w) vec_ok &= ((uintptr_t)grads[w] % (s->dtype == PSGD_F16 ? 8 : 16) == 0);
+  for (int w = 0; w < s->W; ++w) vec_ok &= ((uintptr_t)grads[w] % (s->dtype == PSGD_F32 ? 16 : 8) == 0);
   a.vec_ok = vec_ok;
   Launcher L{s, st};
   PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, sizeof(int), st));
@@ -813,7 +814,7 @@ int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_los
 namespace {
 // Allocates the two staging sets, the copy streams and their events.
 int host_staging_init(psgd_state* s) {
-  const size_t gsz = s->dtype == PSGD_F16 ? 2 : 4;
+  const size_t gsz = s->dtype == PSGD_F32 ? 4 : 2;
   for (int k = 0; k < 2; ++k) {
     s->stage_grads[k].assign(s->W, nullptr);
     for (int w = 0; w < s->W; ++w)
@@ -860,7 +861,7 @@ int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out
   for (int w = 0; w < s->W; ++w)
     if (!host_grads[w]) return fail(PSGD_EINVAL, "host_grads[w] is NULL");
   DeviceGuard g(s->device);
-  const size_t gsz = s->dtype == PSGD_F16 ? 2 : 4;
+  const size_t gsz = s->dtype == PSGD_F32 ? 4 : 2;
   if (!s->s_in) {
     int rc = host_staging_init(s);
     if (rc) {

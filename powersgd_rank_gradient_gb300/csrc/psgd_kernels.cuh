@@ -18,9 +18,12 @@
 // so the value it sees is exactly fl(M_w - out).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "psgd_internal.h"
 
@@ -32,7 +35,7 @@ namespace psgd {
 struct StepArgs {
   GradPtrs grads;
   int W;
-  int f16;            // grads are __half
+  int gtype;          // gradient type: 0 float, 1 __half, 2 __nv_bfloat16
   float scale;        // inverse loss scale
   float invW;
   float* out;
@@ -156,6 +159,37 @@ __device__ __forceinline__ void load_grad<1, __half>(const __half* p, float (&v)
   unsigned short raw;
   asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(raw) : "l"(p));
   v[0] = __half2float(__ushort_as_half(raw));
+}
+
+template <>
+__device__ __forceinline__ void load_grad<4, __nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
+  uint2 raw;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(raw.x), "=r"(raw.y)
+               : "l"(p));
+  const float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.x));
+  const float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.y));
+  v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+template <>
+__device__ __forceinline__ void load_grad<1, __nv_bfloat16>(const __nv_bfloat16* p, float (&v)[1]) {
+  unsigned short raw;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(raw) : "l"(p));
+  v[0] = __bfloat162float(__ushort_as_bfloat16(raw));
+}
+
+// Four 16-bit gradient values (8 bytes, e.g. from a shared-memory slot) as floats.
+template <typename GT>
+__device__ __forceinline__ void cvt4(uint2 raw, float (&v)[4]) {
+  if constexpr (std::is_same<GT, __half>::value) {
+    const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+  } else {
+    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+    v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+  }
 }
 
 template <int NC>
@@ -548,10 +582,7 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
             const float4 x = *reinterpret_cast<const float4*>(slot + (q * WT + w) * St::GSEG + lane * GB);
             gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
           } else {
-            const uint2 raw = *reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB);
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-            gv[0] = fa.x; gv[1] = fa.y; gv[2] = fb.x; gv[3] = fb.y;
+            cvt4<GT>(*reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB), gv);
           }
           float ev[4] = {0.f, 0.f, 0.f, 0.f};
           if (a.ef) {
@@ -725,10 +756,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
             const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
             gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
           } else {
-            const uint2 raw = *reinterpret_cast<const uint2*>(slot + w * St::GSEG + lane * GB);
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-            gv[0] = fa.x; gv[1] = fa.y; gv[2] = fb.x; gv[3] = fb.y;
+            cvt4<GT>(*reinterpret_cast<const uint2*>(slot + w * St::GSEG + lane * GB), gv);
           }
           float mv[4];
           if (a.ef) {

@@ -7,6 +7,18 @@
 
 namespace psgd {
 
+// Calls f with a value of the gradient type named by gtype (0 float,
+// 1 __half, 2 __nv_bfloat16).
+template <typename F>
+inline void by_gtype(int gtype, F&& f) {
+  if (gtype == 1)
+    f(__half());
+  else if (gtype == 2)
+    f(__nv_bfloat16());
+  else
+    f(0.0f);
+}
+
 template <int RP, int WT, typename GT, int RW, int MINB>
 void launch_pass1_staged(const StepArgs& a, int grid, cudaStream_t s) {
   using St = Pass1Stage<RP, WT, GT, RW, MINB>;
@@ -35,43 +47,26 @@ void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
 // 16 and 32 keep Q in L1 and use pass1_tile_staged (one CTA per SM).
 template <int RP>
 void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
-  if constexpr (RP <= 8) {
-    if (a.f16) {
+  by_gtype(a.gtype, [&](auto tag) {
+    using GT = decltype(tag);
+    if constexpr (RP <= 8) {
       switch (a.W) {
-        case 1: launch_pass1_cs<RP, 1, __half, 2>(a, grid, s); break;
-        case 2: launch_pass1_cs<RP, 2, __half, 2>(a, grid, s); break;
-        case 4: launch_pass1_cs<RP, 4, __half, 1>(a, grid, s); break;
-        case 8: launch_pass1_cs<RP, 8, __half, 1>(a, grid, s); break;
-        default: k_pass1<RP, 0, __half, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+        case 1: launch_pass1_cs<RP, 1, GT, 2>(a, grid, s); break;
+        case 2: launch_pass1_cs<RP, 2, GT, 2>(a, grid, s); break;
+        case 4: launch_pass1_cs<RP, 4, GT, 1>(a, grid, s); break;
+        case 8: launch_pass1_cs<RP, 8, GT, 1>(a, grid, s); break;
+        default: k_pass1<RP, 0, GT, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
       }
     } else {
       switch (a.W) {
-        case 1: launch_pass1_cs<RP, 1, float, 2>(a, grid, s); break;
-        case 2: launch_pass1_cs<RP, 2, float, 2>(a, grid, s); break;
-        case 4: launch_pass1_cs<RP, 4, float, 1>(a, grid, s); break;
-        case 8: launch_pass1_cs<RP, 8, float, 1>(a, grid, s); break;
-        default: k_pass1<RP, 0, float, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
+        case 1: launch_pass1_staged<RP, 1, GT, 1, 1>(a, grid, s); break;
+        case 2: launch_pass1_staged<RP, 2, GT, 1, 1>(a, grid, s); break;
+        case 4: launch_pass1_staged<RP, 4, GT, 1, 1>(a, grid, s); break;
+        case 8: launch_pass1_staged<RP, 8, GT, 1, 1>(a, grid, s); break;
+        default: k_pass1<RP, 0, GT, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
       }
     }
-  } else {
-    if (a.f16) {
-      switch (a.W) {
-        case 1: launch_pass1_staged<RP, 1, __half, 1, 1>(a, grid, s); break;
-        case 2: launch_pass1_staged<RP, 2, __half, 1, 1>(a, grid, s); break;
-        case 4: launch_pass1_staged<RP, 4, __half, 1, 1>(a, grid, s); break;
-        case 8: launch_pass1_staged<RP, 8, __half, 1, 1>(a, grid, s); break;
-        default: k_pass1<RP, 0, __half, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
-      }
-    } else {
-      switch (a.W) {
-        case 1: launch_pass1_staged<RP, 1, float, 1, 1>(a, grid, s); break;
-        case 2: launch_pass1_staged<RP, 2, float, 1, 1>(a, grid, s); break;
-        case 4: launch_pass1_staged<RP, 4, float, 1, 1>(a, grid, s); break;
-        case 8: launch_pass1_staged<RP, 8, float, 1, 1>(a, grid, s); break;
-        default: k_pass1<RP, 0, float, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
-      }
-    }
-  }
+  });
 }
 
 template <int RP>
@@ -107,19 +102,16 @@ void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s) {
       k_pass2<RP, 1, float, 2><<<grid, kThreads, 0, s>>>(a);
     else
       k_pass2<RP, 1, float, 0><<<grid, kThreads, 0, s>>>(a);
-  } else if (a.f16) {
-    switch (a.W) {
-      case 1: k_pass2<RP, 2, __half, 1><<<grid, kThreads, 0, s>>>(a); break;
-      case 2: k_pass2<RP, 2, __half, 2><<<grid, kThreads, 0, s>>>(a); break;
-      case 4: k_pass2<RP, 2, __half, 4><<<grid, kThreads, 0, s>>>(a); break;
-      default: k_pass2<RP, 2, __half, 0><<<grid, kThreads, 0, s>>>(a); break;
-    }
   } else {
-    switch (a.W) {
-      case 1: k_pass2<RP, 2, float, 1><<<grid, kThreads, 0, s>>>(a); break;
-      case 2: k_pass2<RP, 2, float, 2><<<grid, kThreads, 0, s>>>(a); break;
-      default: k_pass2<RP, 2, float, 0><<<grid, kThreads, 0, s>>>(a); break;
-    }
+    by_gtype(a.gtype, [&](auto tag) {
+      using GT = decltype(tag);
+      switch (a.W) {
+        case 1: k_pass2<RP, 2, GT, 1><<<grid, kThreads, 0, s>>>(a); break;
+        case 2: k_pass2<RP, 2, GT, 2><<<grid, kThreads, 0, s>>>(a); break;
+        case 4: k_pass2<RP, 2, GT, 4><<<grid, kThreads, 0, s>>>(a); break;
+        default: k_pass2<RP, 2, GT, 0><<<grid, kThreads, 0, s>>>(a); break;
+      }
+    });
   }
 }
 

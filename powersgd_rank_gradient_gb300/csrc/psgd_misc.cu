@@ -60,23 +60,22 @@ __global__ void __launch_bounds__(kThreads) k_mean(const StepArgs a, const Segme
 
 void launch_mean(const StepArgs& a, const Segment* segs, int nsegs, int grid, cudaStream_t s) {
   if (nsegs == 0) return;
-  if (a.f16) {
+  auto go = [&](auto tag) {
+    using GT = decltype(tag);
     switch (a.W) {
-      case 1: k_mean<1, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      case 2: k_mean<2, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      case 4: k_mean<4, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      case 8: k_mean<8, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      default: k_mean<0, __half><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 1: k_mean<1, GT><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 2: k_mean<2, GT><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 4: k_mean<4, GT><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      case 8: k_mean<8, GT><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
+      default: k_mean<0, GT><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
     }
-  } else {
-    switch (a.W) {
-      case 1: k_mean<1, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      case 2: k_mean<2, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      case 4: k_mean<4, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      case 8: k_mean<8, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-      default: k_mean<0, float><<<grid, kThreads, 0, s>>>(a, segs, nsegs); break;
-    }
-  }
+  };
+  if (a.gtype == 1)
+    go(__half());
+  else if (a.gtype == 2)
+    go(__nv_bfloat16());
+  else
+    go(0.0f);
 }
 
 // End of a step: a step that saw no inf/NaN makes the next half of the

@@ -17,7 +17,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import PSGD_F16, PSGD_F32, PSGD_SKIPPED_NONFINITE, check
+from ._lib import PSGD_BF16, PSGD_F16, PSGD_F32, PSGD_SKIPPED_NONFINITE, check
 
 
 def _stream_ptr(stream):
@@ -36,8 +36,8 @@ class PowerSGDState:
         if device is None:
             device = torch.cuda.current_device()
         device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
-        if grad_dtype not in (torch.float32, torch.float16):
-            raise ValueError("grad_dtype must be torch.float32 or torch.float16")
+        if grad_dtype not in (torch.float32, torch.float16, torch.bfloat16):
+            raise ValueError("grad_dtype must be torch.float32, torch.float16 or torch.bfloat16")
         self.shapes = [tuple(int(d) for d in s) for s in shapes]
         self.world_size = int(world_size)
         self.matrix_approximation_rank = int(matrix_approximation_rank)
@@ -59,7 +59,8 @@ class PowerSGDState:
             self.start_powerSGD_iter, self.min_compression_rate, int(self.use_error_feedback),
             int(self.warm_start), self.orthogonalization_epsilon, self.random_seed & (2**64 - 1),
             int(self.batch_tensors_with_same_shape),
-            PSGD_F16 if grad_dtype == torch.float16 else PSGD_F32, device.index or 0,
+            {torch.float16: PSGD_F16, torch.bfloat16: PSGD_BF16}.get(grad_dtype, PSGD_F32),
+            device.index or 0,
             ctypes.byref(handle)))
         self._h = handle
         self._lib = L

@@ -357,3 +357,43 @@ def test_library_draw_matches_oracle_philox(warm):
             sl = slice(p.offset, p.offset + p.numel)
             assert rel(got[sl], exp[sl]) <= 1e-4, (step, p.index)
     st.close()
+
+
+@pytest.mark.parametrize("world,ef", [(1, True), (2, True), (3, False), (8, True)])
+def test_bf16_buckets(world, ef):
+    """16-bit (bf16) replica buckets, as the bf16 compress wrapper produces:
+    the oracle is fed the same bf16 values widened to float64."""
+    import oracle
+
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = MIXED
+    st = PowerSGDState(shapes, world, matrix_approximation_rank=4, start_powerSGD_iter=1,
+                       min_compression_rate=1.0, use_error_feedback=ef, grad_dtype=torch.bfloat16,
+                       device=DEV)
+    ref = oracle.PowerSGDOracle(shapes=shapes, world_size=world, matrix_approximation_rank=4,
+                                start_powerSGD_iter=1, min_compression_rate=1.0, use_error_feedback=ef)
+    for t, plan in enumerate(ref.plans):
+        if plan.compressed:
+            from powersgd_rank_gradient_gb300 import workloads as wl
+            draw = wl.standard_normal_np((plan.cols, plan.rank), 500 + t)
+            st.set_q(t, draw, is_draw=True)
+            ref.set_q_draw(t, draw.astype(np.float64))
+    for step in range(3):
+        g32 = grads_for(shapes, world, step)
+        gb = [torch.from_numpy(x).to(torch.bfloat16) for x in g32]
+        out = st.step([x.to(DEV) for x in gb])
+        assert not st.status()
+        _, exp = ref.step([x.double().numpy() for x in gb])
+        got = out.double().cpu().numpy()
+        for p in ref.plans:
+            sl = slice(p.offset, p.offset + p.numel)
+            assert rel(got[sl], exp[sl]) <= 1e-4, (step, p.index)
+        if ef:
+            for w in range(world):
+                e = st.get_error(w).double().cpu().numpy()
+                for p in ref.plans:
+                    if p.compressed:
+                        po = st.tensor_info(p.index)["packed_offset"]
+                        assert rel(e[po:po + p.numel], ref.error_of(w, p.index).reshape(-1)) <= 1e-4
+    st.close()
