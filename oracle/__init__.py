@@ -3,6 +3,7 @@
 from .powersgd_oracle import (  # noqa: F401
     OK,
     SKIPPED,
+    BatchedPowerSGDOracle,
     PowerSGDOracle,
     TensorPlan,
     allreduce_mean,

@@ -301,3 +301,80 @@ class PowerSGDOracle:
         after = sum((p.rows + p.cols) * p.rank if p.compressed else p.numel
                     for p in self.plans)
         return before, after
+
+
+@dataclass
+class BatchedPowerSGDOracle:
+    """batched_powerSGD_hook ("PowerSGD Hooks", batched_powerSGD_hook steps
+    1-9): the whole flat bucket of N elements is viewed as one square matrix
+    of side ceil(sqrt(N)) with zero padding, compressed by one PowerSGD step,
+    and the result truncated to N elements.  Reading: error feedback (one
+    residual per replica) covers the whole padded square, as the per-tensor
+    hook's covers each compressed tensor; there is no compression-rate gate.
+    """
+
+    numel: int
+    world_size: int
+    matrix_approximation_rank: int = 1
+    start_powerSGD_iter: int = 1000
+    use_error_feedback: bool = True
+    warm_start: bool = True
+    orthogonalization_epsilon: float = 0.0
+    random_seed: int = 0
+    iter: int = 0
+    q: object = None
+    error: dict = field(default_factory=dict)
+    last_p: object = None
+    _draw: object = None
+
+    def __post_init__(self):
+        self.side = math.isqrt(self.numel - 1) + 1 if self.numel > 0 else 0
+        self.rank = min(self.matrix_approximation_rank, self.side)
+
+    def set_q_draw(self, draw):
+        self._draw = np.asarray(draw, dtype=np.float64).reshape(self.side, self.rank).copy()
+
+    def step(self, grads, inv_loss_scale=1.0):
+        g = [np.asarray(x).reshape(-1).astype(np.float64) * float(inv_loss_scale) for x in grads]
+        assert len(g) == self.world_size and all(x.size == self.numel for x in g)
+        if not all(np.all(np.isfinite(x)) for x in g):
+            self.iter += 1
+            return SKIPPED, None
+        if self.iter < self.start_powerSGD_iter:
+            self.iter += 1
+            return OK, allreduce_mean(g)
+        n = self.side
+        # 1: the square view with zero padding (plus the replica's residual)
+        m_w = []
+        for w in range(self.world_size):
+            sq = np.zeros(n * n)
+            sq[:self.numel] = g[w]
+            sq = sq.reshape(n, n)
+            if self.use_error_feedback and w in self.error:
+                sq = sq + self.error[w]
+            m_w.append(sq)
+        # 2: Q from a standard-normal draw, orthogonalised, unless warm
+        if self.warm_start and self.q is not None:
+            q = self.q
+        else:
+            if self._draw is None:
+                rng = np.random.default_rng((self.random_seed, self.iter))
+                self._draw = rng.standard_normal((n, self.rank))
+            q = orthogonalize(self._draw, self.orthogonalization_epsilon)
+            self._draw = None
+        # 3-5: P = M Q, allreduce (mean), orthogonalise
+        p = orthogonalize(allreduce_mean([compute_p(m, q) for m in m_w]), self.orthogonalization_epsilon)
+        # 6-7: Q = M^T P, allreduce (mean)
+        q_new = allreduce_mean([compute_q(m, p) for m in m_w])
+        # 8: M ~ P Q^T; 9: truncate to the original length
+        m_hat = decompress(p, q_new)
+        if self.use_error_feedback:
+            for w in range(self.world_size):
+                self.error[w] = m_w[w] - m_hat
+        self.q = q_new
+        self.last_p = p
+        self.iter += 1
+        return OK, m_hat.reshape(-1)[:self.numel].copy()
+
+    def error_of(self, replica):
+        return self.error.get(replica, np.zeros((self.side, self.side)))

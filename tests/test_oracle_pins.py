@@ -487,3 +487,55 @@ def test_box_muller_moments():
     assert abs(z.mean()) < 0.02
     assert abs(z.var() - 1.0) < 0.03
     assert abs(np.mean(z ** 4) - 3.0) < 0.15   # Gaussian kurtosis
+
+
+# --------------------------------------------------------------------------
+# batched_powerSGD_hook
+# --------------------------------------------------------------------------
+def check_batched_golden():
+    """N = 4 is a square: the batched hook on the 2x2 worked example's matrix
+    gives the hand-worked values."""
+    g = _load("powersgd_2x2_two_replicas.json")
+    o = oracle.BatchedPowerSGDOracle(numel=4, world_size=2, matrix_approximation_rank=1,
+                                     start_powerSGD_iter=0)
+    o.set_q_draw(np.array(g["q_draw"]))
+    for st in g["steps"]:
+        _, out = o.step([np.array(x[:4]) for x in st["grads"]])
+        np.testing.assert_allclose(out, st["out"][:4], atol=1e-13)
+        for w in range(2):
+            np.testing.assert_allclose(o.error_of(w).reshape(-1), st["error"][w], atol=1e-13)
+
+
+def test_batched_golden():
+    check_batched_golden()
+
+
+@pytest.mark.parametrize("numel", [36, 37, 50, 1000])
+def test_batched_is_padded_square(numel):
+    """The batched hook equals the per-tensor hook run on the explicitly
+    zero-padded square matrix, truncated to the bucket's length."""
+    rng = np.random.default_rng(numel)
+    world, rank = 3, 2
+    b = oracle.BatchedPowerSGDOracle(numel=numel, world_size=world, matrix_approximation_rank=rank,
+                                     start_powerSGD_iter=1)
+    n = b.side
+    assert n * n >= numel > (n - 1) * (n - 1)
+    t = PowerSGDOracle(shapes=[(n, n)], world_size=world, matrix_approximation_rank=rank,
+                       start_powerSGD_iter=1, min_compression_rate=0.0)
+    draw = rng.standard_normal((n, min(rank, n)))
+    b.set_q_draw(draw)
+    t.set_q_draw(0, draw)
+    for step in range(4):
+        g = [rng.standard_normal(numel) for _ in range(world)]
+        padded = []
+        for x in g:
+            y = np.zeros(n * n)
+            y[:numel] = x
+            padded.append(y)
+        _, ob = b.step(g)
+        _, ot = t.step(padded)
+        if step == 0:
+            np.testing.assert_allclose(ob, sum(g) / world, atol=1e-14)   # vanilla phase
+        np.testing.assert_allclose(ob, ot[:numel], atol=1e-12)
+        for w in range(world):
+            np.testing.assert_allclose(b.error_of(w), t.error_of(w, 0), atol=1e-12)
