@@ -107,6 +107,27 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
                       int32_t batch_tensors_with_same_shape, psgd_dtype grad_dtype,
                       int32_t device, psgd_state** out);
 
+/*
+ * psgd_state_create_batched -- the state of [DDP] batched_powerSGD_hook
+ * ("PowerSGD Hooks", batched_powerSGD_hook steps 1-9): the whole flat bucket
+ * of `numel` elements is viewed as ONE square matrix of side
+ * ceil(sqrt(numel)), zero beyond the bucket, compressed by one PowerSGD step
+ * per psgd_step call, and the result truncated to `numel` elements.  There
+ * is no compression-rate gate.  Error feedback covers the padded square
+ * (psgd_error_numel = side * side; tensor 0 of psgd_tensor_info is the
+ * square).  Other arguments as psgd_state_create; psgd_step and the other
+ * calls work unchanged on the returned state.  Rows are read with 16-byte
+ * vector accesses when side is a multiple of 4, element by element
+ * otherwise.
+ * Errors: PSGD_EINVAL (numel < 1, rank outside [1, 32], ...), PSGD_ENOMEM,
+ * PSGD_ECUDA.
+ */
+int psgd_state_create_batched(int64_t numel, int32_t world_size, int32_t matrix_approximation_rank,
+                              int64_t start_powerSGD_iter, int32_t use_error_feedback,
+                              int32_t warm_start, float orthogonalization_epsilon,
+                              uint64_t random_seed, psgd_dtype grad_dtype, int32_t device,
+                              psgd_state** out);
+
 /* Frees every device and host allocation of the state.  NULL is a no-op. */
 void psgd_state_destroy(psgd_state* s);
 

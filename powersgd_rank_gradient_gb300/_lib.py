@@ -25,7 +25,8 @@ PSGD_MAX_WORLD = 64
 
 # every symbol include/psgd.h declares
 EXPORTS = [
-    "psgd_plan", "psgd_state_create", "psgd_state_destroy", "psgd_step", "psgd_step_host",
+    "psgd_plan", "psgd_state_create", "psgd_state_create_batched", "psgd_state_destroy",
+    "psgd_step", "psgd_step_host",
     "psgd_step_status", "psgd_get_stats", "psgd_tensor_info", "psgd_error_numel", "psgd_set_q",
     "psgd_get_q", "psgd_get_p", "psgd_get_error", "psgd_set_error", "psgd_workspace_bytes",
     "psgd_profile", "psgd_profile_kinds", "psgd_profile_read", "psgd_last_error",
@@ -60,6 +61,9 @@ def lib():
                                     c_i32, ctypes.c_float, c_u64, c_i32, ctypes.c_int, c_i32,
                                     ctypes.POINTER(P)]
     L.psgd_state_create.restype = ctypes.c_int
+    L.psgd_state_create_batched.argtypes = [c_i64, c_i32, c_i32, c_i64, c_i32, c_i32, ctypes.c_float,
+                                            c_u64, ctypes.c_int, c_i32, ctypes.POINTER(P)]
+    L.psgd_state_create_batched.restype = ctypes.c_int
     L.psgd_state_destroy.argtypes = [P]
     L.psgd_state_destroy.restype = None
     L.psgd_step.argtypes = [P, ctypes.POINTER(P), P, ctypes.c_float, P]

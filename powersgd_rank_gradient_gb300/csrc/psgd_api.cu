@@ -50,6 +50,7 @@ struct HostTensor {
   int rank = 0;
   int cidx = -1;          // compressed ordinal
   long long e_off = -1;   // packed error offset
+  long long valid = -1;   // elements backed by the bucket (-1: all)
 };
 
 int next_pow2(int r) {
@@ -131,6 +132,7 @@ struct psgd_state {
   float eps = 0.f;
   unsigned long long seed = 0;
   int batch = 0;
+  int batched = 0;        // the batched hook's single padded square
   psgd_dtype dtype = PSGD_F32;
   // plan
   std::vector<HostTensor> tensors;
@@ -295,6 +297,7 @@ void build_plan(psgd_state* s) {
       td.n = (int)h.rows;
       td.m = (int)h.cols;
       td.r = h.rank;
+      td.valid = h.valid >= 0 ? h.valid : h.numel;
       td.ctiles = (int)((h.cols + CT - 1) / CT);
       td.ctiles1 = (int)((h.cols + CT1 - 1) / CT1);
       td.rblocks = (int)((h.rows + s->row_block - 1) / s->row_block);
@@ -577,6 +580,12 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 }  // namespace
 
+namespace {
+int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start_iter, double mcr,
+                  int32_t use_error_feedback, int32_t warm_start, float eps, uint64_t random_seed,
+                  int32_t batch, psgd_dtype grad_dtype, int32_t device, psgd_state** out);
+}  // namespace
+
 extern "C" {
 
 const char* psgd_last_error(void) { return g_last_error.c_str(); }
@@ -638,6 +647,53 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
     delete s;
     return rc;
   }
+  for (auto& h : s->tensors) s->N += h.numel;
+  return create_common(s, world_size, rank, start_iter, mcr, use_error_feedback, warm_start, eps, random_seed,
+                       batch, grad_dtype, device, out);
+}
+
+// The batched hook: one compressed (side x side) view of the whole bucket,
+// side = ceil(sqrt(numel)), backed by the bucket for its first `numel`
+// elements and zero beyond.
+int psgd_state_create_batched(int64_t numel, int32_t world_size, int32_t rank, int64_t start_iter,
+                              int32_t use_error_feedback, int32_t warm_start, float eps, uint64_t random_seed,
+                              psgd_dtype grad_dtype, int32_t device, psgd_state** out) {
+  if (!out) return fail(PSGD_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (numel < 1) return fail(PSGD_EINVAL, "numel must be >= 1");
+  if (rank < 1 || rank > PSGD_MAX_RANK) return fail(PSGD_EINVAL, "matrix_approximation_rank must be in [1, 32]");
+  if (world_size < 1 || world_size > PSGD_MAX_WORLD) return fail(PSGD_EINVAL, "world_size must be in [1, 64]");
+  if (start_iter < 0) return fail(PSGD_EINVAL, "start_powerSGD_iter < 0");
+  if (!(eps >= 0.f)) return fail(PSGD_EINVAL, "orthogonalization_epsilon must be >= 0");
+  if (grad_dtype != PSGD_F32 && grad_dtype != PSGD_F16 && grad_dtype != PSGD_BF16)
+    return fail(PSGD_EINVAL, "grad_dtype");
+  long long side = (long long)std::sqrt((double)numel);
+  while (side * side < numel) ++side;
+  while (side > 1 && (side - 1) * (side - 1) >= numel) --side;
+  if (side > 2147483647LL) return fail(PSGD_EINVAL, "bucket too large");
+  psgd_state* s = new psgd_state();
+  HostTensor h;
+  h.shape = {side, side};
+  h.offset = 0;
+  h.numel = side * side;
+  h.compressed = 1;
+  h.rows = side;
+  h.cols = side;
+  h.rank = (int)std::min<long long>(rank, side);
+  h.valid = numel;
+  s->tensors.push_back(h);
+  s->N = numel;
+  s->batched = 1;
+  return create_common(s, world_size, rank, start_iter, 0.0, use_error_feedback, warm_start, eps, random_seed,
+                       0, grad_dtype, device, out);
+}
+
+}  // extern "C"
+
+namespace {
+int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start_iter, double mcr,
+                  int32_t use_error_feedback, int32_t warm_start, float eps, uint64_t random_seed,
+                  int32_t batch, psgd_dtype grad_dtype, int32_t device, psgd_state** out) {
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
     cudaGetLastError();
@@ -657,7 +713,6 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
   s->seed = random_seed;
   s->batch = batch ? 1 : 0;
   s->dtype = grad_dtype;
-  for (auto& h : s->tensors) s->N += h.numel;
   cudaDeviceGetAttribute(&s->sms, cudaDevAttrMultiProcessorCount, device);
   build_plan(s);
   // Where pass 2 reads the replica mean: a scratch copy written by pass 1
@@ -749,6 +804,9 @@ int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tenso
   return PSGD_OK;
 #undef TRY
 }
+}  // namespace
+
+extern "C" {
 
 int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_loss_scale, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
@@ -897,11 +955,8 @@ int psgd_step_status(psgd_state* s, void* stream) {
 
 int psgd_get_stats(const psgd_state* s, int64_t* before, int64_t* after, int64_t* iter) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
-  long long b = 0, a = 0;
-  for (auto& h : s->tensors) {
-    b += h.numel;
-    a += h.compressed ? (h.rows + h.cols) * h.rank : h.numel;
-  }
+  long long b = s->N, a = 0;
+  for (auto& h : s->tensors) a += h.compressed ? (h.rows + h.cols) * h.rank : h.numel;
   if (before) *before = b;
   if (after) *after = a;
   if (iter) *iter = s->iter;

@@ -44,6 +44,8 @@ struct TensorDesc {
   long long pp_off;  // first element of praw_part (ctiles1 x rows x RP)
   long long qp_off;  // first element of qpart (rblocks x RP x cols; 32-aligned)
   long long e_off;   // first element in the user-visible packed error (no padding)
+  long long valid;   // elements of the view backed by the bucket (n * m, or the bucket
+                     // length for the batched hook's zero-padded square)
   int n, m, r;       // rows, cols, effective rank
   int ctiles;        // column tiles of passes 2 and 3
   int ctiles1;       // column tiles of pass 1 (praw_part slices)

@@ -346,7 +346,16 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
           if (!rv[q]) continue;
           const long long i = item.row0 + rr + q;
           float gv[NC];
-          load_grad<NC, GT>(g + td.g_off + i * m + c, gv);
+          if (i * m + c + NC <= td.valid) {
+            load_grad<NC, GT>(g + td.g_off + i * m + c, gv);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+              float t1[1] = {0.f};
+              if (i * m + c + cc < td.valid) load_grad<1, GT>(g + td.g_off + i * m + c + cc, t1);
+              gv[cc] = t1[0];
+            }
+          }
           float ev[NC];
           if (a.ef) load_f<NC>(ecur + i * m + c, ev, false);
           float mv[NC];
@@ -492,11 +501,14 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 #pragma unroll
     for (int q = 0; q < RW; ++q) {
       if (rr + q >= item.nrows || !cin) continue;
+      const bool gfull = grow[q] - td.g_off + c + 4 <= td.valid;
 #pragma unroll
       for (int w = 0; w < WT; ++w) {
         const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + grow[q] + c;
         char* gdst = slot + (q * WT + w) * St::GSEG + lane * GB;
-        if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+        if (gfull) {
+          if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+        }
         if (a.ef) {
           const float* esrc = a.estore + erow[q] + (long long)w * a.nc_pad + c;
           cp_async16(slot + RW * WT * St::GSEG + (q * WT + w) * St::ESEG + lane * 16, esrc);
@@ -578,11 +590,22 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
           if (!rv[q]) continue;
           const long long i = item.row0 + rr + q;
           float gv[4];
-          if constexpr (GB == 16) {
-            const float4 x = *reinterpret_cast<const float4*>(slot + (q * WT + w) * St::GSEG + lane * GB);
-            gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
+          if (i * m + c + 4 <= td.valid) {
+            if constexpr (GB == 16) {
+              const float4 x = *reinterpret_cast<const float4*>(slot + (q * WT + w) * St::GSEG + lane * GB);
+              gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
+            } else {
+              cvt4<GT>(*reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB), gv);
+            }
           } else {
-            cvt4<GT>(*reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB), gv);
+            // the bucket ends inside (or before) this chunk: padding is zero
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              float t1[1] = {0.f};
+              if (i * m + c + cc < td.valid)
+                load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + i * m + c + cc, t1);
+              gv[cc] = t1[0];
+            }
           }
           float ev[4] = {0.f, 0.f, 0.f, 0.f};
           if (a.ef) {
@@ -716,11 +739,14 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         const long long row = item.row0 + phase + (long long)u * wpc;
         const long long go = td.g_off + row * m + c;
         const long long eo = (long long)cur * a.W * a.nc_pad + td.c_off + row * m + c;
+        const bool gfull = row * m + c + 4 <= td.valid;
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
           const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
           char* gdst = slot + w * St::GSEG + lane * GB;
-          if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+          if (gfull) {
+            if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+          }
           if (a.ef) cp_async16(slot + WT * St::GSEG + w * St::ESEG + lane * 16, a.estore + eo + (long long)w * a.nc_pad);
         }
       }
@@ -749,14 +775,26 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         }
         float mb[4] = {0.f, 0.f, 0.f, 0.f};
         float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + td.c_off + i * m + c;
+        const bool gfull = i * m + c + 4 <= td.valid;
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
           float gv[4];
-          if constexpr (GB == 16) {
-            const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
-            gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
+          if (gfull) {
+            if constexpr (GB == 16) {
+              const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
+              gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
+            } else {
+              cvt4<GT>(*reinterpret_cast<const uint2*>(slot + w * St::GSEG + lane * GB), gv);
+            }
           } else {
-            cvt4<GT>(*reinterpret_cast<const uint2*>(slot + w * St::GSEG + lane * GB), gv);
+            // the bucket ends inside (or before) this chunk: padding is zero
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              float t1[1] = {0.f};
+              if (i * m + c + cc < td.valid)
+                load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + i * m + c + cc, t1);
+              gv[cc] = t1[0];
+            }
           }
           float mv[4];
           if (a.ef) {
@@ -1182,13 +1220,13 @@ __device__ __forceinline__ void load_mbar(const StepArgs& a, const TensorDesc& t
         }
       } else {
         const GT* src = reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + row * m + c0;
-        if constexpr (VEC) {
-          load_grad<4, GT>(src, v);
+        if (VEC && row * m + c0 + 4 <= td.valid) {
+          if constexpr (VEC) load_grad<4, GT>(src, v);
         } else {
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
             float t[1] = {0.f};
-            if (c0 + c < cend) load_grad<1, GT>(src + c, t);
+            if (c0 + c < cend && row * m + c0 + c < td.valid) load_grad<1, GT>(src + c, t);
             v[c] = t[0];
           }
         }
@@ -1370,7 +1408,14 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
       for (int c = 0; c < CPT; ++c) o[c] = dot_chain<RP>(pr, qv[c]);
       if constexpr (NC == CPT && CPT == 4) {
         if constexpr (MODE == 0) {
-          store_f<4>(a.out + td.g_off + row * m + c0, o);
+          if (row * m + c0 + 4 <= td.valid) {
+            store_f<4>(a.out + td.g_off + row * m + c0, o);
+          } else {
+            // the bucket ends inside this chunk (batched hook): truncate
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (row * m + c0 + c < td.valid) st_stream1(a.out + td.g_off + row * m + c0 + c, o[c]);
+          }
         } else if constexpr (MODE == 1) {
           float sv[4];
           load_f<4>(store + td.c_off + row * m + c0, sv, true);
@@ -1389,7 +1434,7 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
           if (c0 + c >= cend) continue;
           const long long idx = row * m + c0 + c;
           if constexpr (MODE == 0) {
-            st_stream1(a.out + td.g_off + idx, o[c]);
+            if (idx < td.valid) st_stream1(a.out + td.g_off + idx, o[c]);
           } else if constexpr (MODE == 1) {
             a.eio[td.e_off + idx] = store[td.c_off + idx] - o[c];
           } else if constexpr (MODE == 2) {

@@ -175,6 +175,50 @@ class PowerSGDState:
         return res
 
 
+class BatchedPowerSGDState(PowerSGDState):
+    """State of batched_powerSGD_hook ("PowerSGD Hooks"): the whole flat
+    bucket of ``numel`` elements is compressed as one zero-padded square
+    matrix of side ceil(sqrt(numel)); the result is truncated to ``numel``."""
+
+    def __init__(self, numel, world_size, matrix_approximation_rank=1, start_powerSGD_iter=1000,
+                 use_error_feedback=True, warm_start=True, orthogonalization_epsilon=0.0,
+                 random_seed=0, grad_dtype=torch.float32, device=None):
+        if device is None:
+            device = torch.cuda.current_device()
+        device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        if grad_dtype not in (torch.float32, torch.float16, torch.bfloat16):
+            raise ValueError("grad_dtype must be torch.float32, torch.float16 or torch.bfloat16")
+        self.shapes = None
+        self.world_size = int(world_size)
+        self.matrix_approximation_rank = int(matrix_approximation_rank)
+        self.start_powerSGD_iter = int(start_powerSGD_iter)
+        self.min_compression_rate = 0.0
+        self.use_error_feedback = bool(use_error_feedback)
+        self.warm_start = bool(warm_start)
+        self.orthogonalization_epsilon = float(orthogonalization_epsilon)
+        self.random_seed = int(random_seed)
+        self.batch_tensors_with_same_shape = False
+        self.grad_dtype = grad_dtype
+        self.device = device
+        self.numel = int(numel)
+        L = _lib.lib()
+        handle = ctypes.c_void_p()
+        check(L.psgd_state_create_batched(
+            self.numel, self.world_size, self.matrix_approximation_rank, self.start_powerSGD_iter,
+            int(self.use_error_feedback), int(self.warm_start), self.orthogonalization_epsilon,
+            self.random_seed & (2**64 - 1),
+            {torch.float16: PSGD_F16, torch.bfloat16: PSGD_BF16}.get(grad_dtype, PSGD_F32),
+            device.index or 0, ctypes.byref(handle)))
+        self._h = handle
+        self._lib = L
+        self.side = self.tensor_info(0)["rows"]
+
+
+def batched_powerSGD_hook(state, grads, out=None, inv_loss_scale=1.0, stream=None):
+    """One call of batched_powerSGD_hook ("PowerSGD Hooks") on the W replica buckets."""
+    return state.step(grads, out=out, inv_loss_scale=inv_loss_scale, stream=stream)
+
+
 def powerSGD_hook(state, grads, out=None, inv_loss_scale=1.0, stream=None):
     """One hook call ("PowerSGD Hooks", powerSGD_hook) on the W replica buckets."""
     return state.step(grads, out=out, inv_loss_scale=inv_loss_scale, stream=stream)
