@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--rank", type=int, default=None, help="rank of the rank-sweep workload")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling cases: only this many transformer layers, no embeddings")
+    ap.add_argument("--batched", action="store_true",
+                    help="also time batched_powerSGD_hook on the workload's bucket (one padded square)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -300,6 +302,8 @@ def run_native(spec, args, dist, rank_id, world, device):
                        "survey_min_frac_of_measured": sb["survey_min"] / (ms_step / 1e3) / 1e9 / peak},
         kernels=kernels, counts=counts)
     res["rows"] = run_rows(spec, args, dist, device, sets, out, W, N)
+    if args.batched:
+        res["rows"]["next_batched_hook"] = run_batched(spec, args, dist, device, sets, out, W, N)
     del sets
     torch.cuda.empty_cache()
     if not args.no_e2e:
@@ -359,6 +363,41 @@ def run_rows(spec, args, dist, device, sets, out, W, N):
     rows["A3_first_compressed_call"] = {"ms": times[0], "next_calls_ms": times[1:],
                                         "q_init_overhead_ms": times[0] - min(times[1:])}
     return rows
+
+
+def run_batched(spec, args, dist, device, sets, out, W, N):
+    """batched_powerSGD_hook on the same bucket: one zero-padded square of
+    side ceil(sqrt(N)), warm-started steps."""
+    import torch
+
+    from powersgd_rank_gradient_gb300 import BatchedPowerSGDState
+
+    stream = torch.cuda.current_stream(device)
+    st = BatchedPowerSGDState(N, W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
+                              device=device)
+    for i in range(3):
+        st.step(sets[i % 2], out=out)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        st.step(sets[i % 2], out=out)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
+    # per-kind kernel times on separate (profiled) steps
+    st.profile(True)
+    st.profile_read()
+    for i in range(args.steps):
+        st.step(sets[i % 2], out=out)
+    torch.cuda.synchronize(device)
+    kinds = {k: round(v[1] / args.steps, 4) for k, v in st.profile_read().items() if v[0]}
+    st.profile(False)
+    side = st.side
+    st.close()
+    return {"side": side, "vector_path": side % 4 == 0, "ms_per_step": ms,
+            "gradient_gbs": W * N * 4 / (ms / 1e3) / 1e9, "kernel_ms_per_step": kinds}
 
 
 def run_e2e(st, spec, args, dist, device, N, W):

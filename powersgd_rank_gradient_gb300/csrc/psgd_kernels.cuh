@@ -229,18 +229,24 @@ __device__ __forceinline__ void load_row(const float* __restrict__ p, float (&v)
 
 // Columns c .. c+NC-1 of a k-major factor (element (j, k) at base + k * ld + j):
 // v[cc][k].  One coalesced access per k across the warp.
-template <int RP, int NC>
+// Columns c .. c+NC-1 of a k-major Q block (leading dimension ld).  AL: the
+// NC = 4 columns are one aligned float4.  !AL: only the first `nvalid`
+// columns are read; the rest are zero.
+template <int RP, int NC, bool AL = true>
 __device__ __forceinline__ void load_qcols(const float* __restrict__ base, long long ld, long long c,
-                                           float (&v)[NC][RP]) {
+                                           float (&v)[NC][RP], int nvalid = NC) {
 #pragma unroll
   for (int k = 0; k < RP; ++k) {
     const float* p = base + (long long)k * ld + c;
-    if constexpr (NC == 4) {
+    if constexpr (NC == 4 && AL) {
       float4 x = __ldg(reinterpret_cast<const float4*>(p));
       v[0][k] = x.x; v[1][k] = x.y; v[2][k] = x.z; v[3][k] = x.w;
-    } else {
+    } else if constexpr (AL) {
 #pragma unroll
       for (int cc = 0; cc < NC; ++cc) v[cc][k] = __ldg(p + cc);
+    } else {
+#pragma unroll
+      for (int cc = 0; cc < NC; ++cc) v[cc][k] = cc < nvalid ? __ldg(p + cc) : 0.f;
     }
   }
 }
@@ -411,6 +417,10 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -699,7 +709,10 @@ struct Pass1CS {
   static constexpr int SMEM = 8 * S * UNIT_BYTES + RED_BYTES;
 };
 
-template <int RP, int WT, typename GT, int MINB>
+// AL: rows are 16-byte aligned (vector copies and stores).  !AL (fp32 only):
+// rows of any alignment, copied into the same slots with 4-byte cp.async and
+// written back element by element.
+template <int RP, int WT, typename GT, int MINB, bool AL>
 __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDesc& td, const Item& item,
                                               const float* __restrict__ Qp, const float* __restrict__ Qc,
                                               const float* __restrict__ Pc, int cur, float& chk,
@@ -729,9 +742,10 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
     for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
       for (int k = 0; k < RP; ++k) { qc[cc][k] = 0.f; qp[cc][k] = 0.f; }
+    const int ncv = cin ? (int)min(4LL, (long long)cend - c) : 0;   // columns of this lane in the tile
     if (cin) {
-      if (a.ef) load_qcols<RP, 4>(Qc + td.q_off, m, c, qc);
-      if (!(a.ef && same_q)) load_qcols<RP, 4>(Qp + td.q_off, m, c, qp);
+      if (a.ef) load_qcols<RP, 4, AL>(Qc + td.q_off, m, c, qc, ncv);
+      if (!(a.ef && same_q)) load_qcols<RP, 4, AL>(Qp + td.q_off, m, c, qp, ncv);
     }
     auto issue = [&](int u) {
       char* slot = wsm + (u % S) * St::UNIT_BYTES;
@@ -744,10 +758,19 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         for (int w = 0; w < WT; ++w) {
           const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
           char* gdst = slot + w * St::GSEG + lane * GB;
-          if (gfull) {
-            if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+          char* edst = slot + WT * St::GSEG + w * St::ESEG + lane * 16;
+          const float* esrc = a.estore + eo + (long long)w * a.nc_pad;
+          if constexpr (AL) {
+            if (gfull) {
+              if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
+            }
+            if (a.ef) cp_async16(edst, esrc);
+          } else {
+            for (int cc = 0; cc < ncv; ++cc) {
+              if (row * m + c + cc < td.valid) cp_async4(gdst + 4 * cc, gsrc + cc);
+              if (a.ef) cp_async4(edst + 4 * cc, esrc + cc);
+            }
           }
-          if (a.ef) cp_async16(slot + WT * St::GSEG + w * St::ESEG + lane * 16, a.estore + eo + (long long)w * a.nc_pad);
         }
       }
       cp_async_commit();
@@ -775,11 +798,17 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         }
         float mb[4] = {0.f, 0.f, 0.f, 0.f};
         float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + td.c_off + i * m + c;
-        const bool gfull = i * m + c + 4 <= td.valid;
+        const bool gfull = AL ? (i * m + c + 4 <= td.valid) : false;
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
           float gv[4];
-          if (gfull) {
+          if (!AL) {
+            // staged element by element; padding and the tile's end are zero
+            const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) gv[cc] = (cc < ncv && i * m + c + cc < td.valid) ? xs[cc] : 0.f;
+          } else if (gfull) {
             if constexpr (GB == 16) {
               const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
               gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
@@ -799,14 +828,23 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
           float mv[4];
           if (a.ef) {
             const float4 x = *reinterpret_cast<const float4*>(slot + WT * St::GSEG + w * St::ESEG + lane * 16);
-            const float ev[4] = {x.x, x.y, x.z, x.w};
+            float ev[4] = {x.x, x.y, x.z, x.w};
+            if constexpr (!AL) {
+              // slots past the tile's last column hold stale bytes
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) ev[cc] = cc < ncv ? ev[cc] : 0.f;
+            }
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
               const float v = unit_scale ? gv[cc] : gv[cc] * a.scale;
               mv[cc] = v + (ev[cc] - corr[cc]);
               mb[cc] += mv[cc];
             }
-            store_f<4>(enxt + (long long)w * a.nc_pad, mv);
+            if constexpr (AL) {
+              store_f<4>(enxt + (long long)w * a.nc_pad, mv);
+            } else {
+              for (int cc = 0; cc < ncv; ++cc) st_stream1(enxt + (long long)w * a.nc_pad + cc, mv[cc]);
+            }
           } else {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -817,7 +855,13 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) mb[cc] *= a.invW;
-        if (a.mbar) store_f<4>(a.mbar + td.c_off + i * m + c, mb);
+        if (a.mbar) {
+          if constexpr (AL) {
+            store_f<4>(a.mbar + td.c_off + i * m + c, mb);
+          } else {
+            for (int cc = 0; cc < ncv; ++cc) st_stream1(a.mbar + td.c_off + i * m + c + cc, mb[cc]);
+          }
+        }
         const float (*qq)[RP] = (a.ef && same_q) ? qc : qp;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -858,7 +902,9 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
     const Item item = a.p1items[it];
     const TensorDesc td = a.tensors[item.t];
     if (td.vec && a.vec_ok)
-      pass1_tile_cs<RP, WT, GT, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+      pass1_tile_cs<RP, WT, GT, MINB, true>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+    else if constexpr (std::is_same<GT, float>::value)
+      pass1_tile_cs<RP, WT, GT, MINB, false>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
     else
       pass1_tile<RP, WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
   }
