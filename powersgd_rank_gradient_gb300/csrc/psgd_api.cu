@@ -146,6 +146,8 @@ struct psgd_state {
   std::vector<int> gsp_first, gsp_count, gsq_first, gsq_count;
   std::vector<Segment> unc_segs, all_segs;
   long long N = 0, Nc = 0, Nc_pad = 0, Nunc = 0, Ne = 0;
+  int any_aligned = 0;     // a compressed tensor's rows are 16-byte aligned
+  int any_unaligned = 0;   // a compressed tensor's rows are not
   long long p_total = 0, q_total = 0, pp_total = 0, qp_total = 0;
   int pass2_src = 0;  // 0 mbar scratch, 1 error store, 2 gradients
   int row_block = kRowBlock;  // rows per pass-2 item
@@ -296,6 +298,7 @@ void build_plan(psgd_state* s) {
       td.q_off = q_off;
       td.n = (int)h.rows;
       td.m = (int)h.cols;
+      td.ld = (int)((h.cols + 3) / 4 * 4);
       td.r = h.rank;
       td.valid = h.valid >= 0 ? h.valid : h.numel;
       td.ctiles = (int)((h.cols + CT - 1) / CT);
@@ -305,10 +308,11 @@ void build_plan(psgd_state* s) {
       td.qp_off = qp_off;
       td.e_off = e_off;
       td.vec = (h.cols % 4 == 0) && (h.offset % 4 == 0);
+      if (td.vec) s->any_aligned = 1; else s->any_unaligned = 1;
       h.cidx = (int)s->cdesc.size();
       h.e_off = e_off;
       s->cdesc.push_back(td);
-      c_off += (h.numel + 31) / 32 * 32;
+      c_off += (h.rows * td.ld + 31) / 32 * 32;
       auto r32 = [](long long x) { return (x + 31) / 32 * 32; };
       p_off += h.rows * RP;
       q_off += r32(h.cols * RP);
@@ -446,6 +450,9 @@ StepArgs make_args(psgd_state* s) {
   a.ef = s->ef;
   a.warm_start = s->warm;
   a.vec_ok = 1;
+  a.has_aligned = s->any_aligned;
+  a.has_unaligned = s->any_unaligned;
+  a.gn = s->N;
   a.eps = s->eps;
   return a;
 }
@@ -834,8 +841,8 @@ int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_los
   const int grid_seg = std::max(1, std::min<int>((int)s->all_segs.size(), s->sms * 4));
   bool compressed_step = false;
   if (s->iter < s->start_iter) {
-    // "Note that this communication hook enforces vanilla allreduce for the
-    // first state.start_powerSGD_iter iterations."
+    // before start_powerSGD_iter calls the hook only averages the replicas
+    // ("PowerSGD State", start_powerSGD_iter)
     L.begin(K_MEAN);
     launch_mean(a, s->d_all, (int)s->all_segs.size(), grid_seg, st);
     L.end();

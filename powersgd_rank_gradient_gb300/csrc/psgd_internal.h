@@ -47,6 +47,9 @@ struct TensorDesc {
   long long valid;   // elements of the view backed by the bucket (n * m, or the bucket
                      // length for the batched hook's zero-padded square)
   int n, m, r;       // rows, cols, effective rank
+  int ld;            // row stride in the error store and mbar: m rounded up to a
+                     // multiple of 4, so their rows are 16-byte aligned; the
+                     // padding columns stay zero
   int ctiles;        // column tiles of passes 2 and 3
   int ctiles1;       // column tiles of pass 1 (praw_part slices)
   int rblocks;       // row blocks

@@ -77,6 +77,9 @@ struct StepArgs {
   int ef;
   int warm_start;
   int vec_ok;          // grads/out base pointers allow 16-byte (8 for f16) accesses
+  int has_aligned;     // some compressed tensor has 16-byte aligned rows
+  int has_unaligned;   // some compressed tensor has not
+  long long gn;        // elements in each replica's bucket
   float eps;
   // error get/set
   int replica;
@@ -119,6 +122,9 @@ __device__ __forceinline__ void st_stream4(float* p, float4 v) {
 }
 __device__ __forceinline__ void st_stream1(float* p, float v) {
   asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_stream2(float* p, float a, float b) {
+  asm volatile("st.global.cs.v2.f32 [%0], {%1,%2};" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
 
 // NC consecutive elements of a gradient bucket as floats.  NC = 4 is one
@@ -363,7 +369,7 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
             }
           }
           float ev[NC];
-          if (a.ef) load_f<NC>(ecur + i * m + c, ev, false);
+          if (a.ef) load_f<NC>(ecur + i * td.ld + c, ev, false);
           float mv[NC];
 #pragma unroll
           for (int cc = 0; cc < NC; ++cc) {
@@ -372,14 +378,14 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
             mv[cc] = a.ef ? v + (ev[cc] - corr[q][cc]) : v;
             mb[q][cc] += mv[cc];
           }
-          if (a.ef) store_f<NC>(enxt + i * m + c, mv);
+          if (a.ef) store_f<NC>(enxt + i * td.ld + c, mv);
         }
       }
 #pragma unroll
       for (int q = 0; q < RW; ++q) {
 #pragma unroll
         for (int cc = 0; cc < NC; ++cc) mb[q][cc] *= a.invW;
-        if (a.mbar && rv[q]) store_f<NC>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * m + c, mb[q]);
+        if (a.mbar && rv[q]) store_f<NC>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * td.ld + c, mb[q]);
       }
       {
         float qv[NC][RP];
@@ -500,7 +506,7 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
       for (int q = 0; q < RW; ++q) {
         const long long row = item.row0 + rr + q;
         grow[q] = td.g_off + row * m;
-        erow[q] = (long long)cur * a.W * a.nc_pad + td.c_off + row * m;
+        erow[q] = (long long)cur * a.W * a.nc_pad + td.c_off + row * td.ld;
       }
     }
     const int c = item.col0 + ich * 128 + lane * 4;
@@ -629,14 +635,14 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
             mv[cc] = a.ef ? v + (ev[cc] - corr[q][cc]) : v;
             mb[q][cc] += mv[cc];
           }
-          if (a.ef) store_f<4>(enxt + i * m + c, mv);
+          if (a.ef) store_f<4>(enxt + i * td.ld + c, mv);
         }
       }
 #pragma unroll
       for (int q = 0; q < RW; ++q) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) mb[q][cc] *= a.invW;
-        if (a.mbar && rv[q]) store_f<4>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * m + c, mb[q]);
+        if (a.mbar && rv[q]) store_f<4>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * td.ld + c, mb[q]);
       }
       if constexpr (QB == 4) {
         if (!(a.ef && same_q)) load_qcols<RP, 4>(Qp + td.q_off, m, c, qv);
@@ -695,13 +701,16 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 // shared memory; at the end of the item the CTA adds the chunk partials in
 // chunk order and writes one partial per (row, column tile).
 // ---------------------------------------------------------------------------
-template <int RP, int WT, typename GT, int MINB>
+template <int RP, int WT, typename GT, int MINB, bool SH = false>
 struct Pass1CS {
   static constexpr int NCH = ctile1_for(RP) / 128;                // chunks per column tile
   static constexpr int GB = 4 * (int)sizeof(GT);
   static constexpr int GSEG = 32 * GB;
   static constexpr int ESEG = 32 * 16;
-  static constexpr int UNIT_BYTES = WT * (GSEG + ESEG);           // one row x 128 columns
+  // rows of any alignment (SH): after the segments, the chunk that follows
+  // lane 31's, for every gradient and error segment
+  static constexpr int XOFF = WT * (GSEG + ESEG);
+  static constexpr int UNIT_BYTES = XOFF + (SH ? 2 * WT * 16 : 0);   // one row x 128 columns
   static constexpr int RED_BYTES = kFineRows * NCH * RP * 4;
   static constexpr int BUDGET = (MINB == 1 ? 200 * 1024 : 96 * 1024) - RED_BYTES;
   static constexpr int S_RAW = BUDGET / (8 * UNIT_BYTES);
@@ -709,21 +718,56 @@ struct Pass1CS {
   static constexpr int SMEM = 8 * S * UNIT_BYTES + RED_BYTES;
 };
 
-// AL: rows are 16-byte aligned (vector copies and stores).  !AL (fp32 only):
-// rows of any alignment, copied into the same slots with 4-byte cp.async and
-// written back element by element.
-template <int RP, int WT, typename GT, int MINB, bool AL>
+// Four values of a row that starts r elements (0..3, warp-uniform) into the
+// aligned chunk `lo`; `hi` is the next aligned chunk.
+__device__ __forceinline__ void shift_sel(const float (&lo)[4], const float (&hi)[4], int r, float (&v)[4]) {
+  switch (r) {
+    case 0: v[0] = lo[0]; v[1] = lo[1]; v[2] = lo[2]; v[3] = lo[3]; break;
+    case 1: v[0] = lo[1]; v[1] = lo[2]; v[2] = lo[3]; v[3] = hi[0]; break;
+    case 2: v[0] = lo[2]; v[1] = lo[3]; v[2] = hi[0]; v[3] = hi[1]; break;
+    default: v[0] = lo[3]; v[1] = hi[0]; v[2] = hi[1]; v[3] = hi[2]; break;
+  }
+}
+
+// Streams v[0..nv) to p, which sits r = (address / 4) mod 4 elements past a
+// 16-byte boundary: a full group of four is one 16-byte store (r = 0), two
+// 8-byte stores (r = 2) or 4 + 8 + 4 bytes (r odd).
+__device__ __forceinline__ void store4_split(float* p, const float (&v)[4], int nv, int r) {
+  if (nv == 4) {
+    if (r == 0) {
+      st_stream4(p, make_float4(v[0], v[1], v[2], v[3]));
+    } else if (r == 2) {
+      st_stream2(p, v[0], v[1]);
+      st_stream2(p + 2, v[2], v[3]);
+    } else {
+      st_stream1(p, v[0]);
+      st_stream2(p + 1, v[1], v[2]);
+      st_stream1(p + 3, v[3]);
+    }
+  } else {
+    for (int cc = 0; cc < nv; ++cc) st_stream1(p + cc, v[cc]);
+  }
+}
+
+// MODE 0: the tensor's rows are 16-byte aligned in the bucket.  MODE 1: the
+// bucket rows have any alignment (the base pointers are still aligned): each
+// lane stages the aligned gradient chunk that holds its first column, lane 31
+// also the chunk after it (at XOFF in the stage), and a lane takes its four
+// values from its own chunk and the next lane's.  The error store and mbar
+// rows (stride ld) are aligned in both modes.
+template <int RP, int WT, typename GT, int MINB, int MODE>
 __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDesc& td, const Item& item,
                                               const float* __restrict__ Qp, const float* __restrict__ Qc,
                                               const float* __restrict__ Pc, int cur, float& chk,
                                               char* __restrict__ wsm, float* __restrict__ red) {
-  using St = Pass1CS<RP, WT, GT, MINB>;
+  constexpr bool SH = (MODE == 1);
+  using St = Pass1CS<RP, WT, GT, MINB, SH>;
   constexpr int S = St::S;
   constexpr int GB = St::GB;
   constexpr int NCH = St::NCH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nxt = cur ^ 1;
-  const long long m = td.m;
+  const long long m = td.m, ld = td.ld;
   const int cend = item.col0 + item.ncols;
   const int nch = (item.ncols + 127) / 128;
   // wpc warps per chunk (rows interleaved among them): a full tile has one
@@ -736,41 +780,56 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
   if (warp < nch * wpc) {
     const int c = item.col0 + ch * 128 + lane * 4;
     const bool cin = c < cend;
+    const int ncv = cin ? (int)min(4LL, (long long)cend - c) : 0;   // this lane's columns in the tile
     const int units = phase < item.nrows ? (item.nrows - phase + wpc - 1) / wpc : 0;
     float qc[4][RP], qp[4][RP];
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
       for (int k = 0; k < RP; ++k) { qc[cc][k] = 0.f; qp[cc][k] = 0.f; }
-    const int ncv = cin ? (int)min(4LL, (long long)cend - c) : 0;   // columns of this lane in the tile
     if (cin) {
-      if (a.ef) load_qcols<RP, 4, AL>(Qc + td.q_off, m, c, qc, ncv);
-      if (!(a.ef && same_q)) load_qcols<RP, 4, AL>(Qp + td.q_off, m, c, qp, ncv);
+      if (a.ef) load_qcols<RP, 4, !SH>(Qc + td.q_off, m, c, qc, ncv);
+      if (!(a.ef && same_q)) load_qcols<RP, 4, !SH>(Qp + td.q_off, m, c, qp, ncv);
     }
     auto issue = [&](int u) {
       char* slot = wsm + (u % S) * St::UNIT_BYTES;
-      if (cin) {
-        const long long row = item.row0 + phase + (long long)u * wpc;
-        const long long go = td.g_off + row * m + c;
-        const long long eo = (long long)cur * a.W * a.nc_pad + td.c_off + row * m + c;
-        const bool gfull = row * m + c + 4 <= td.valid;
+      const long long row = item.row0 + phase + (long long)u * wpc;
+      const long long eo = (long long)cur * a.W * a.nc_pad + td.c_off + row * ld + c;
+      if constexpr (!SH) {
+        if (cin) {
+          const long long go = td.g_off + row * m + c;
+          const bool gfull = row * m + c + 4 <= td.valid;
+#pragma unroll
+          for (int w = 0; w < WT; ++w) {
+            const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
+            if (gfull) {
+              if constexpr (GB == 16) cp_async16(slot + w * St::GSEG + lane * GB, gsrc);
+              else cp_async8(slot + w * St::GSEG + lane * GB, gsrc);
+            }
+            if (a.ef) cp_async16(slot + WT * St::GSEG + w * St::ESEG + lane * 16, a.estore + eo + (long long)w * a.nc_pad);
+          }
+        }
+      } else {
+        // aligned chunk (element offset in the bucket) holding this lane's first column
+        const long long gp = td.g_off + row * m + c;
+        const int rg = (int)(gp & 3);
+        const bool gneed = c - rg < cend;
+        const bool gx = lane == 31 && rg > 0 && c + 4 - rg < cend;
+        auto gcopy = [&](char* dst, const GT* g, long long at) {
+          if (at + 4 <= a.gn) {
+            if constexpr (GB == 16) cp_async16(dst, g + at); else cp_async8(dst, g + at);
+          } else {
+            // the bucket ends inside this chunk
+            for (int e = 0; e < 4; ++e)
+              if (at + e < a.gn) reinterpret_cast<GT*>(dst)[e] = g[at + e];
+          }
+        };
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
-          const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
-          char* gdst = slot + w * St::GSEG + lane * GB;
-          char* edst = slot + WT * St::GSEG + w * St::ESEG + lane * 16;
-          const float* esrc = a.estore + eo + (long long)w * a.nc_pad;
-          if constexpr (AL) {
-            if (gfull) {
-              if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
-            }
-            if (a.ef) cp_async16(edst, esrc);
-          } else {
-            for (int cc = 0; cc < ncv; ++cc) {
-              if (row * m + c + cc < td.valid) cp_async4(gdst + 4 * cc, gsrc + cc);
-              if (a.ef) cp_async4(edst + 4 * cc, esrc + cc);
-            }
-          }
+          const GT* g = reinterpret_cast<const GT*>(a.grads.p[w]);
+          if (gneed) gcopy(slot + w * St::GSEG + lane * GB, g, gp - rg);
+          if (gx) gcopy(slot + St::XOFF + w * 16, g, gp - rg + 4);
+          if (cin && a.ef) cp_async16(slot + WT * St::GSEG + w * St::ESEG + lane * 16, a.estore + eo + (long long)w * a.nc_pad);
         }
       }
       cp_async_commit();
@@ -781,6 +840,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
     }
     for (int u = 0; u < units; ++u) {
       cp_async_wait<S - 2>();
+      if constexpr (SH) __syncwarp();   // lanes read their neighbour's chunk
       if (u + S - 1 < units) issue(u + S - 1); else cp_async_commit();
       const int rr = phase + u * wpc;
       const long long i = item.row0 + rr;
@@ -797,17 +857,31 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
           for (int cc = 0; cc < 4; ++cc) corr[cc] = dot_chain<RP>(po, qc[cc]);
         }
         float mb[4] = {0.f, 0.f, 0.f, 0.f};
-        float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + td.c_off + i * m + c;
-        const bool gfull = AL ? (i * m + c + 4 <= td.valid) : false;
+        float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + td.c_off + i * ld + c;
+        const long long lim = td.valid - (i * m + c);   // bucket-backed columns from c on
+        const bool gfull = lim >= 4;
+        // SH: columns taken from the bucket (the tile's and the bucket's ends)
+        const int nvg = lim >= ncv ? ncv : (lim > 0 ? (int)lim : 0);
+        const int rg = (int)((td.g_off + i * m + c) & 3);
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
           float gv[4];
-          if (!AL) {
-            // staged element by element; padding and the tile's end are zero
-            const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
-            const float xs[4] = {x.x, x.y, x.z, x.w};
+          if constexpr (SH) {
+            float lo[4], hi[4];
+            const char* own = slot + w * St::GSEG + lane * GB;
+            const char* nx = lane < 31 ? own + GB : slot + St::XOFF + w * 16;
+            if constexpr (GB == 16) {
+              const float4 x = *reinterpret_cast<const float4*>(own);
+              const float4 y = *reinterpret_cast<const float4*>(nx);
+              lo[0] = x.x; lo[1] = x.y; lo[2] = x.z; lo[3] = x.w;
+              hi[0] = y.x; hi[1] = y.y; hi[2] = y.z; hi[3] = y.w;
+            } else {
+              cvt4<GT>(*reinterpret_cast<const uint2*>(own), lo);
+              cvt4<GT>(*reinterpret_cast<const uint2*>(nx), hi);
+            }
+            shift_sel(lo, hi, rg, gv);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) gv[cc] = (cc < ncv && i * m + c + cc < td.valid) ? xs[cc] : 0.f;
+            for (int cc = 0; cc < 4; ++cc) gv[cc] = cc < nvg ? gv[cc] : 0.f;
           } else if (gfull) {
             if constexpr (GB == 16) {
               const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
@@ -820,31 +894,24 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
               float t1[1] = {0.f};
-              if (i * m + c + cc < td.valid)
-                load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + i * m + c + cc, t1);
+              if (cc < lim) load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + i * m + c + cc, t1);
               gv[cc] = t1[0];
             }
           }
           float mv[4];
           if (a.ef) {
             const float4 x = *reinterpret_cast<const float4*>(slot + WT * St::GSEG + w * St::ESEG + lane * 16);
-            float ev[4] = {x.x, x.y, x.z, x.w};
-            if constexpr (!AL) {
-              // slots past the tile's last column hold stale bytes
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc) ev[cc] = cc < ncv ? ev[cc] : 0.f;
-            }
+            // a lane's columns past cend are the store's padding (cend is
+            // m there, else a multiple of 4), which stays zero
+            const float ev[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
               const float v = unit_scale ? gv[cc] : gv[cc] * a.scale;
               mv[cc] = v + (ev[cc] - corr[cc]);
               mb[cc] += mv[cc];
             }
-            if constexpr (AL) {
-              store_f<4>(enxt + (long long)w * a.nc_pad, mv);
-            } else {
-              for (int cc = 0; cc < ncv; ++cc) st_stream1(enxt + (long long)w * a.nc_pad + cc, mv[cc]);
-            }
+            // SH: columns past m get 0 + (0 - 0), keeping the padding zero
+            store_f<4>(enxt + (long long)w * a.nc_pad, mv);
           } else {
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -855,13 +922,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) mb[cc] *= a.invW;
-        if (a.mbar) {
-          if constexpr (AL) {
-            store_f<4>(a.mbar + td.c_off + i * m + c, mb);
-          } else {
-            for (int cc = 0; cc < ncv; ++cc) st_stream1(a.mbar + td.c_off + i * m + c + cc, mb[cc]);
-          }
-        }
+        if (a.mbar) store_f<4>(a.mbar + td.c_off + i * ld + c, mb);
         const float (*qq)[RP] = (a.ef && same_q) ? qc : qp;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -870,8 +931,8 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       }
       const float tot = warp_reduce_scatter<RP>(pacc);
       chk = fmaf(tot, 0.f, chk);   // inf/NaN in the row's inputs reach the sums
-      constexpr int SH = 5 - log2_rp<RP>();
-      if ((lane & ((1 << SH) - 1)) == 0) red[(rr * NCH + ch) * RP + (lane >> SH)] = tot;
+      constexpr int SHF = 5 - log2_rp<RP>();
+      if ((lane & ((1 << SHF) - 1)) == 0) red[(rr * NCH + ch) * RP + (lane >> SHF)] = tot;
     }
     cp_async_wait<0>();
   }
@@ -885,10 +946,10 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
   __syncthreads();
 }
 
-template <int RP, int WT, typename GT, int MINB>
+template <int RP, int WT, typename GT, int MINB, int KIND>
 __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
   extern __shared__ __align__(16) char p1smem[];
-  using St = Pass1CS<RP, WT, GT, MINB>;
+  using St = Pass1CS<RP, WT, GT, MINB, KIND == 1>;
   const int cur = a.ctrl->cur;
   const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
   const float* Qc = a.Qf + (long long)cur * a.q_total;
@@ -901,12 +962,16 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
   for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
     const Item item = a.p1items[it];
     const TensorDesc td = a.tensors[item.t];
-    if (td.vec && a.vec_ok)
-      pass1_tile_cs<RP, WT, GT, MINB, true>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
-    else if constexpr (std::is_same<GT, float>::value)
-      pass1_tile_cs<RP, WT, GT, MINB, false>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
-    else
-      pass1_tile<RP, WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
+    const bool aligned = td.vec && a.vec_ok;
+    if constexpr (KIND == 0) {
+      if (aligned) pass1_tile_cs<RP, WT, GT, MINB, 0>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+    } else {
+      if (aligned) continue;
+      if (a.vec_ok)
+        pass1_tile_cs<RP, WT, GT, MINB, 1>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+      else
+        pass1_tile<RP, WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
+    }
   }
   bad |= !(chk == 0.f);
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
@@ -1240,14 +1305,14 @@ __host__ __device__ constexpr int row_batch_for(int rp) { return 32 / cpt_for(rp
 template <int SRC, typename GT, int WT, int NC, bool VEC>
 __device__ __forceinline__ void load_mbar(const StepArgs& a, const TensorDesc& td, long long row, int c0,
                                           int cend, int nxt, float (&mv)[NC]) {
-  const long long m = td.m;
+  const long long m = td.m, ld = td.ld;
   static_assert(!VEC || NC == 4, "vector path is 4 wide");
   if constexpr (SRC == 0) {
     if constexpr (VEC) {
-      load_f<4>(a.mbar + td.c_off + row * m + c0, mv, true);
+      load_f<4>(a.mbar + td.c_off + row * ld + c0, mv, true);
     } else {
 #pragma unroll
-      for (int c = 0; c < NC; ++c) mv[c] = (c0 + c < cend) ? ld_stream1(a.mbar + td.c_off + row * m + c0 + c) : 0.f;
+      for (int c = 0; c < NC; ++c) mv[c] = (c0 + c < cend) ? ld_stream1(a.mbar + td.c_off + row * ld + c0 + c) : 0.f;
     }
   } else {
     const int W = WT > 0 ? WT : a.W;
@@ -1257,7 +1322,7 @@ __device__ __forceinline__ void load_mbar(const StepArgs& a, const TensorDesc& t
     for (int w = 0; w < W; ++w) {
       float v[NC];
       if constexpr (SRC == 1) {
-        const float* src = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * m + c0;
+        const float* src = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * ld + c0;
         if constexpr (VEC) {
           load_f<4>(src, v, true);
         } else {
@@ -1333,10 +1398,11 @@ __device__ __forceinline__ void pass2_tile(const StepArgs& a, const TensorDesc& 
   }
   if (c0 >= cend) return;
   float* dst = a.qpart + td.qp_off + (long long)item.rb * RP * td.m;
+  const bool qvec = (td.m & 3) == 0;
 #pragma unroll
   for (int k = 0; k < RP; ++k) {
     float* d = dst + (long long)k * td.m + c0;
-    if constexpr (NA == 4 && NC == 4) {
+    if (NA == 4 && NC == 4 && qvec) {
       *reinterpret_cast<float4*>(d) = make_float4(acc[0][k], acc[1][k], acc[2][k], acc[3][k]);
     } else {
 #pragma unroll
@@ -1346,9 +1412,10 @@ __device__ __forceinline__ void pass2_tile(const StepArgs& a, const TensorDesc& 
   }
 }
 
-// The vector path needs 16-byte aligned rows of the source; unaligned tensors
-// take the element-wise path (NC = 1): same CPT columns per thread, one access
-// per element.
+// The vector path needs 16-byte aligned rows of the source: the mbar scratch
+// and the store always have them (stride ld); gradients read directly need
+// an aligned tensor, else the element-wise path (NC = 1): same CPT columns
+// per thread, one access per element.
 template <int RP, int SRC, typename GT, int WT>
 __global__ void __launch_bounds__(kThreads, 3) k_pass2(const StepArgs a) {
   __shared__ __align__(16) float ps[kPStage][RP];
@@ -1358,7 +1425,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_pass2(const StepArgs a) {
   for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
     const Item item = a.items[it];
     const TensorDesc td = a.tensors[item.t];
-    const bool vec = (SRC == 2) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
+    const bool vec = (SRC == 2) ? (td.vec && a.vec_ok) : true;
     if (vec && CPT == 4)
       pass2_tile<RP, SRC, GT, WT, CPT>(a, td, item, P, ps);
     else
@@ -1412,12 +1479,15 @@ __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
 // store from a.eio + P Q^T.  MODE 3: fold the factors into the store in place
 // (store -= P Q^T), after which the factors can be replaced.
 // ---------------------------------------------------------------------------
-template <int RP, int MODE, int NC>
+// SHF (MODE 0, CPT 4): out rows of any alignment, written through
+// store4_split.
+template <int RP, int MODE, int NC, bool SHF = false>
 __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& td, const Item& item,
                                            const float* __restrict__ P, const float* __restrict__ Q,
                                            float (*ps)[RP], float* __restrict__ store) {
   constexpr int CPT = cpt_for(RP);
-  const long long m = td.m;
+  static_assert(!SHF || (MODE == 0 && CPT == 4 && NC == 1), "shifted stores: out, 4 columns a thread");
+  const long long m = td.m, ld = td.ld;
   const int c0 = item.col0 + threadIdx.x * CPT;
   const int cend = item.col0 + item.ncols;
   float qv[CPT][RP];
@@ -1452,7 +1522,13 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
       float o[CPT];
 #pragma unroll
       for (int c = 0; c < CPT; ++c) o[c] = dot_chain<RP>(pr, qv[c]);
-      if constexpr (NC == CPT && CPT == 4) {
+      if constexpr (SHF) {
+        const long long pos = row * m + c0;
+        const long long lim = min((long long)cend - c0, td.valid - pos);
+        const int nv = lim >= 4 ? 4 : (lim > 0 ? (int)lim : 0);
+        const float ov[4] = {o[0], o[1], o[2], o[3]};
+        store4_split(a.out + td.g_off + pos, ov, nv, (int)((td.g_off + pos) & 3));
+      } else if constexpr (NC == CPT && CPT == 4) {
         if constexpr (MODE == 0) {
           if (row * m + c0 + 4 <= td.valid) {
             store_f<4>(a.out + td.g_off + row * m + c0, o);
@@ -1464,29 +1540,30 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
           }
         } else if constexpr (MODE == 1) {
           float sv[4];
-          load_f<4>(store + td.c_off + row * m + c0, sv, true);
+          load_f<4>(store + td.c_off + row * ld + c0, sv, true);
 #pragma unroll
           for (int c = 0; c < 4; ++c) a.eio[td.e_off + row * m + c0 + c] = sv[c] - o[c];
         } else if constexpr (MODE == 2) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) store[td.c_off + row * m + c0 + c] = a.eio[td.e_off + row * m + c0 + c] + o[c];
+          for (int c = 0; c < 4; ++c) store[td.c_off + row * ld + c0 + c] = a.eio[td.e_off + row * m + c0 + c] + o[c];
         } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) store[td.c_off + row * m + c0 + c] -= o[c];
+          for (int c = 0; c < 4; ++c) store[td.c_off + row * ld + c0 + c] -= o[c];
         }
       } else {
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
           if (c0 + c >= cend) continue;
-          const long long idx = row * m + c0 + c;
+          const long long idx = row * m + c0 + c;        // bucket / packed view
+          const long long sdx = row * ld + c0 + c;       // store
           if constexpr (MODE == 0) {
             if (idx < td.valid) st_stream1(a.out + td.g_off + idx, o[c]);
           } else if constexpr (MODE == 1) {
-            a.eio[td.e_off + idx] = store[td.c_off + idx] - o[c];
+            a.eio[td.e_off + idx] = store[td.c_off + sdx] - o[c];
           } else if constexpr (MODE == 2) {
-            store[td.c_off + idx] = a.eio[td.e_off + idx] + o[c];
+            store[td.c_off + sdx] = a.eio[td.e_off + idx] + o[c];
           } else {
-            store[td.c_off + idx] -= o[c];
+            store[td.c_off + sdx] -= o[c];
           }
         }
       }
@@ -1512,6 +1589,8 @@ __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
     const bool vec = (MODE == 0) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
     if (vec && CPT == 4)
       pass3_tile<RP, MODE, CPT>(a, td, item, P, Q, ps, store);
+    else if (MODE == 0 && CPT == 4 && a.vec_ok)
+      pass3_tile<RP, MODE, 1, MODE == 0 && CPT == 4>(a, td, item, P, Q, ps, store);
     else
       pass3_tile<RP, MODE, 1>(a, td, item, P, Q, ps, store);
   }

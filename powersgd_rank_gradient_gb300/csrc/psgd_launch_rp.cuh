@@ -33,13 +33,17 @@ void launch_pass1_staged(const StepArgs& a, int grid, cudaStream_t s) {
 
 template <int RP, int WT, typename GT, int MINB>
 void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
-  using St = Pass1CS<RP, WT, GT, MINB>;
+  using St0 = Pass1CS<RP, WT, GT, MINB, false>;
+  using St1 = Pass1CS<RP, WT, GT, MINB, true>;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, St::SMEM);
+    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, St0::SMEM);
+    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, St1::SMEM);
     configured = true;
   }
-  k_pass1_cs<RP, WT, GT, MINB><<<grid * MINB, kThreads, St::SMEM, s>>>(a);
+  if (a.vec_ok && a.has_aligned) k_pass1_cs<RP, WT, GT, MINB, 0><<<grid * MINB, kThreads, St0::SMEM, s>>>(a);
+  if (!a.vec_ok || a.has_unaligned)
+    k_pass1_cs<RP, WT, GT, MINB, 1><<<grid * MINB, kThreads, a.vec_ok ? St1::SMEM : 0, s>>>(a);
 }
 
 // grid = one CTA per SM; the kernels run MINB CTAs per SM.  Ranks up to 8 use

@@ -16,14 +16,17 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-@pytest.mark.parametrize("numel,world,rank", [(1000, 2, 1), (5000, 1, 4), (70001, 3, 4),
-                                              (1 << 20, 2, 8), ((1 << 20) + 3, 4, 2),
-                                              (25557032, 4, 1)])
-def test_batched_matches_oracle(numel, world, rank):
+@pytest.mark.parametrize("numel,world,rank,dtype", [
+    (1000, 2, 1, "f32"), (5000, 1, 4, "f32"), (70001, 3, 4, "f32"), (1 << 20, 2, 8, "f32"),
+    ((1 << 20) + 3, 4, 2, "f32"), (25557032, 4, 1, "f32"),
+    # side 1733: rows start at every offset mod 4 (the shifted-chunk pass 1)
+    (3000001, 2, 8, "f32"), (3000001, 2, 8, "bf16"), (70001, 8, 4, "bf16")])
+def test_batched_matches_oracle(numel, world, rank, dtype):
     from powersgd_rank_gradient_gb300 import BatchedPowerSGDState
 
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     st = BatchedPowerSGDState(numel, world, matrix_approximation_rank=rank, start_powerSGD_iter=1,
-                              device=DEV)
+                              grad_dtype=tdt, device=DEV)
     ref = oracle.BatchedPowerSGDOracle(numel=numel, world_size=world, matrix_approximation_rank=rank,
                                        start_powerSGD_iter=1)
     assert st.side == ref.side and st.error_numel() == ref.side ** 2
@@ -32,10 +35,12 @@ def test_batched_matches_oracle(numel, world, rank):
     ref.set_q_draw(draw.astype(np.float64))
     rng = np.random.default_rng(numel)
     for step in range(3):
-        g = [(rng.standard_normal(numel) * 1e-3).astype(np.float32) for _ in range(world)]
-        out = st.step([torch.from_numpy(x).to(DEV) for x in g])
+        g = [torch.from_numpy((rng.standard_normal(numel) * 1e-3).astype(np.float32)).to(tdt)
+             for _ in range(world)]
+        out = st.step([x.to(DEV) for x in g])
         assert not st.status()
-        _, exp = ref.step([x.astype(np.float64) for x in g])
+        # the oracle sees the same (bf16-rounded) values, widened to float64
+        _, exp = ref.step([x.double().numpy() for x in g])
         assert rel(out.double().cpu().numpy(), exp) <= REL_TOL, f"step {step}"
         if step >= 1:
             for w in range(world):
