@@ -147,7 +147,7 @@ struct psgd_state {
   std::vector<Segment> unc_segs, all_segs;
   long long N = 0, Nc = 0, Nc_pad = 0, Nunc = 0, Ne = 0;
   int any_aligned = 0;     // a compressed tensor's rows are 16-byte aligned
-  int any_unaligned = 0;   // a compressed tensor's rows are not
+  int any_unaligned = 0;   // some are not, or the bucket ends inside the view
   long long p_total = 0, q_total = 0, pp_total = 0, qp_total = 0;
   int pass2_src = 0;  // 0 mbar scratch, 1 error store, 2 gradients
   int row_block = kRowBlock;  // rows per pass-2 item
@@ -308,7 +308,8 @@ void build_plan(psgd_state* s) {
       td.qp_off = qp_off;
       td.e_off = e_off;
       td.vec = (h.cols % 4 == 0) && (h.offset % 4 == 0);
-      if (td.vec) s->any_aligned = 1; else s->any_unaligned = 1;
+      if (td.vec) s->any_aligned = 1;
+      if (!td.vec || td.valid < (long long)td.n * td.m) s->any_unaligned = 1;
       h.cidx = (int)s->cdesc.size();
       h.e_off = e_off;
       s->cdesc.push_back(td);
@@ -350,16 +351,22 @@ void build_plan(psgd_state* s) {
       if (it == shapes.end()) shapes.push_back(sh);
     }
   }
-  auto make_items = [&](std::vector<Item>* out, int rows_per_item, int ctw) {
+  // cut: end a row block at the first row the bucket does not wholly back
+  // (batched hook), so that the checked kernels get only the rows that need
+  // them.  Not for pass 2, whose row blocks index its partial sums.
+  auto make_items = [&](std::vector<Item>* out, int rows_per_item, int ctw, bool cut) {
     for (size_t c = 0; c < s->cdesc.size(); ++c) {
       const TensorDesc& td = s->cdesc[c];
       const int nct = (td.m + ctw - 1) / ctw;
-      for (int r0 = 0; r0 < td.n; r0 += rows_per_item)
+      const long long vr = td.valid / td.m;   // rows [0, vr) are wholly backed
+      for (int r0 = 0, r1; r0 < td.n; r0 = r1) {
+        r1 = std::min(r0 + rows_per_item, td.n);
+        if (cut && r0 < vr && vr < r1) r1 = (int)vr;
         for (int ct = 0; ct < nct; ++ct) {
           Item it;
           it.t = (int)c;
           it.row0 = r0;
-          it.nrows = std::min(rows_per_item, td.n - r0);
+          it.nrows = r1 - r0;
           it.col0 = ct * ctw;
           it.ncols = std::min(ctw, td.m - it.col0);
           it.rb = r0 / s->row_block;
@@ -367,6 +374,7 @@ void build_plan(psgd_state* s) {
           it.pad = group_of[c];
           out->push_back(it);
         }
+      }
     }
     // largest items first (static round-robin over a persistent grid); with
     // batching, same-shape groups stay together.
@@ -376,9 +384,9 @@ void build_plan(psgd_state* s) {
     });
     for (auto& it : *out) it.pad = 0;
   };
-  make_items(&s->items, s->row_block, CT);
-  make_items(&s->fitems, kFineRows3, CT);
-  make_items(&s->p1items, kFineRows, CT1);
+  make_items(&s->items, s->row_block, CT, false);
+  make_items(&s->fitems, kFineRows3, CT, true);
+  make_items(&s->p1items, kFineRows, CT1, true);
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const long long len = (long long)s->cdesc[c].m * RP;
     for (long long f = 0; f < len; f += 1024)

@@ -78,7 +78,7 @@ struct StepArgs {
   int warm_start;
   int vec_ok;          // grads/out base pointers allow 16-byte (8 for f16) accesses
   int has_aligned;     // some compressed tensor has 16-byte aligned rows
-  int has_unaligned;   // some compressed tensor has not
+  int has_unaligned;   // some has not, or the bucket ends inside its view
   long long gn;        // elements in each replica's bucket
   float eps;
   // error get/set
@@ -517,14 +517,11 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
 #pragma unroll
     for (int q = 0; q < RW; ++q) {
       if (rr + q >= item.nrows || !cin) continue;
-      const bool gfull = grow[q] - td.g_off + c + 4 <= td.valid;
 #pragma unroll
       for (int w = 0; w < WT; ++w) {
         const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + grow[q] + c;
         char* gdst = slot + (q * WT + w) * St::GSEG + lane * GB;
-        if (gfull) {
-          if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
-        }
+        if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
         if (a.ef) {
           const float* esrc = a.estore + erow[q] + (long long)w * a.nc_pad + c;
           cp_async16(slot + RW * WT * St::GSEG + (q * WT + w) * St::ESEG + lane * 16, esrc);
@@ -606,22 +603,11 @@ __device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const Tenso
           if (!rv[q]) continue;
           const long long i = item.row0 + rr + q;
           float gv[4];
-          if (i * m + c + 4 <= td.valid) {
-            if constexpr (GB == 16) {
-              const float4 x = *reinterpret_cast<const float4*>(slot + (q * WT + w) * St::GSEG + lane * GB);
-              gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
-            } else {
-              cvt4<GT>(*reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB), gv);
-            }
+          if constexpr (GB == 16) {
+            const float4 x = *reinterpret_cast<const float4*>(slot + (q * WT + w) * St::GSEG + lane * GB);
+            gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
           } else {
-            // the bucket ends inside (or before) this chunk: padding is zero
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              float t1[1] = {0.f};
-              if (i * m + c + cc < td.valid)
-                load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + i * m + c + cc, t1);
-              gv[cc] = t1[0];
-            }
+            cvt4<GT>(*reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB), gv);
           }
           float ev[4] = {0.f, 0.f, 0.f, 0.f};
           if (a.ef) {
@@ -749,8 +735,10 @@ __device__ __forceinline__ void store4_split(float* p, const float (&v)[4], int 
   }
 }
 
-// MODE 0: the tensor's rows are 16-byte aligned in the bucket.  MODE 1: the
-// bucket rows have any alignment (the base pointers are still aligned): each
+// MODE 0: the tensor's rows are 16-byte aligned in the bucket and the item
+// lies inside the bucket-backed part of the view (no bounds checks).  MODE 1:
+// the bucket rows have any alignment (the base pointers are still aligned),
+// and the view may end inside the item (batched hook's padding): each
 // lane stages the aligned gradient chunk that holds its first column, lane 31
 // also the chunk after it (at XOFF in the stage), and a lane takes its four
 // values from its own chunk and the next lane's.  The error store and mbar
@@ -798,14 +786,11 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       if constexpr (!SH) {
         if (cin) {
           const long long go = td.g_off + row * m + c;
-          const bool gfull = row * m + c + 4 <= td.valid;
 #pragma unroll
           for (int w = 0; w < WT; ++w) {
             const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
-            if (gfull) {
-              if constexpr (GB == 16) cp_async16(slot + w * St::GSEG + lane * GB, gsrc);
-              else cp_async8(slot + w * St::GSEG + lane * GB, gsrc);
-            }
+            if constexpr (GB == 16) cp_async16(slot + w * St::GSEG + lane * GB, gsrc);
+            else cp_async8(slot + w * St::GSEG + lane * GB, gsrc);
             if (a.ef) cp_async16(slot + WT * St::GSEG + w * St::ESEG + lane * 16, a.estore + eo + (long long)w * a.nc_pad);
           }
         }
@@ -858,11 +843,10 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         }
         float mb[4] = {0.f, 0.f, 0.f, 0.f};
         float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + td.c_off + i * ld + c;
-        const long long lim = td.valid - (i * m + c);   // bucket-backed columns from c on
-        const bool gfull = lim >= 4;
         // SH: columns taken from the bucket (the tile's and the bucket's ends)
+        const long long lim = SH ? td.valid - (i * m + c) : 4;
         const int nvg = lim >= ncv ? ncv : (lim > 0 ? (int)lim : 0);
-        const int rg = (int)((td.g_off + i * m + c) & 3);
+        const int rg = SH ? (int)((td.g_off + i * m + c) & 3) : 0;
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
           float gv[4];
@@ -882,20 +866,12 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
             shift_sel(lo, hi, rg, gv);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) gv[cc] = cc < nvg ? gv[cc] : 0.f;
-          } else if (gfull) {
+          } else {
             if constexpr (GB == 16) {
               const float4 x = *reinterpret_cast<const float4*>(slot + w * St::GSEG + lane * GB);
               gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
             } else {
               cvt4<GT>(*reinterpret_cast<const uint2*>(slot + w * St::GSEG + lane * GB), gv);
-            }
-          } else {
-            // the bucket ends inside (or before) this chunk: padding is zero
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              float t1[1] = {0.f};
-              if (cc < lim) load_grad<1, GT>(reinterpret_cast<const GT*>(a.grads.p[w]) + td.g_off + i * m + c + cc, t1);
-              gv[cc] = t1[0];
             }
           }
           float mv[4];
@@ -946,6 +922,11 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
   __syncthreads();
 }
 
+// KIND 0 takes the items of tensors with 16-byte aligned rows (when the
+// gradient pointers are aligned too) that lie wholly inside the bucket, and
+// skips the rest; KIND 1 takes the rest: shifted chunks (MODE 1) when the
+// pointers are aligned, else the element path.  Separate instantiations keep
+// the aligned kernel free of the other paths' registers and checks.
 template <int RP, int WT, typename GT, int MINB, int KIND>
 __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
   extern __shared__ __align__(16) char p1smem[];
@@ -962,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
   for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
     const Item item = a.p1items[it];
     const TensorDesc td = a.tensors[item.t];
-    const bool aligned = td.vec && a.vec_ok;
+    const bool aligned = td.vec && a.vec_ok && (long long)(item.row0 + item.nrows) * td.m <= td.valid;
     if constexpr (KIND == 0) {
       if (aligned) pass1_tile_cs<RP, WT, GT, MINB, 0>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
     } else {
@@ -993,7 +974,8 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_staged(const StepArgs 
   for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
     const Item item = a.p1items[it];
     const TensorDesc td = a.tensors[item.t];
-    if (td.vec && a.vec_ok)
+    // items the bucket does not wholly back (batched hook) take the checked path
+    if (td.vec && a.vec_ok && (long long)(item.row0 + item.nrows) * td.m <= td.valid)
       pass1_tile_staged<RP, WT, GT, RW, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, qtile);
     else
       pass1_tile<RP, WT, GT, RW, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
@@ -1480,8 +1462,8 @@ __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
 // (store -= P Q^T), after which the factors can be replaced.
 // ---------------------------------------------------------------------------
 // SHF (MODE 0, CPT 4): out rows of any alignment, written through
-// store4_split.
-template <int RP, int MODE, int NC, bool SHF = false>
+// store4_split.  BND: check each store against the end of the bucket.
+template <int RP, int MODE, int NC, bool SHF = false, bool BND = true>
 __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& td, const Item& item,
                                            const float* __restrict__ P, const float* __restrict__ Q,
                                            float (*ps)[RP], float* __restrict__ store) {
@@ -1530,7 +1512,7 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
         store4_split(a.out + td.g_off + pos, ov, nv, (int)((td.g_off + pos) & 3));
       } else if constexpr (NC == CPT && CPT == 4) {
         if constexpr (MODE == 0) {
-          if (row * m + c0 + 4 <= td.valid) {
+          if (!BND || row * m + c0 + 4 <= td.valid) {
             store_f<4>(a.out + td.g_off + row * m + c0, o);
           } else {
             // the bucket ends inside this chunk (batched hook): truncate
@@ -1587,7 +1569,11 @@ __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
     const Item item = a.fitems[it];
     const TensorDesc td = a.tensors[item.t];
     const bool vec = (MODE == 0) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
-    if (vec && CPT == 4)
+    // BND: the view may end inside the item (batched hook's padding)
+    const bool inside = (long long)(item.row0 + item.nrows) * td.m <= td.valid;
+    if (vec && CPT == 4 && inside)
+      pass3_tile<RP, MODE, CPT, false, false>(a, td, item, P, Q, ps, store);
+    else if (vec && CPT == 4)
       pass3_tile<RP, MODE, CPT>(a, td, item, P, Q, ps, store);
     else if (MODE == 0 && CPT == 4 && a.vec_ok)
       pass3_tile<RP, MODE, 1, MODE == 0 && CPT == 4>(a, td, item, P, Q, ps, store);
