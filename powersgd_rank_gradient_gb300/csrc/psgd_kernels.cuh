@@ -823,12 +823,21 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
     for (int u = 0; u < S - 1; ++u) {
       if (u < units) issue(u); else cp_async_commit();
     }
+    // the committed P row of the next unit is loaded one unit ahead
+    float pn[RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) pn[k] = 0.f;
+    if (a.ef && units > 0) load_row<RP>(Pc + td.p_off + (item.row0 + phase) * (long long)RP, pn);
     for (int u = 0; u < units; ++u) {
       cp_async_wait<S - 2>();
       if constexpr (SH) __syncwarp();   // lanes read their neighbour's chunk
       if (u + S - 1 < units) issue(u + S - 1); else cp_async_commit();
       const int rr = phase + u * wpc;
       const long long i = item.row0 + rr;
+      float po[RP];
+#pragma unroll
+      for (int k = 0; k < RP; ++k) po[k] = pn[k];
+      if (a.ef && u + 1 < units) load_row<RP>(Pc + td.p_off + (i + wpc) * RP, pn);
       float pacc[RP];
 #pragma unroll
       for (int k = 0; k < RP; ++k) pacc[k] = 0.f;
@@ -836,8 +845,6 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         const char* slot = wsm + (u % S) * St::UNIT_BYTES;
         float corr[4] = {0.f, 0.f, 0.f, 0.f};
         if (a.ef) {
-          float po[RP];
-          load_row<RP>(Pc + td.p_off + i * RP, po);
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) corr[cc] = dot_chain<RP>(po, qc[cc]);
         }
