@@ -51,6 +51,12 @@ def parse():
                     help="profiling cases: only this many transformer layers, no embeddings")
     ap.add_argument("--batched", action="store_true",
                     help="also time batched_powerSGD_hook on the workload's bucket (one padded square)")
+    ap.add_argument("--buckets", type=float, default=0.0,
+                    help="also time the workload split into DDP-style buckets of at most this many MB "
+                         "(tensors in reverse order), stepped on one stream, on --bucket-streams, and on "
+                         "--bucket-streams with CUDA-graph replay")
+    ap.add_argument("--bucket-streams", type=int, default=16,
+                    help="streams of the overlapped bucket-group runs (--buckets)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -304,6 +310,8 @@ def run_native(spec, args, dist, rank_id, world, device):
     res["rows"] = run_rows(spec, args, dist, device, sets, out, W, N)
     if args.batched:
         res["rows"]["next_batched_hook"] = run_batched(spec, args, dist, device, sets, out, W, N)
+    if args.buckets > 0:
+        res["rows"]["next_bucket_overlap"] = run_buckets(spec, args, dist, device, sets, W, N)
     del sets
     torch.cuda.empty_cache()
     if not args.no_e2e:
@@ -398,6 +406,78 @@ def run_batched(spec, args, dist, device, sets, out, W, N):
     st.close()
     return {"side": side, "vector_path": side % 4 == 0, "ms_per_step": ms,
             "gradient_gbs": W * N * 4 / (ms / 1e3) / 1e9, "kernel_ms_per_step": kinds}
+
+
+def ddp_buckets(shapes, cap_mb, elem_bytes=4):
+    """Tensor indices per bucket, DDP-style: tensors in reverse order, a new
+    bucket whenever the next tensor would take the current one past cap_mb."""
+    from powersgd_rank_gradient_gb300 import workloads as wl
+
+    cap = cap_mb * 2**20
+    buckets, cur, used = [], [], 0
+    for i in reversed(range(len(shapes))):
+        nb = wl.numel(shapes[i]) * elem_bytes
+        if cur and used + nb > cap:
+            buckets.append(cur)
+            cur, used = [], 0
+        cur.append(i)
+        used += nb
+    if cur:
+        buckets.append(cur)
+    return buckets
+
+
+def run_buckets(spec, args, dist, device, sets, W, N):
+    """The same iteration with the bucket split into DDP-style buckets, each
+    its own hook call: a PowerSGDGroup on one stream, on S, and on S with
+    each bucket's steady step replayed as a CUDA graph."""
+    import torch
+
+    from powersgd_rank_gradient_gb300 import PowerSGDGroup, workloads as wl
+
+    shapes = spec["shapes"]
+    idx = ddp_buckets(shapes, args.buckets)
+    off = [0]
+    for s_ in shapes:
+        off.append(off[-1] + wl.numel(s_))
+    bucket_shapes = [[shapes[i] for i in b] for b in idx]
+    # each bucket's replica inputs: the values of input set 0, in fresh tensors
+    grads = [[torch.cat([sets[0][w][off[i]:off[i + 1]] for i in b]) for w in range(W)] for b in idx]
+    outs = [torch.empty(g[0].numel(), dtype=torch.float32, device=device) for g in grads]
+    stream = torch.cuda.current_stream(device)
+    res = {"cap_mb": args.buckets, "n_buckets": len(idx),
+           "largest_bucket_mb": max(g[0].numel() for g in grads) * 4 / 2**20}
+    S = args.bucket_streams
+    for label, n_streams, graphs in (("serial", 1, False), (f"streams_{S}", S, False),
+                                     (f"streams_{S}_graphs", S, True)):
+        grp = PowerSGDGroup(bucket_shapes, W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
+                            min_compression_rate=spec["mcr"],
+                            batch_tensors_with_same_shape=spec["batch_same_shape"], n_streams=n_streams,
+                            graphs=graphs, device=device)
+
+        def iteration():
+            for b in range(len(idx)):
+                grp.step(b, grads[b], out=outs[b])
+            grp.wait()
+
+        for _ in range(max(3, args.warmup)):
+            iteration()
+        if grp.status():
+            raise RuntimeError("bucket group step was skipped (non-finite input)")
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            iteration()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        ms = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
+        res[label] = {"ms_per_step": ms, "gradient_gbs": W * N * 4 / (ms / 1e3) / 1e9}
+        grp.close()
+    del grads, outs
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(st, spec, args, dist, device, N, W):

@@ -177,6 +177,25 @@ int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out
                    float inv_loss_scale, void* stream);
 
 /*
+ * psgd_set_graph -- enable (1) or disable (0) CUDA-graph replay of the steady
+ * compressed step.  Once a state is past start_powerSGD_iter, has made its
+ * first compressed step and warm-starts Q, every step enqueues the same
+ * launches, and what is left to decide (skip on inf/NaN, the double-buffer
+ * half, warm or fresh Q after a skipped first step) is decided on the device.
+ * With graphs enabled, psgd_step captures that sequence once (on a private
+ * stream, executing nothing) for its grads/out pointers and inv_loss_scale,
+ * and afterwards enqueues it on `stream` with one cudaGraphLaunch while they
+ * stay the same; other pointers or another scale capture again.  Results are
+ * bit-identical to the launch-by-launch path.  Not used while profiling is on.
+ * For callers that step with the same buffers every iteration and want the
+ * host's launch cost out of the way (many small buckets).  Default: off.
+ */
+int psgd_set_graph(psgd_state* s, int32_t enable);
+
+/* Graph captures and replays so far (either pointer may be NULL). */
+int psgd_graph_stats(const psgd_state* s, int64_t* captures, int64_t* replays);
+
+/*
  * psgd_step_status -- synchronises `stream` and returns the outcome of the
  * last step enqueued: PSGD_OK, PSGD_SKIPPED_NONFINITE, or PSGD_ECUDA.
  */
@@ -287,6 +306,72 @@ int psgd_profile_read(psgd_state* s, int32_t kind, const char** name, int64_t* l
  */
 int psgd_project_q_static(const float* dev_m, const float* dev_p, float* dev_q, int64_t rows,
                           int64_t cols, int32_t rank, void* stream);
+
+/*
+ * Bucket groups -- overlap across buckets.
+ *
+ * [DDP] "What Does a Communication Hook Operate On?": DDP splits the
+ * gradients into buckets so that communication overlaps computation and calls
+ * the hook once per bucket as it becomes ready; the PowerSGD state keeps its
+ * error-feedback residuals and warm-start Qs per bucket.  A group holds one
+ * psgd_state per bucket, all with the same hyper-parameters, and steps each
+ * bucket on one of n_streams internal CUDA streams, so that one bucket's
+ * latency-bound launches (Gram-Schmidt stage, reductions) run beside another
+ * bucket's streaming passes.  The buckets' compressed tensors are numbered
+ * across the group in bucket order for the Q draws, so a group draws the
+ * same Qs as one state over the concatenated buckets.
+ */
+typedef struct psgd_group psgd_group; /* opaque, library-owned */
+
+#define PSGD_MAX_GROUP_STREAMS 16
+
+/*
+ * psgd_group_create -- n_buckets buckets; bucket b holds tensors_per_bucket[b]
+ * tensors, and dims/ndims list every tensor of every bucket in bucket order,
+ * as psgd_state_create takes them for one bucket.  The other arguments are
+ * psgd_state_create's and apply to every bucket; n_streams in [1, 16].
+ * Allocates every bucket's state and the streams on `device`.
+ * Errors: PSGD_EINVAL, PSGD_ENOMEM, PSGD_ECUDA (nothing is left allocated).
+ */
+int psgd_group_create(int32_t n_buckets, const int32_t* tensors_per_bucket, const int64_t* dims,
+                      const int32_t* ndims, int32_t world_size, int32_t matrix_approximation_rank,
+                      int64_t start_powerSGD_iter, double min_compression_rate,
+                      int32_t use_error_feedback, int32_t warm_start,
+                      float orthogonalization_epsilon, uint64_t random_seed,
+                      int32_t batch_tensors_with_same_shape, psgd_dtype grad_dtype,
+                      int32_t n_streams, int32_t device, psgd_group** out);
+
+/* Synchronises the group's streams and frees everything.  NULL is a no-op. */
+void psgd_group_destroy(psgd_group* g);
+
+/*
+ * psgd_group_step -- psgd_step of bucket `bucket` (grads/out/inv_loss_scale
+ * as there, sized for that bucket), enqueued on internal stream
+ * bucket mod n_streams after the work enqueued so far on `stream`.  Returns
+ * once enqueued; grads and out must stay valid until psgd_group_wait's
+ * stream has reached the step.  Each bucket is stepped once per training
+ * iteration, in any order.
+ * Errors: psgd_step's, and PSGD_EINVAL for a bucket index out of range.
+ */
+int psgd_group_step(psgd_group* g, int32_t bucket, const void* const* grads, float* out,
+                    float inv_loss_scale, void* stream);
+
+/* Makes `stream` wait for every bucket step enqueued so far.  Enqueues only. */
+int psgd_group_wait(psgd_group* g, void* stream);
+
+/*
+ * psgd_group_status -- psgd_group_wait, then synchronises `stream`:
+ * PSGD_SKIPPED_NONFINITE if the last step of any bucket was skipped ([AMP]
+ * inf/NaN; each bucket skips on its own inputs), else PSGD_OK.
+ */
+int psgd_group_status(psgd_group* g, void* stream);
+
+/* Bucket b's state, owned by the group (introspection, Q and error views,
+ * checkpointing); do not destroy it. */
+int psgd_group_bucket(psgd_group* g, int32_t bucket, psgd_state** out);
+
+/* Number of buckets (0 for NULL). */
+int32_t psgd_group_size(const psgd_group* g);
 
 /* Message of the last failing call on this thread ("" if none). */
 const char* psgd_last_error(void);

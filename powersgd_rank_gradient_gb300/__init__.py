@@ -7,7 +7,8 @@ to a CPU implementation.
 
 
 def __getattr__(name):
-    if name in ("PowerSGDState", "powerSGD_hook", "BatchedPowerSGDState", "batched_powerSGD_hook"):
+    if name in ("PowerSGDState", "powerSGD_hook", "BatchedPowerSGDState", "batched_powerSGD_hook",
+                "PowerSGDGroup"):
         from . import hook
 
         return getattr(hook, name)

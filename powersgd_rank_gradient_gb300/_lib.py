@@ -22,6 +22,7 @@ PSGD_F16 = 1
 PSGD_BF16 = 2
 PSGD_MAX_RANK = 32
 PSGD_MAX_WORLD = 64
+PSGD_MAX_GROUP_STREAMS = 16
 
 # every symbol include/psgd.h declares
 EXPORTS = [
@@ -31,6 +32,8 @@ EXPORTS = [
     "psgd_get_q", "psgd_get_p", "psgd_get_error", "psgd_set_error", "psgd_workspace_bytes",
     "psgd_profile", "psgd_profile_kinds", "psgd_profile_read", "psgd_last_error",
     "psgd_project_q_static",
+    "psgd_group_create", "psgd_group_destroy", "psgd_group_step", "psgd_group_wait",
+    "psgd_group_status", "psgd_group_bucket", "psgd_group_size", "psgd_set_graph", "psgd_graph_stats",
 ]
 
 _lib = None
@@ -99,6 +102,26 @@ def lib():
     L.psgd_profile_read.restype = ctypes.c_int
     L.psgd_project_q_static.argtypes = [P, P, P, c_i64, c_i64, c_i32, P]
     L.psgd_project_q_static.restype = ctypes.c_int
+    L.psgd_group_create.argtypes = [c_i32, pi32, pi64, pi32, c_i32, c_i32, c_i64, ctypes.c_double, c_i32,
+                                    c_i32, ctypes.c_float, c_u64, c_i32, ctypes.c_int, c_i32, c_i32,
+                                    ctypes.POINTER(P)]
+    L.psgd_group_create.restype = ctypes.c_int
+    L.psgd_group_destroy.argtypes = [P]
+    L.psgd_group_destroy.restype = None
+    L.psgd_group_step.argtypes = [P, c_i32, ctypes.POINTER(P), P, ctypes.c_float, P]
+    L.psgd_group_step.restype = ctypes.c_int
+    L.psgd_group_wait.argtypes = [P, P]
+    L.psgd_group_wait.restype = ctypes.c_int
+    L.psgd_group_status.argtypes = [P, P]
+    L.psgd_group_status.restype = ctypes.c_int
+    L.psgd_group_bucket.argtypes = [P, c_i32, ctypes.POINTER(P)]
+    L.psgd_group_bucket.restype = ctypes.c_int
+    L.psgd_group_size.argtypes = [P]
+    L.psgd_group_size.restype = c_i32
+    L.psgd_set_graph.argtypes = [P, c_i32]
+    L.psgd_set_graph.restype = ctypes.c_int
+    L.psgd_graph_stats.argtypes = [P, pi64, pi64]
+    L.psgd_graph_stats.restype = ctypes.c_int
     L.psgd_last_error.argtypes = []
     L.psgd_last_error.restype = ctypes.c_char_p
     _lib = L

@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpsgd.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["psgd_api.cu", "psgd_misc.cu", "psgd_static.cu"] + [f"kern_rp{r}.cu" for r in (1, 2, 4, 8, 16, 32)]
+SOURCES = ["psgd_api.cu", "psgd_misc.cu", "psgd_static.cu", "psgd_group.cu"] + [f"kern_rp{r}.cu" for r in (1, 2, 4, 8, 16, 32)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -131,6 +131,7 @@ struct psgd_state {
   int warm = 1;
   float eps = 0.f;
   unsigned long long seed = 0;
+  int tensor_base = 0;    // added to the compressed-tensor number in the draw's counter
   int batch = 0;
   int batched = 0;        // the batched hook's single padded square
   psgd_dtype dtype = PSGD_F32;
@@ -189,6 +190,15 @@ struct psgd_state {
   cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
   int set_used[2] = {0, 0};
   long long host_calls = 0;
+  // CUDA graph of the steady compressed step (psgd_set_graph): captured on
+  // s_cap for one (grads, out, scale) key and replayed while the key holds
+  int graph_mode = 0;
+  cudaStream_t s_cap = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  std::vector<const void*> gkey_grads;
+  const void* gkey_out = nullptr;
+  float gkey_scale = 0.f;
+  long long graph_captures = 0, graph_replays = 0;
   // counters
   long long iter = 0;
   long long compressed_launched = 0;
@@ -539,7 +549,7 @@ struct Ops {
     if (need_fresh) {
       cudaMemcpyAsync(s->d_mask, mask.data(), mask.size() * sizeof(int), cudaMemcpyHostToDevice, L.st);
       L.begin(K_RANDN);
-      launch_randn(a, s->d_mask, s->seed, (unsigned long long)s->iter, RP, grid_q, L.st);
+      launch_randn(a, s->d_mask, s->seed, (unsigned long long)s->iter, s->tensor_base, RP, grid_q, L.st);
       L.end();
       gs(s, a, L, 1);
     }
@@ -632,6 +642,8 @@ void psgd_state_destroy(psgd_state* s) {
   }
   if (s->s_in) cudaStreamDestroy(s->s_in);
   if (s->s_out) cudaStreamDestroy(s->s_out);
+  if (s->gexec) cudaGraphExecDestroy(s->gexec);
+  if (s->s_cap) cudaStreamDestroy(s->s_cap);
   if (s->h_status) cudaFreeHost(s->h_status);
   for (auto& v : s->ev)
     for (auto& e : v) {
@@ -823,6 +835,86 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
 
 extern "C" {
 
+}  // extern "C"
+
+namespace {
+
+// The work of one step, enqueued on `st`; host counters are the caller's.
+int enqueue_step(psgd_state* s, const StepArgs& a, cudaStream_t st, bool vanilla, bool compressed_step,
+                 bool need_fresh, const std::vector<int>& mask) {
+  Launcher L{s, st};
+  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, sizeof(int), st));
+  const int grid_seg = std::max(1, std::min<int>((int)s->all_segs.size(), s->sms * 4));
+  if (vanilla) {
+    // before start_powerSGD_iter calls the hook only averages the replicas
+    // ("PowerSGD State", start_powerSGD_iter)
+    L.begin(K_MEAN);
+    launch_mean(a, s->d_all, (int)s->all_segs.size(), grid_seg, st);
+    L.end();
+  } else {
+    if (!s->unc_segs.empty()) {
+      L.begin(K_MEAN);
+      launch_mean(a, s->d_unc, (int)s->unc_segs.size(),
+                  std::max(1, std::min<int>((int)s->unc_segs.size(), s->sms * 4)), st);
+      L.end();
+    }
+    if (compressed_step) by_rp<RunCompressed>(s->RP, s, a, L, need_fresh, mask);
+  }
+  L.begin(K_COMMIT);
+  launch_commit(s->ctrl, compressed_step ? 1 : 0, s->d_status, st);
+  L.end();
+  PSGD_CUDA_TRY(cudaGetLastError());
+  PSGD_CUDA_TRY(cudaMemcpyAsync(s->h_status, s->d_status, sizeof(int), cudaMemcpyDeviceToHost, st));
+  return PSGD_OK;
+}
+
+void drop_graph(psgd_state* s) {
+  if (s->gexec) cudaGraphExecDestroy(s->gexec);
+  s->gexec = nullptr;
+  s->gkey_grads.clear();
+  s->gkey_out = nullptr;
+}
+
+// Replays the steady step's graph on `st`, capturing it first (on the
+// private stream s_cap, which executes nothing while capturing) when there is
+// none for these pointers and this scale.
+int step_graph(psgd_state* s, const StepArgs& a, const void* const* grads, const float* out, float scale,
+               cudaStream_t st) {
+  bool same = s->gexec && s->gkey_out == out && s->gkey_scale == scale && (int)s->gkey_grads.size() == s->W;
+  for (int w = 0; same && w < s->W; ++w) same = s->gkey_grads[w] == grads[w];
+  if (!same) {
+    drop_graph(s);
+    if (!s->s_cap) PSGD_CUDA_TRY(cudaStreamCreateWithFlags(&s->s_cap, cudaStreamNonBlocking));
+    PSGD_CUDA_TRY(cudaStreamBeginCapture(s->s_cap, cudaStreamCaptureModeThreadLocal));
+    const int rc = enqueue_step(s, a, s->s_cap, false, true, false, std::vector<int>(s->cdesc.size(), 0));
+    cudaGraph_t graph = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(s->s_cap, &graph);
+    if (rc < 0 || e != cudaSuccess || !graph) {
+      if (graph) cudaGraphDestroy(graph);
+      cudaGetLastError();
+      return rc < 0 ? rc : fail(PSGD_ECUDA, std::string("psgd_step: graph capture: ") + cudaGetErrorString(e));
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&s->gexec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) {
+      s->gexec = nullptr;
+      cudaGetLastError();
+      return fail(PSGD_ECUDA, std::string("psgd_step: graph instantiate: ") + cudaGetErrorString(ei));
+    }
+    s->gkey_grads.assign(grads, grads + s->W);
+    s->gkey_out = out;
+    s->gkey_scale = scale;
+    s->graph_captures++;
+  }
+  PSGD_CUDA_TRY(cudaGraphLaunch(s->gexec, st));
+  s->graph_replays++;
+  return PSGD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_loss_scale, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
   if (!grads || !out) return fail(PSGD_EINVAL, "grads/out is NULL");
@@ -844,43 +936,42 @@ int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_los
   int vec_ok = ((uintptr_t)out % 16 == 0);
   for (int w = 0; w < s->W; ++w) vec_ok &= ((uintptr_t)grads[w] % (s->dtype == PSGD_F32 ? 16 : 8) == 0);
   a.vec_ok = vec_ok;
-  Launcher L{s, st};
-  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, sizeof(int), st));
-  const int grid_seg = std::max(1, std::min<int>((int)s->all_segs.size(), s->sms * 4));
-  bool compressed_step = false;
-  if (s->iter < s->start_iter) {
-    // before start_powerSGD_iter calls the hook only averages the replicas
-    // ("PowerSGD State", start_powerSGD_iter)
-    L.begin(K_MEAN);
-    launch_mean(a, s->d_all, (int)s->all_segs.size(), grid_seg, st);
-    L.end();
+  const bool vanilla = s->iter < s->start_iter;
+  const bool compressed_step = !vanilla && !s->cdesc.empty();
+  const bool need_fresh = compressed_step && ((!s->warm) || s->compressed_launched == 0);
+  if (s->graph_mode && !s->prof && compressed_step && !need_fresh) {
+    // steady compressed step: the launch sequence no longer changes, and every
+    // decision left (skip, double-buffer half, warm or fresh Q) is taken on
+    // the device, so one captured graph replays it
+    int rc = step_graph(s, a, grads, out, inv_loss_scale, st);
+    if (rc < 0) return rc;
   } else {
-    if (!s->unc_segs.empty()) {
-      L.begin(K_MEAN);
-      launch_mean(a, s->d_unc, (int)s->unc_segs.size(),
-                  std::max(1, std::min<int>((int)s->unc_segs.size(), s->sms * 4)), st);
-      L.end();
-    }
-    if (!s->cdesc.empty()) {
-      compressed_step = true;
-      const bool need_fresh = (!s->warm) || s->compressed_launched == 0;
-      std::vector<int> mask(s->cdesc.size(), 0);
-      if (need_fresh) {
-        for (size_t c = 0; c < s->cdesc.size(); ++c) {
-          mask[c] = s->pending_draw[c] ? 0 : 1;
-          s->pending_draw[c] = 0;
-        }
+    std::vector<int> mask(s->cdesc.size(), 0);
+    if (need_fresh) {
+      for (size_t c = 0; c < s->cdesc.size(); ++c) {
+        mask[c] = s->pending_draw[c] ? 0 : 1;
+        s->pending_draw[c] = 0;
       }
-      by_rp<RunCompressed>(s->RP, s, a, L, need_fresh, mask);
-      s->compressed_launched++;
     }
+    int rc = enqueue_step(s, a, st, vanilla, compressed_step, need_fresh, mask);
+    if (rc < 0) return rc;
   }
-  L.begin(K_COMMIT);
-  launch_commit(s->ctrl, compressed_step ? 1 : 0, s->d_status, st);
-  L.end();
-  PSGD_CUDA_TRY(cudaGetLastError());
-  PSGD_CUDA_TRY(cudaMemcpyAsync(s->h_status, s->d_status, sizeof(int), cudaMemcpyDeviceToHost, st));
+  if (compressed_step) s->compressed_launched++;
   s->iter++;
+  return PSGD_OK;
+}
+
+int psgd_set_graph(psgd_state* s, int32_t enable) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  s->graph_mode = enable ? 1 : 0;
+  if (!enable) drop_graph(s);
+  return PSGD_OK;
+}
+
+int psgd_graph_stats(const psgd_state* s, int64_t* captures, int64_t* replays) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (captures) *captures = s->graph_captures;
+  if (replays) *replays = s->graph_replays;
   return PSGD_OK;
 }
 
@@ -960,6 +1051,16 @@ int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out
   s->host_calls++;
   return PSGD_OK;
 }
+
+// Bucket groups (psgd_group.cu): the first compressed-tensor number of a
+// bucket in the group's numbering, and the bucket's count of compressed tensors.
+int psgd_internal_set_tensor_base(psgd_state* s, int32_t base) {
+  if (!s || base < 0) return fail(PSGD_EINVAL, "tensor base");
+  s->tensor_base = base;
+  return PSGD_OK;
+}
+
+int psgd_internal_compressed_count(const psgd_state* s) { return s ? (int)s->cdesc.size() : 0; }
 
 int psgd_step_status(psgd_state* s, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");

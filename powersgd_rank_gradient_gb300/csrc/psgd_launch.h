@@ -23,6 +23,6 @@ template <int RP> void launch_pass3(const StepArgs& a, int mode, int grid, cudaS
 void launch_mean(const StepArgs& a, const Segment* segs, int nsegs, int grid, cudaStream_t s);
 void launch_commit(Ctrl* ctrl, int compressed, int* status, cudaStream_t s);
 void launch_randn(const StepArgs& a, const int* mask, unsigned long long seed,
-                  unsigned long long counter, int rp, int grid, cudaStream_t s);
+                  unsigned long long counter, int tbase, int rp, int grid, cudaStream_t s);
 
 }  // namespace psgd

@@ -125,11 +125,13 @@ __device__ __forceinline__ Philox4 philox4x32_10(Philox4 c, unsigned int k0, uns
 
 // Standard-normal draw of Q for the tensors whose mask is set ("PowerSGD
 // Hooks" step 3.1: Q is initialised from a standard normal distribution).
-// Element (j, k) of tensor t uses counter (j * RP + k, t, counter_lo,
-// counter_hi) and key = random_seed; Box-Muller on the first two words.
+// Element (j, k) of compressed tensor t uses counter (j * RP + k, T,
+// counter_lo, counter_hi) with T = tbase + t (tbase numbers a bucket's
+// tensors after those of the buckets before it in a group) and key =
+// random_seed; Box-Muller on the first two words.
 __global__ void __launch_bounds__(kThreads) k_randn(const StepArgs a, const int* __restrict__ mask,
                                                     unsigned long long seed, unsigned long long counter,
-                                                    int rp) {
+                                                    int tbase, int rp) {
   for (int it = blockIdx.x; it < a.n_gsq; it += gridDim.x) {
     const GsItem gi = a.gsq_items[it];
     if (!mask[gi.t]) continue;
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) k_randn(const StepArgs a, const int*
         Philox4 c;
         const unsigned long long e = (unsigned long long)j * rp + k;
         c.v[0] = (unsigned int)e;
-        c.v[1] = (unsigned int)(e >> 32) ^ ((unsigned int)gi.t << 8);
+        c.v[1] = (unsigned int)(e >> 32) ^ ((unsigned int)(tbase + gi.t) << 8);
         c.v[2] = (unsigned int)counter;
         c.v[3] = (unsigned int)(counter >> 32);
         const Philox4 o = philox4x32_10(c, (unsigned int)seed, (unsigned int)(seed >> 32));
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(kThreads) k_randn(const StepArgs a, const int*
 }
 
 void launch_randn(const StepArgs& a, const int* mask, unsigned long long seed,
-                  unsigned long long counter, int rp, int grid, cudaStream_t s) {
-  k_randn<<<grid, kThreads, 0, s>>>(a, mask, seed, counter, rp);
+                  unsigned long long counter, int tbase, int rp, int grid, cudaStream_t s) {
+  k_randn<<<grid, kThreads, 0, s>>>(a, mask, seed, counter, tbase, rp);
 }
 
 }  // namespace psgd

@@ -67,6 +67,9 @@ class PowerSGDState:
 
     # -- lifetime -------------------------------------------------------------
     def close(self):
+        if getattr(self, "_owner", None) is not None:
+            self._h = ctypes.c_void_p()   # a group's bucket: the group frees it
+            return
         if getattr(self, "_h", None) and self._h.value:
             self._lib.psgd_state_destroy(self._h)
             self._h = ctypes.c_void_p()
@@ -106,6 +109,16 @@ class PowerSGDState:
         """Synchronises and returns True when the last step was skipped (inf/NaN)."""
         rc = check(self._lib.psgd_step_status(self._h, _stream_ptr(stream)))
         return rc == PSGD_SKIPPED_NONFINITE
+
+    def set_graph(self, enable=True):
+        """psgd_set_graph: replay the steady compressed step as a CUDA graph."""
+        check(self._lib.psgd_set_graph(self._h, int(bool(enable))))
+
+    def graph_stats(self):
+        """(captures, replays) of the steady-step graph."""
+        c, r = ctypes.c_int64(), ctypes.c_int64()
+        check(self._lib.psgd_graph_stats(self._h, ctypes.byref(c), ctypes.byref(r)))
+        return c.value, r.value
 
     # -- introspection ----------------------------------------------------------
     def stats(self):
@@ -212,6 +225,103 @@ class BatchedPowerSGDState(PowerSGDState):
         self._h = handle
         self._lib = L
         self.side = self.tensor_info(0)["rows"]
+
+
+class PowerSGDGroup:
+    """Per-bucket PowerSGD states stepped on several CUDA streams ("DDP
+    Communication Hooks", "What Does a Communication Hook Operate On?": the
+    hook runs once per gradient bucket, and bucketing lets one bucket's work
+    overlap another's).  ``bucket_shapes[b]`` lists bucket b's tensor shapes;
+    the keyword arguments are PowerSGDState's and apply to every bucket.
+    ``graphs``: replay each bucket's steady step as a CUDA graph (the buckets'
+    buffers must then stay the same from step to step to avoid recaptures)."""
+
+    def __init__(self, bucket_shapes, world_size, matrix_approximation_rank=1, start_powerSGD_iter=1000,
+                 min_compression_rate=2, use_error_feedback=True, warm_start=True,
+                 orthogonalization_epsilon=0.0, random_seed=0, batch_tensors_with_same_shape=False,
+                 grad_dtype=torch.float32, n_streams=8, graphs=True, device=None):
+        if device is None:
+            device = torch.cuda.current_device()
+        device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        if grad_dtype not in (torch.float32, torch.float16, torch.bfloat16):
+            raise ValueError("grad_dtype must be torch.float32, torch.float16 or torch.bfloat16")
+        self.bucket_shapes = [[tuple(int(d) for d in sh) for sh in b] for b in bucket_shapes]
+        self.world_size = int(world_size)
+        self.grad_dtype = grad_dtype
+        self.device = device
+        self.n_streams = int(n_streams)
+        L = _lib.lib()
+        flat = [sh for b in self.bucket_shapes for sh in b]
+        d, n = _lib.shape_arrays(flat)
+        counts = (ctypes.c_int32 * max(1, len(self.bucket_shapes)))(*[len(b) for b in self.bucket_shapes])
+        handle = ctypes.c_void_p()
+        check(L.psgd_group_create(
+            len(self.bucket_shapes), counts, d, n, self.world_size, int(matrix_approximation_rank),
+            int(start_powerSGD_iter), float(min_compression_rate), int(bool(use_error_feedback)),
+            int(bool(warm_start)), float(orthogonalization_epsilon), int(random_seed) & (2**64 - 1),
+            int(bool(batch_tensors_with_same_shape)),
+            {torch.float16: PSGD_F16, torch.bfloat16: PSGD_BF16}.get(grad_dtype, PSGD_F32),
+            self.n_streams, device.index or 0, ctypes.byref(handle)))
+        self._h = handle
+        self._lib = L
+        self.buckets = [self._bucket_view(b) for b in range(len(self.bucket_shapes))]
+        # the steady step of every bucket as one CUDA graph launch (psgd_set_graph)
+        for v in self.buckets:
+            v.set_graph(graphs)
+
+    def _bucket_view(self, b):
+        h = ctypes.c_void_p()
+        check(self._lib.psgd_group_bucket(self._h, b, ctypes.byref(h)))
+        v = PowerSGDState.__new__(PowerSGDState)
+        v._h, v._lib, v._owner = h, self._lib, self
+        v.shapes = self.bucket_shapes[b]
+        v.world_size = self.world_size
+        v.grad_dtype = self.grad_dtype
+        v.device = self.device
+        v.numel = sum(_numel(sh) for sh in v.shapes)
+        return v
+
+    def __len__(self):
+        return len(self.bucket_shapes)
+
+    def step(self, bucket, grads, out=None, inv_loss_scale=1.0, stream=None):
+        """Enqueue bucket ``bucket``'s hook call; returns ``out`` (valid after wait())."""
+        v = self.buckets[bucket]
+        if len(grads) != self.world_size:
+            raise ValueError(f"expected {self.world_size} replica buckets, got {len(grads)}")
+        for g in grads:
+            if not (g.is_cuda and g.dtype == self.grad_dtype and g.is_contiguous() and g.numel() == v.numel):
+                raise ValueError(f"bucket {bucket}: each replica bucket must be a contiguous CUDA tensor of "
+                                 f"{v.numel} {self.grad_dtype} elements")
+        if out is None:
+            out = torch.empty(v.numel, dtype=torch.float32, device=self.device)
+        if not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous() and out.numel() == v.numel):
+            raise ValueError("out must be a contiguous CUDA float32 tensor of the bucket's size")
+        ptrs = (ctypes.c_void_p * self.world_size)(*[g.data_ptr() for g in grads])
+        check(self._lib.psgd_group_step(self._h, int(bucket), ptrs, ctypes.c_void_p(out.data_ptr()),
+                                        float(inv_loss_scale), _stream_ptr(stream)))
+        return out
+
+    def wait(self, stream=None):
+        """Make ``stream`` (default: the current stream) wait for every enqueued bucket step."""
+        check(self._lib.psgd_group_wait(self._h, _stream_ptr(stream)))
+
+    def status(self, stream=None):
+        """Synchronises; True when any bucket's last step was skipped (inf/NaN)."""
+        return check(self._lib.psgd_group_status(self._h, _stream_ptr(stream))) == PSGD_SKIPPED_NONFINITE
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            for v in getattr(self, "buckets", []):
+                v._h = ctypes.c_void_p()
+            self._lib.psgd_group_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def batched_powerSGD_hook(state, grads, out=None, inv_loss_scale=1.0, stream=None):

@@ -86,3 +86,28 @@ def test_null_state_calls_fail_cleanly():
     assert L.psgd_error_numel(None) == 0
     assert L.psgd_workspace_bytes(None) == 0
     L.psgd_state_destroy(None)
+
+
+def test_group_rejects_bad_arguments():
+    """Bucket-group argument checks run before any CUDA call."""
+    L = _lib.lib()
+    d, n = _lib.shape_arrays([(4, 4)])
+    counts = (ctypes.c_int32 * 1)(1)
+    out = ctypes.c_void_p()
+
+    def create(nb, cnt, n_streams):
+        return L.psgd_group_create(nb, cnt, d, n, 1, 1, 0, 2.0, 1, 1, 0.0, 0, 0, _lib.PSGD_F32, n_streams, 0,
+                                   ctypes.byref(out))
+
+    assert create(0, counts, 4) == _lib.PSGD_EINVAL
+    assert create(1, None, 4) == _lib.PSGD_EINVAL
+    assert create(1, counts, 0) == _lib.PSGD_EINVAL
+    assert create(1, counts, _lib.PSGD_MAX_GROUP_STREAMS + 1) == _lib.PSGD_EINVAL
+    assert b"n_streams" in L.psgd_last_error()
+    assert create(1, (ctypes.c_int32 * 1)(-1), 4) == _lib.PSGD_EINVAL
+    assert not out.value
+    assert L.psgd_group_step(None, 0, None, None, 1.0, None) == _lib.PSGD_EINVAL
+    assert L.psgd_group_wait(None, None) == _lib.PSGD_EINVAL
+    assert L.psgd_group_bucket(None, 0, ctypes.byref(out)) == _lib.PSGD_EINVAL
+    assert L.psgd_group_size(None) == 0
+    L.psgd_group_destroy(None)

@@ -397,3 +397,42 @@ def test_bf16_buckets(world, ef):
                         po = st.tensor_info(p.index)["packed_offset"]
                         assert rel(e[po:po + p.numel], ref.error_of(w, p.index).reshape(-1)) <= 1e-4
     st.close()
+
+
+def test_graph_replay_bit_identical():
+    """psgd_set_graph: the steady step replayed as a CUDA graph gives the same
+    bits as the launch-by-launch path, through a skipped step (inf) and a
+    change of output buffer (a second capture)."""
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = MIXED
+    mk = lambda: PowerSGDState(shapes, 2, matrix_approximation_rank=4, start_powerSGD_iter=1,
+                               min_compression_rate=1.0, random_seed=5, device=DEV)
+    plain, graphed = mk(), mk()
+    graphed.set_graph(True)
+    n = plain.numel
+    outs = [torch.empty(n, device=DEV), torch.empty(n, device=DEV)]
+    hosts = [grads_for(shapes, 2, k) for k in range(6)]
+    hosts[3] = [x.copy() for x in hosts[3]]
+    hosts[3][1][7] = np.inf
+    dev_sets = [[torch.empty(n, device=DEV) for _ in range(2)] for _ in range(2)]
+    for step in range(6):
+        ds = dev_sets[0]
+        for w in range(2):
+            ds[w].copy_(torch.from_numpy(hosts[step][w]))
+        o = outs[1] if step == 4 else outs[0]
+        a = plain.step(ds, out=o).clone()
+        sa = plain.status()
+        b = graphed.step(ds, out=o).clone()
+        sb = graphed.status()
+        assert sa == sb == (step == 3), step
+        if step != 3:
+            assert torch.equal(a, b), step
+        for w in range(2):
+            assert torch.equal(plain.get_error(w), graphed.get_error(w)), (step, w)
+    # step 0 is vanilla and step 1 draws Q (no graph); step 2 captures and
+    # replays, step 3 replays (skipped on the device), steps 4 and 5 change
+    # the output buffer and so capture again
+    assert graphed.graph_stats() == (3, 4), graphed.graph_stats()
+    plain.close()
+    graphed.close()
