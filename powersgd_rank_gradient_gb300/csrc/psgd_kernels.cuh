@@ -779,13 +779,16 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       if (a.ef) load_qcols<RP, 4, !SH>(Qc + td.q_off, m, c, qc, ncv);
       if (!(a.ef && same_q)) load_qcols<RP, 4, !SH>(Qp + td.q_off, m, c, qp, ncv);
     }
-    auto issue = [&](int u) {
-      char* slot = wsm + (u % S) * St::UNIT_BYTES;
-      const long long row = item.row0 + phase + (long long)u * wpc;
-      const long long eo = (long long)cur * a.W * a.nc_pad + td.c_off + row * ld + c;
+    // units are issued and consumed in order, wpc rows apart, the issued one
+    // S - 1 units ahead of the consumed one: running offsets of the consumed
+    // unit (bucket position, store offset) and rotating stage slots replace
+    // per-row products.  go / eo: bucket and store offsets of the unit issued.
+    const long long gstep = (long long)wpc * m, estep = (long long)wpc * ld;
+    const long long row_first = (long long)item.row0 + phase;
+    const long long ecur = (long long)cur * a.W * a.nc_pad;
+    auto issue = [&](char* slot, long long go, long long eo) {
       if constexpr (!SH) {
         if (cin) {
-          const long long go = td.g_off + row * m + c;
 #pragma unroll
           for (int w = 0; w < WT; ++w) {
             const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
@@ -796,7 +799,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         }
       } else {
         // aligned chunk (element offset in the bucket) holding this lane's first column
-        const long long gp = td.g_off + row * m + c;
+        const long long gp = go;
         const int rg = (int)(gp & 3);
         const bool gneed = c - rg < cend;
         const bool gx = lane == 31 && rg > 0 && c + 4 - rg < cend;
@@ -821,39 +824,54 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
     };
 #pragma unroll
     for (int u = 0; u < S - 1; ++u) {
-      if (u < units) issue(u); else cp_async_commit();
+      const long long r = row_first + (long long)u * wpc;
+      if (u < units) issue(wsm + u * St::UNIT_BYTES, td.g_off + r * m + c, ecur + td.c_off + r * ld + c);
+      else cp_async_commit();
     }
     // the committed P row of the next unit is loaded one unit ahead
+    const float* p_next = Pc + td.p_off + row_first * RP;
     float pn[RP];
 #pragma unroll
     for (int k = 0; k < RP; ++k) pn[k] = 0.f;
-    if (a.ef && units > 0) load_row<RP>(Pc + td.p_off + (item.row0 + phase) * (long long)RP, pn);
+    if (a.ef && units > 0) load_row<RP>(p_next, pn);
+    p_next += wpc * RP;
+    long long r_off = td.c_off + row_first * ld + c;   // store / mbar offset of the unit
+    long long g_pos = row_first * m + c;               // its position in the tensor's view
+    const long long g_ahead = td.g_off + (S - 1) * gstep, e_ahead = ecur + (S - 1) * estep;
+    int s_use = 0;
     for (int u = 0; u < units; ++u) {
       cp_async_wait<S - 2>();
       if constexpr (SH) __syncwarp();   // lanes read their neighbour's chunk
-      if (u + S - 1 < units) issue(u + S - 1); else cp_async_commit();
+      // unit u + S - 1 goes to the slot unit u - 1 used
+      if (u + S - 1 < units)
+        issue(wsm + (s_use == 0 ? S - 1 : s_use - 1) * St::UNIT_BYTES, g_pos + g_ahead, r_off + e_ahead);
+      else
+        cp_async_commit();
       const int rr = phase + u * wpc;
-      const long long i = item.row0 + rr;
+      const char* slot = wsm + s_use * St::UNIT_BYTES;
+      s_use = (s_use + 1 == S) ? 0 : s_use + 1;
       float po[RP];
 #pragma unroll
       for (int k = 0; k < RP; ++k) po[k] = pn[k];
-      if (a.ef && u + 1 < units) load_row<RP>(Pc + td.p_off + (i + wpc) * RP, pn);
+      if (a.ef && u + 1 < units) {
+        load_row<RP>(p_next, pn);
+        p_next += wpc * RP;
+      }
       float pacc[RP];
 #pragma unroll
       for (int k = 0; k < RP; ++k) pacc[k] = 0.f;
       if (cin) {
-        const char* slot = wsm + (u % S) * St::UNIT_BYTES;
         float corr[4] = {0.f, 0.f, 0.f, 0.f};
         if (a.ef) {
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) corr[cc] = dot_chain<RP>(po, qc[cc]);
         }
         float mb[4] = {0.f, 0.f, 0.f, 0.f};
-        float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + td.c_off + i * ld + c;
+        float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + r_off;
         // SH: columns taken from the bucket (the tile's and the bucket's ends)
-        const long long lim = SH ? td.valid - (i * m + c) : 4;
+        const long long lim = SH ? td.valid - g_pos : 4;
         const int nvg = lim >= ncv ? ncv : (lim > 0 ? (int)lim : 0);
-        const int rg = SH ? (int)((td.g_off + i * m + c) & 3) : 0;
+        const int rg = SH ? (int)((td.g_off + g_pos) & 3) : 0;
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
           float gv[4];
@@ -905,7 +923,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) mb[cc] *= a.invW;
-        if (a.mbar) store_f<4>(a.mbar + td.c_off + i * ld + c, mb);
+        if (a.mbar) store_f<4>(a.mbar + r_off, mb);
         const float (*qq)[RP] = (a.ef && same_q) ? qc : qp;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -916,6 +934,8 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       chk = fmaf(tot, 0.f, chk);   // inf/NaN in the row's inputs reach the sums
       constexpr int SHF = 5 - log2_rp<RP>();
       if ((lane & ((1 << SHF) - 1)) == 0) red[(rr * NCH + ch) * RP + (lane >> SHF)] = tot;
+      r_off += estep;
+      g_pos += gstep;
     }
     cp_async_wait<0>();
   }
