@@ -1038,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads) k_pass1(const StepArgs a) {
 // operation is a column operation, so the result is X T for an RP x RP upper
 // triangular T that depends only on the Gram matrix G = X^T X.  The stage
 // therefore (1) reduces G over row blocks in fp64 (k_gram), (2) runs modified
-// Gram-Schmidt with epsilon symbolically on G to get T (k_solve, one warp per
+// Gram-Schmidt with epsilon symbolically on G to get T (k_solve, one CTA per
 // tensor, fp64), (3) applies X T (k_apply).  It runs twice (the second sweep
 // re-orthogonalises the first sweep's output), which keeps P^T P = I to fp32
 // rounding even when X is ill conditioned.
@@ -1154,19 +1154,28 @@ __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float
 
 // One CTA per tensor: the whole CTA adds up the item Gram matrices (each
 // entry split over SPLIT threads, four accumulators each, then combined in a
-// fixed order), then warp 0 runs modified Gram-Schmidt with epsilon on the
-// coefficient matrix T (X_out = X T), with G and T in shared memory.  Step i:
-// g = G t_i, ||x_i||^2 = t_i . g, scale column i by 1 / (||x_i|| + eps), then
-// every later column j (lane j) loses its projection (t_i^T G t_j) t_i.
-// fp64 throughout; the dot products keep four independent chains.
+// fixed order), then runs modified Gram-Schmidt with epsilon on the
+// coefficient matrix T (X_out = X T), in fp64 with T and H = G T in shared
+// memory.  Step i, with t_i still unscaled: ||x_i||^2 = t_i . h_i, sc_i =
+// 1 / (||x_i|| + eps); every later column j loses its projection on the
+// normalised x_i: t_j -= c t_i and h_j -= c h_i with c = sc_i^2 (t_i . h_j).
+// The column scalings are applied to T at the end (t_i is not read again
+// after its own step).  Thread (j, p) of the TEAM owns rows [p R, p R + R)
+// of column j; the PARTS threads of a column add their partial dot products
+// with shuffles.  Ranks up to 8 fit one warp (steps end with __syncwarp),
+// larger ones use the whole CTA (__syncthreads).
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const double* __restrict__ gram_in,
                                                     int is_q, int only_init) {
   constexpr int ENT = RP * RP;
   constexpr int SPLIT = ENT >= kThreads ? 1 : kThreads / ENT;
-  __shared__ double G[ENT];
-  __shared__ double T[ENT];   // T[k * RP + j] = row k of column j
-  __shared__ double gv[RP];
+  constexpr int TEAM = ENT <= 64 ? 32 : kThreads;
+  constexpr int R = ENT > TEAM ? ENT / TEAM : 1;            // rows per thread
+  constexpr int PARTS = RP / R;                             // threads per column
+  constexpr int LD = RP + 1;                                // padded column stride
+  __shared__ double H[RP * LD];   // H[j * LD + k] = row k of column j of G T
+  __shared__ double T[RP * LD];   // T[j * LD + k] = row k of column j
+  __shared__ double scal[RP];
   __shared__ double part[kThreads];
   const int t = blockIdx.x;
   if (a.ctrl->flag) return;
@@ -1193,33 +1202,21 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const doub
     if (sp == 0 && idx < ENT) {
       double v = 0.0;
       for (int q = 0; q < SPLIT; ++q) v += part[threadIdx.x + q];
-      G[idx] = v;
-      const int k = idx / RP, j = idx % RP;
-      T[idx] = (k == j && j < td.r) ? 1.0 : 0.0;
+      const int k = idx / RP, j = idx % RP;   // G is symmetric: entry (k, j)
+      H[j * LD + k] = v;
+      T[j * LD + k] = (k == j && j < td.r) ? 1.0 : 0.0;
     }
     __syncthreads();
   }
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
+  if (threadIdx.x >= TEAM) return;
   const int r = td.r;
   const double eps = (double)a.eps;
+  const int lane = threadIdx.x & 31;
+  const int j = threadIdx.x / PARTS, p = threadIdx.x % PARTS;
+  const bool own = j < RP;
   for (int i = 0; i < r; ++i) {
-    if (lane < r) {
-      double c0 = 0.0, c1 = 0.0, c2 = 0.0, c3 = 0.0;
-      int l = 0;
-      // G is symmetric: row `lane` is read as column `lane`, contiguous across
-      // the warp (no shared-memory bank conflicts)
-      for (; l + 4 <= r; l += 4) {
-        c0 += G[l * RP + lane] * T[l * RP + i];
-        c1 += G[(l + 1) * RP + lane] * T[(l + 1) * RP + i];
-        c2 += G[(l + 2) * RP + lane] * T[(l + 2) * RP + i];
-        c3 += G[(l + 3) * RP + lane] * T[(l + 3) * RP + i];
-      }
-      for (; l < r; ++l) c0 += G[l * RP + lane] * T[l * RP + i];
-      gv[lane] = (c0 + c1) + (c2 + c3);
-    }
-    __syncwarp();
-    double nn = (lane < r) ? T[lane * RP + i] * gv[lane] : 0.0;
+    // ||x_i||^2 = t_i . h_i, by every warp (t_i has no entries below row i)
+    double nn = (lane <= i) ? T[i * LD + lane] * H[i * LD + lane] : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nn += __shfl_xor_sync(0xffffffffu, nn, o);
     // sc = 1 / (sqrt(nn) + eps).  For eps = 0 and nn > 0 it is 1 / sqrt(nn):
@@ -1236,29 +1233,33 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const doub
     } else {
       sc = 1.0 / (sqrt(fmax(nn, 0.0)) + eps);
     }
-    __syncwarp();
-    if (lane < r) {
-      T[lane * RP + i] *= sc;
-      gv[lane] *= sc;
-    }
-    __syncwarp();
-    if (lane > i && lane < r) {
-      double d0 = 0.0, d1 = 0.0, d2 = 0.0, d3 = 0.0;
-      int k = 0;
-      for (; k + 4 <= r; k += 4) {
-        d0 += gv[k] * T[k * RP + lane];
-        d1 += gv[k + 1] * T[(k + 1) * RP + lane];
-        d2 += gv[k + 2] * T[(k + 2) * RP + lane];
-        d3 += gv[k + 3] * T[(k + 3) * RP + lane];
+    if (threadIdx.x == 0) scal[i] = sc;
+    double d = 0.0;
+    if (own && j > i && j < r) {
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int k = p * R + q;
+        d += T[i * LD + k] * H[j * LD + k];
       }
-      for (; k < r; ++k) d0 += gv[k] * T[k * RP + lane];
-      const double d = (d0 + d1) + (d2 + d3);
-      for (k = 0; k < r; ++k) T[k * RP + lane] -= d * T[k * RP + i];
     }
-    __syncwarp();
+#pragma unroll
+    for (int o = PARTS / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if (own && j > i && j < r) {
+      const double c = d * sc * sc;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int k = p * R + q;
+        T[j * LD + k] -= c * T[i * LD + k];
+        H[j * LD + k] -= c * H[i * LD + k];
+      }
+    }
+    if constexpr (TEAM == 32) __syncwarp(); else __syncthreads();
   }
   float* Tout = a.tmat + (long long)t * RP * RP;
-  for (int idx = lane; idx < ENT; idx += 32) Tout[idx] = (float)T[idx];
+  for (int idx = threadIdx.x; idx < ENT; idx += TEAM) {
+    const int k = idx / RP, jj = idx % RP;
+    Tout[idx] = (float)(jj < r ? T[jj * LD + k] * scal[jj] : 0.0);
+  }
 }
 
 // dst rows = src rows x T (thread per row).
