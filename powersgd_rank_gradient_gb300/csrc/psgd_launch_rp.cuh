@@ -2,6 +2,7 @@
 // kern_rp<RP>.cu, which instantiates them.
 #pragma once
 
+#include "psgd_gs.cuh"
 #include "psgd_kernels.cuh"
 #include "psgd_launch.h"
 
