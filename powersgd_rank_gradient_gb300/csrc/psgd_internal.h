@@ -31,6 +31,11 @@ constexpr int kGsRows = 256;       // rows per work item of the Gram-Schmidt ker
 // a padded rank RP: the per-thread accumulators hold CPT x RP floats.
 __host__ __device__ constexpr int cpt_for(int rp) { return rp <= 8 ? 4 : (rp == 16 ? 2 : 1); }
 __host__ __device__ constexpr int ctile_for(int rp) { return kThreads * cpt_for(rp); }
+// Pass 3 (and the error views) keeps CPT3 columns of Q in registers per
+// thread: more columns than pass 2 at ranks 16 and 32 give its dot-product
+// chains more independent work per staged P value.
+__host__ __device__ constexpr int cpt3_for(int rp) { return rp <= 16 ? 4 : 2; }
+__host__ __device__ constexpr int ctile3_for(int rp) { return kThreads * cpt3_for(rp); }
 // Column tile of pass 1: 1024 columns (eight 128-column chunks, one per warp)
 // for ranks up to 8; for larger ranks the tile's slice of Q (ctile1 x RP
 // floats) stays at 32 KB so that it stays in L1 next to the stages.

@@ -1215,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Pass 3: out = P Q'^T.  Each thread keeps its CPT columns of Q' in registers.
+// Pass 3: out = P Q'^T.  Each thread keeps its CPT3 columns of Q' in registers.
 // MODE 0: write out (bucket layout).  MODE 1: materialise replica `a.replica`'s
 // residual store - P Q^T of the committed half into a.eio.  MODE 2: set the
 // store from a.eio + P Q^T.  MODE 3: fold the factors into the store in place
@@ -1227,7 +1227,7 @@ template <int RP, int MODE, int NC, bool SHF = false, bool BND = true>
 __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& td, const Item& item,
                                            const float* __restrict__ P, const float* __restrict__ Q,
                                            float (*ps)[RP], float* __restrict__ store) {
-  constexpr int CPT = cpt_for(RP);
+  constexpr int CPT = cpt3_for(RP);
   static_assert(!SHF || (MODE == 0 && CPT == 4 && NC == 1), "shifted stores: out, 4 columns a thread");
   const long long m = td.m, ld = td.ld;
   const int c0 = item.col0 + threadIdx.x * CPT;
@@ -1324,7 +1324,7 @@ __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
   const float* Q = a.Qf + (long long)half * a.q_total;
   float* store = nullptr;
   if (MODE != 0) store = a.estore + ((long long)a.ctrl->cur * a.W + a.replica) * a.nc_pad;
-  constexpr int CPT = cpt_for(RP);
+  constexpr int CPT = cpt3_for(RP);
   for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
     const Item item = a.fitems[it];
     const TensorDesc td = a.tensors[item.t];
