@@ -29,7 +29,7 @@ What it computes, and where each step comes from:
   step that sees one is skipped and leaves the parameters (here: the hook's
   state) untouched.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 epsilon is added to the column NORM in the denominator; "allreduce" is the mean
 over the W simulated replicas; each replica computes its own P = M_w Q and the
 P's are then averaged (no linearity shortcut here); the initial Q is a standard
