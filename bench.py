@@ -49,12 +49,13 @@ def parse():
     ap.add_argument("--rank", type=int, default=None, help="rank of the rank-sweep workload")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling cases: only this many transformer layers, no embeddings")
-    ap.add_argument("--batched", action="store_true",
-                    help="also time batched_powerSGD_hook on the workload's bucket (one padded square)")
-    ap.add_argument("--buckets", type=float, default=0.0,
+    ap.add_argument("--batched", dest="batched", action="store_true", default=True,
+                    help="also time batched_powerSGD_hook on the workload's bucket (one padded square; default)")
+    ap.add_argument("--no-batched", dest="batched", action="store_false")
+    ap.add_argument("--buckets", type=float, default=25.0,
                     help="also time the workload split into DDP-style buckets of at most this many MB "
                          "(tensors in reverse order), stepped on one stream, on --bucket-streams, and on "
-                         "--bucket-streams with CUDA-graph replay")
+                         "--bucket-streams with CUDA-graph replay (default 25, DDP's bucket_cap_mb; 0: off)")
     ap.add_argument("--bucket-streams", type=int, default=16,
                     help="streams of the overlapped bucket-group runs (--buckets)")
     ap.add_argument("--no-e2e", action="store_true")
