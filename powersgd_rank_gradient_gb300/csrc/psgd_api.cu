@@ -396,7 +396,7 @@ void build_plan(psgd_state* s) {
   };
   make_items(&s->items, s->row_block, CT, false);
   make_items(&s->fitems, kFineRows3, ctile3_for(RP), true);
-  make_items(&s->p1items, kFineRows, CT1, true);
+  make_items(&s->p1items, rows1_for(RP), CT1, true);
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const long long len = (long long)s->cdesc[c].m * RP;
     for (long long f = 0; f < len; f += 1024)

@@ -413,12 +413,9 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
 }
 
 // ---------------------------------------------------------------------------
-// Pass 1, staged: the same arithmetic as pass1_tile, but each lane copies the
-// 16 bytes it will consume of every source row segment into its own slot of
-// shared memory with cp.async, S units ahead ("unit" = RW rows x 128 columns).
-// Bytes in flight then cost shared memory instead of registers, so a warp
-// keeps (S - 1) units of HBM traffic outstanding.  Warps are independent: no
-// CTA barrier, each warp owns rows warp*RW + g*8*RW of the item.
+// cp.async staging: a lane copies the bytes it will consume of a source row
+// segment into its own slot of shared memory, several units ahead, so bytes
+// in flight cost shared memory instead of registers.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -436,253 +433,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int RP, int WT, typename GT, int RW, int MINB>
-struct Pass1Stage {
-  static constexpr int GB = 4 * (int)sizeof(GT);                 // gradient bytes per lane per unit row
-  static constexpr int GSEG = 32 * GB;                            // one gradient row segment (warp)
-  static constexpr int ESEG = 32 * 16;                            // one store row segment (warp)
-  static constexpr int UNIT_BYTES = RW * WT * (GSEG + ESEG);      // per warp per unit
-  // Shared-memory budget per CTA: 192 KB with one CTA per SM, 96 KB with two,
-  // 56 KB with three, so that the carve-out leaves L1 room for the CTAs' Q
-  // tiles next to the stages.
-  // Ranks >= 16 also keep the item's Q tiles (projection and correction,
-  // ctile1 x RP floats each) in shared memory.
-  static constexpr int QTILE = RP >= 16 ? ctile1_for(RP) * RP * 4 : 0;
-  static constexpr int BUDGET = (MINB == 1 ? 192 * 1024 : (MINB == 2 ? 96 * 1024 : (MINB == 3 ? 56 * 1024 : 40 * 1024))) - 2 * QTILE;
-  static constexpr int S_RAW = BUDGET / (8 * UNIT_BYTES);
-  static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
-  static constexpr int SMEM = 8 * S * UNIT_BYTES + 2 * QTILE;     // per CTA
-};
-
-template <int RP, int WT, typename GT, int RW, int MINB>
-__device__ __forceinline__ void pass1_tile_staged(const StepArgs& a, const TensorDesc& td, const Item& item,
-                                                  const float* __restrict__ Qp, const float* __restrict__ Qc,
-                                                  const float* __restrict__ Pc, int cur, float& chk,
-                                                  char* __restrict__ wsm, float* __restrict__ qtile) {
-  using St = Pass1Stage<RP, WT, GT, RW, MINB>;
-  constexpr int S = St::S;
-  constexpr int GB = St::GB;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nxt = cur ^ 1;
-  const long long m = td.m;
-  const int cend = item.col0 + item.ncols;
-  const int nchunks = (item.ncols + 127) / 128;
-  const int first = warp * RW;
-  const int ngroups = first < item.nrows ? (item.nrows - first + 8 * RW - 1) / (8 * RW) : 0;
-  const int units = ngroups * nchunks;
-  const bool same_q = (Qp == Qc);
-  const bool unit_scale = (a.scale == 1.0f);
-  constexpr int CT1 = ctile1_for(RP);
-  // ranks >= 16: the item's Q tiles, k-major [k][column - col0], in shared
-  // memory (qtile: correction Q, then projection Q)
-  float* qts_c = qtile;
-  float* qts_p = qtile + CT1 * RP;
-  if constexpr (RP >= 16) {
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < RP * (CT1 / 4); idx += kThreads) {
-      const int k = idx / (CT1 / 4), c4 = (idx - k * (CT1 / 4)) * 4;
-      if (c4 < item.ncols) {
-        const long long src = td.q_off + (long long)k * m + item.col0 + c4;
-        if (a.ef) *reinterpret_cast<float4*>(qts_c + k * CT1 + c4) = __ldg(reinterpret_cast<const float4*>(Qc + src));
-        if (!(a.ef && same_q))
-          *reinterpret_cast<float4*>(qts_p + k * CT1 + c4) = __ldg(reinterpret_cast<const float4*>(Qp + src));
-      }
-    }
-    __syncthreads();
-  }
-  // slot layout: [q][w] gradient segments, then [q][w] store segments; inside
-  // a segment lane l owns bytes [l * width, (l + 1) * width), so a warp's
-  // accesses to one segment are contiguous and free of bank conflicts.
-
-  // unit u = (row group g, chunk ch); the issuer runs S - 1 units ahead of
-  // the consumer, each with its own counters.  The issuer keeps the row start
-  // of every source (element offsets) and adds the chunk's column.
-  int ig = 0, ich = 0, islot = 0;
-  long long grow[RW], erow[RW];
-  auto issue = [&]() {
-    const int rr = first + ig * 8 * RW;
-    if (ich == 0) {
-#pragma unroll
-      for (int q = 0; q < RW; ++q) {
-        const long long row = item.row0 + rr + q;
-        grow[q] = td.g_off + row * m;
-        erow[q] = (long long)cur * a.W * a.nc_pad + td.c_off + row * td.ld;
-      }
-    }
-    const int c = item.col0 + ich * 128 + lane * 4;
-    char* slot = wsm + islot * St::UNIT_BYTES;
-    const bool cin = c < cend;
-    if (++ich == nchunks) { ich = 0; ++ig; }
-    if (++islot == S) islot = 0;
-#pragma unroll
-    for (int q = 0; q < RW; ++q) {
-      if (rr + q >= item.nrows || !cin) continue;
-#pragma unroll
-      for (int w = 0; w < WT; ++w) {
-        const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + grow[q] + c;
-        char* gdst = slot + (q * WT + w) * St::GSEG + lane * GB;
-        if constexpr (GB == 16) cp_async16(gdst, gsrc); else cp_async8(gdst, gsrc);
-        if (a.ef) {
-          const float* esrc = a.estore + erow[q] + (long long)w * a.nc_pad + c;
-          cp_async16(slot + RW * WT * St::GSEG + (q * WT + w) * St::ESEG + lane * 16, esrc);
-        }
-      }
-    }
-    cp_async_commit();
-  };
-
-#pragma unroll
-  for (int u = 0; u < S - 1; ++u) {
-    if (u < units) issue(); else cp_async_commit();
-  }
-  float po[RW][RP];
-  float pacc[RW][RP];
-  int g = 0, ch = 0, cslot = 0;
-  for (int u = 0; u < units; ++u) {
-    cp_async_wait<S - 2>();
-    if (u + S - 1 < units) issue(); else cp_async_commit();
-    const int rr = first + g * 8 * RW;
-    const int c = item.col0 + ch * 128 + lane * 4;
-    bool rv[RW];
-#pragma unroll
-    for (int q = 0; q < RW; ++q) rv[q] = (rr + q) < item.nrows;
-    if (ch == 0) {
-#pragma unroll
-      for (int q = 0; q < RW; ++q) {
-        const int i = item.row0 + (rv[q] ? rr + q : rr);
-#pragma unroll
-        for (int k = 0; k < RP; ++k) { pacc[q][k] = 0.f; po[q][k] = 0.f; }
-        if (a.ef) load_row<RP>(Pc + td.p_off + (long long)i * RP, po[q]);
-      }
-    }
-    if (c < cend) {
-      const char* slot = wsm + cslot * St::UNIT_BYTES;
-      // Q columns c .. c+3: as one 4 x RP block for small RP, one column at a
-      // time (RP registers) for RP >= 16.
-      constexpr int QB = RP <= 8 ? 4 : 1;
-      float qv[QB][RP];
-      float corr[RW][4];
-      if (a.ef) {
-        if constexpr (QB == 4) {
-          load_qcols<RP, 4>(Qc + td.q_off, m, c, qv);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int q = 0; q < RW; ++q) corr[q][cc] = dot_chain<RP>(po[q], qv[cc]);
-        } else {
-          // one 16-byte shared-memory read per k; each correction is the
-          // increasing-k FMA chain of dot_chain (bit-identical to pass 3)
-          const float* qt = qts_c + (c - item.col0);
-#pragma unroll
-          for (int q = 0; q < RW; ++q)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) corr[q][cc] = 0.f;
-#pragma unroll
-          for (int k = 0; k < RP; ++k) {
-            const float4 x = *reinterpret_cast<const float4*>(qt + k * CT1);
-#pragma unroll
-            for (int q = 0; q < RW; ++q) {
-              corr[q][0] = fmaf(po[q][k], x.x, corr[q][0]);
-              corr[q][1] = fmaf(po[q][k], x.y, corr[q][1]);
-              corr[q][2] = fmaf(po[q][k], x.z, corr[q][2]);
-              corr[q][3] = fmaf(po[q][k], x.w, corr[q][3]);
-            }
-          }
-        }
-      }
-      float mb[RW][4];
-#pragma unroll
-      for (int q = 0; q < RW; ++q)
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) mb[q][cc] = 0.f;
-#pragma unroll
-      for (int w = 0; w < WT; ++w) {
-        float* enxt = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off;
-#pragma unroll
-        for (int q = 0; q < RW; ++q) {
-          if (!rv[q]) continue;
-          const long long i = item.row0 + rr + q;
-          float gv[4];
-          if constexpr (GB == 16) {
-            const float4 x = *reinterpret_cast<const float4*>(slot + (q * WT + w) * St::GSEG + lane * GB);
-            gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
-          } else {
-            cvt4<GT>(*reinterpret_cast<const uint2*>(slot + (q * WT + w) * St::GSEG + lane * GB), gv);
-          }
-          float ev[4] = {0.f, 0.f, 0.f, 0.f};
-          if (a.ef) {
-            const float4 x = *reinterpret_cast<const float4*>(slot + RW * WT * St::GSEG + (q * WT + w) * St::ESEG + lane * 16);
-            ev[0] = x.x; ev[1] = x.y; ev[2] = x.z; ev[3] = x.w;
-          }
-          float mv[4];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const float v = unit_scale ? gv[cc] : gv[cc] * a.scale;
-            mv[cc] = a.ef ? v + (ev[cc] - corr[q][cc]) : v;
-            mb[q][cc] += mv[cc];
-          }
-          if (a.ef) store_f<4>(enxt + i * td.ld + c, mv);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < RW; ++q) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) mb[q][cc] *= a.invW;
-        if (a.mbar && rv[q]) store_f<4>(a.mbar + td.c_off + (long long)(item.row0 + rr + q) * td.ld + c, mb[q]);
-      }
-      if constexpr (QB == 4) {
-        if (!(a.ef && same_q)) load_qcols<RP, 4>(Qp + td.q_off, m, c, qv);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int q = 0; q < RW; ++q)
-#pragma unroll
-            for (int k = 0; k < RP; ++k) pacc[q][k] = fmaf(mb[q][cc], qv[cc][k], pacc[q][k]);
-      } else {
-        const float* qt = ((a.ef && same_q) ? qts_c : qts_p) + (c - item.col0);
-#pragma unroll
-        for (int k = 0; k < RP; ++k) {
-          const float4 x = *reinterpret_cast<const float4*>(qt + k * CT1);
-#pragma unroll
-          for (int q = 0; q < RW; ++q) {
-            float t = pacc[q][k];
-            t = fmaf(mb[q][0], x.x, t);
-            t = fmaf(mb[q][1], x.y, t);
-            t = fmaf(mb[q][2], x.z, t);
-            t = fmaf(mb[q][3], x.w, t);
-            pacc[q][k] = t;
-          }
-        }
-      }
-    }
-    if (ch == nchunks - 1) {
-#pragma unroll
-      for (int q = 0; q < RW; ++q) {
-        const float tot = warp_reduce_scatter<RP>(pacc[q]);
-        // An inf or NaN among the row's inputs reaches every sum it enters
-        // (inf * 0 is NaN), so the reduced partial is non-finite exactly when
-        // an input was (or the sums overflowed).
-        chk = fmaf(tot, 0.f, chk);
-        constexpr int SH = 5 - log2_rp<RP>();
-        if (rv[q] && (lane & ((1 << SH) - 1)) == 0) {
-          float* dst = a.praw_part + td.pp_off + ((long long)item.ct * td.n + item.row0 + rr + q) * RP;
-          dst[lane >> SH] = tot;
-        }
-      }
-    }
-    if (++ch == nchunks) { ch = 0; ++g; }
-    if (++cslot == S) cslot = 0;
-  }
-  cp_async_wait<0>();
-}
-
 // ---------------------------------------------------------------------------
 // Pass 1, chunk-stationary (RP <= 8).  Warp w of the CTA owns chunk
 // (w % nch) of the item's column tile (nch <= 8 chunks of 128 columns) and
 // every (8 / nch)-th row of the item, so each lane loads the Q values of its
 // 4 columns once per item and keeps them in registers.  Its
 // source segments (one row x 128 columns of every replica's gradient and
-// store) are staged by cp.async S rows ahead, as in pass1_tile_staged.  Each
+// store) are staged by cp.async S rows ahead.  Each
 // row's P partial over the chunk is reduced across the warp and parked in
 // shared memory; at the end of the item the CTA adds the chunk partials in
 // chunk order and writes one partial per (row, column tile).
@@ -980,32 +737,6 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
       else
         pass1_tile<RP, WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
     }
-  }
-  bad |= !(chk == 0.f);
-  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
-}
-
-template <int RP, int WT, typename GT, int RW, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB) k_pass1_staged(const StepArgs a) {
-  extern __shared__ __align__(16) char p1smem[];
-  using St = Pass1Stage<RP, WT, GT, RW, MINB>;
-  const int cur = a.ctrl->cur;
-  const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
-  const float* Qc = a.Qf + (long long)cur * a.q_total;
-  const float* Pc = a.Pf + (long long)cur * a.p_total;
-  const float* Qp = use_init ? a.qinit : Qc;
-  char* wsm = p1smem + (threadIdx.x >> 5) * (St::S * St::UNIT_BYTES);
-  float* qtile = reinterpret_cast<float*>(p1smem + 8 * St::S * St::UNIT_BYTES);
-  int bad = 0;
-  float chk = 0.f;
-  for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
-    const Item item = a.p1items[it];
-    const TensorDesc td = a.tensors[item.t];
-    // items the bucket does not wholly back (batched hook) take the checked path
-    if (td.vec && a.vec_ok && (long long)(item.row0 + item.nrows) * td.m <= td.valid)
-      pass1_tile_staged<RP, WT, GT, RW, MINB>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, qtile);
-    else
-      pass1_tile<RP, WT, GT, RW, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
   }
   bad |= !(chk == 0.f);
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);

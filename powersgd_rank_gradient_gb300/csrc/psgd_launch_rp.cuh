@@ -5,6 +5,7 @@
 #include "psgd_gs.cuh"
 #include "psgd_kernels.cuh"
 #include "psgd_launch.h"
+#include "psgd_tiled.cuh"
 
 namespace psgd {
 
@@ -20,16 +21,16 @@ inline void by_gtype(int gtype, F&& f) {
     f(0.0f);
 }
 
-template <int RP, int WT, typename GT, int RW, int MINB>
-void launch_pass1_staged(const StepArgs& a, int grid, cudaStream_t s) {
-  using St = Pass1Stage<RP, WT, GT, RW, MINB>;
+template <int RP, typename GT>
+void launch_pass1_tiled(const StepArgs& a, int grid, cudaStream_t s) {
+  using T = Pass1Tiled<RP, GT>;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(k_pass1_staged<RP, WT, GT, RW, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         St::SMEM);
+    cudaFuncSetAttribute(k_pass1_tiled<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
     configured = true;
   }
-  k_pass1_staged<RP, WT, GT, RW, MINB><<<grid * MINB, kThreads, St::SMEM, s>>>(a);
+  if (a.vec_ok && a.has_aligned) k_pass1_tiled<RP, GT><<<grid, kThreads, T::SMEM, s>>>(a);
+  if (!a.vec_ok || a.has_unaligned) k_pass1_rest<RP, GT><<<grid * 2, kThreads, 0, s>>>(a);
 }
 
 template <int RP, int WT, typename GT, int MINB>
@@ -49,7 +50,7 @@ void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
 
 // grid = one CTA per SM; the kernels run MINB CTAs per SM.  Ranks up to 8 use
 // the chunk-stationary kernel (two CTAs per SM for W <= 2, one above); ranks
-// 16 and 32 keep Q in L1 and use pass1_tile_staged (one CTA per SM).
+// 16 and 32 the register-tiled kernel (one CTA per SM, any W).
 template <int RP>
 void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
   by_gtype(a.gtype, [&](auto tag) {
@@ -63,13 +64,7 @@ void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
         default: k_pass1<RP, 0, GT, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
       }
     } else {
-      switch (a.W) {
-        case 1: launch_pass1_staged<RP, 1, GT, 1, 1>(a, grid, s); break;
-        case 2: launch_pass1_staged<RP, 2, GT, 1, 1>(a, grid, s); break;
-        case 4: launch_pass1_staged<RP, 4, GT, 1, 1>(a, grid, s); break;
-        case 8: launch_pass1_staged<RP, 8, GT, 1, 1>(a, grid, s); break;
-        default: k_pass1<RP, 0, GT, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
-      }
+      launch_pass1_tiled<RP, GT>(a, grid, s);
     }
   });
 }

@@ -77,6 +77,40 @@ def test_mixed_bucket_ranks(rank):
     _run(MIXED, 2, rank, 3, min_compression_rate=0.25, label=f"r={rank}")
 
 
+# Tensors whose rows are 16-byte aligned in the bucket (column counts and
+# offsets multiples of 4): ranks 16 and 32 run them through the register-tiled
+# pass 1.  Ragged row items (300 = 2 x 128 + 44 rows, 129 rows), ragged column
+# tiles and chunks (1060 = 2 x 512 + 36 columns, 516, 36).  Every view has more
+# than 32 rows and columns, so at rank 32 the residual is not rounding noise.
+ALIGNED = [(300, 1060), (129, 36), (64,), (1000, 516), (48, 16, 2, 2)]
+
+
+@pytest.mark.parametrize("rank", [16, 32])
+@pytest.mark.parametrize("world,kw", [
+    (1, {}),
+    (3, {}),
+    (8, {"heavy": 0.01, "std": 1e-3}),
+    (2, {"use_error_feedback": False}),
+    (2, {"orthogonalization_epsilon": 1e-8}),
+], ids=["W1", "W3", "W8-heavy", "W2-noEF", "W2-eps"])
+def test_aligned_bucket_high_ranks(rank, world, kw):
+    _run(ALIGNED, world, rank, 3, min_compression_rate=0.25, label=f"aligned r={rank} W={world}", **kw)
+
+
+@pytest.mark.parametrize("rank", [16, 32])
+def test_aligned_bucket_high_ranks_cold(rank):
+    """warm_start off: pass 1 projects on a fresh draw while it subtracts the
+    committed factors (two different Q matrices in one pass)."""
+    pair = Pair(ALIGNED, 2, rank, DEV, start_powerSGD_iter=0, min_compression_rate=0.25, warm_start=False)
+    for step in range(3):
+        if step > 0:
+            pair.inject_draws(seed=20 + step)
+        skipped, status, out, exp = pair.step(grads_for(ALIGNED, 2, step))
+        assert not skipped
+        pair.compare(out, exp, label=f"cold r={rank} step {step}")
+    pair.close()
+
+
 def test_heavy_rows_batched():
     _run(MIXED, 8, 4, 4, heavy=0.01, std=1e-3, batch_tensors_with_same_shape=True, label="heavy")
 
@@ -359,8 +393,9 @@ def test_library_draw_matches_oracle_philox(warm):
     st.close()
 
 
+@pytest.mark.parametrize("rank", [4, 32])
 @pytest.mark.parametrize("world,ef", [(1, True), (2, True), (3, False), (8, True)])
-def test_bf16_buckets(world, ef):
+def test_bf16_buckets(world, ef, rank):
     """16-bit (bf16) replica buckets, as the bf16 compress wrapper produces:
     the oracle is fed the same bf16 values widened to float64."""
     import oracle
@@ -368,10 +403,10 @@ def test_bf16_buckets(world, ef):
     from powersgd_rank_gradient_gb300 import PowerSGDState
 
     shapes = MIXED
-    st = PowerSGDState(shapes, world, matrix_approximation_rank=4, start_powerSGD_iter=1,
+    st = PowerSGDState(shapes, world, matrix_approximation_rank=rank, start_powerSGD_iter=1,
                        min_compression_rate=1.0, use_error_feedback=ef, grad_dtype=torch.bfloat16,
                        device=DEV)
-    ref = oracle.PowerSGDOracle(shapes=shapes, world_size=world, matrix_approximation_rank=4,
+    ref = oracle.PowerSGDOracle(shapes=shapes, world_size=world, matrix_approximation_rank=rank,
                                 start_powerSGD_iter=1, min_compression_rate=1.0, use_error_feedback=ef)
     for t, plan in enumerate(ref.plans):
         if plan.compressed:
