@@ -176,7 +176,8 @@ struct psgd_state {
   float* pgs = nullptr;
   float* qpart = nullptr;
   float* tmat = nullptr;
-  double* gram = nullptr;
+  float2* gram = nullptr;   // per Gram-Schmidt item RP x RP double-float partials
+  float2* gram_t = nullptr; // per tensor RP x RP summed Gram matrix (double-float)
   Ctrl* ctrl = nullptr;
   int* d_status = nullptr;
   int* h_status = nullptr;  // pinned
@@ -442,6 +443,7 @@ StepArgs make_args(psgd_state* s) {
   a.pgs = s->pgs;
   a.qpart = s->qpart;
   a.gram = s->gram;
+  a.gram_t = s->gram_t;
   a.tmat = s->tmat;
   a.tensors = s->d_tensors;
   a.items = s->d_items;
@@ -517,18 +519,20 @@ struct Ops {
     }
     L.begin(K_GRAM);
     launch_gram<RP>(a, src_dense, nullptr, is_q, 0, s->gram, grid, L.st);
+    launch_gram_sum<RP>(a, is_q, L.st);
     L.end();
     L.begin(K_SOLVE);
-    launch_solve<RP>(a, s->gram, is_q, L.st);
+    launch_solve<RP>(a, s->gram_t, is_q, L.st);
     L.end();
     L.begin(K_APPLY);
     launch_apply<RP>(a, src_dense, s->pgs, is_q, -1, grid, L.st);
     L.end();
     L.begin(K_GRAM);
     launch_gram<RP>(a, s->pgs, nullptr, is_q, 0, s->gram, grid, L.st);
+    launch_gram_sum<RP>(a, is_q, L.st);
     L.end();
     L.begin(K_SOLVE);
-    launch_solve<RP>(a, s->gram, is_q, L.st);
+    launch_solve<RP>(a, s->gram_t, is_q, L.st);
     L.end();
     L.begin(K_APPLY);
     if (is_q)
@@ -788,7 +792,8 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   TRY(dalloc(s, (void**)&s->pgs, (size_t)std::max(s->p_total, s->q_total) * sizeof(float)));
   TRY(dalloc(s, (void**)&s->qpart, (size_t)s->qp_total * sizeof(float)));
   TRY(dalloc(s, (void**)&s->tmat, std::max(1, nt) * RP * RP * sizeof(float)));
-  TRY(dalloc(s, (void**)&s->gram, std::max<size_t>(1, std::max(s->gsp.size(), s->gsq.size())) * RP * RP * sizeof(double)));
+  TRY(dalloc(s, (void**)&s->gram, std::max<size_t>(1, std::max(s->gsp.size(), s->gsq.size())) * RP * RP * sizeof(float2)));
+  TRY(dalloc(s, (void**)&s->gram_t, std::max(1, nt) * RP * RP * sizeof(float2)));
   TRY(dalloc(s, (void**)&s->ctrl, sizeof(Ctrl)));
   TRY(dalloc(s, (void**)&s->d_status, sizeof(int)));
   if (cudaMallocHost((void**)&s->h_status, sizeof(int)) != cudaSuccess) {

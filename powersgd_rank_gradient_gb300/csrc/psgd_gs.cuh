@@ -60,13 +60,33 @@ __global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
 
 constexpr int kGramTile = 128;
 
-// Rows of P live as column-tile partials (nparts > 1) or dense (nparts == 1).
+// Double-float accumulation on the fp32 pipes (fp64 throughput is a small
+// fraction of fp32 on this GPU): (hi, lo) holds an unevaluated sum.  The
+// product's rounding error comes from one FMA and the sum's from Knuth's
+// two-sum, so each term adds its exact value up to the rounding of `lo`
+// (about 2^-44 relative to the total).  The explicit-rounding intrinsics keep
+// the compiler from contracting the error terms into FMAs.
+__device__ __forceinline__ void df_add(float& hi, float& lo, float b, float blo) {
+  const float s = __fadd_rn(hi, b);
+  const float bp = __fsub_rn(s, hi);
+  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(e, blo));
+}
+__device__ __forceinline__ void df_add_prod(float& hi, float& lo, float a, float b) {
+  const float p = __fmul_rn(a, b);
+  df_add(hi, lo, p, fmaf(a, b, -p));
+}
+
+// Per Gram-Schmidt item: the Gram matrix X^T X of its rows, each entry a
+// double-float (hi, lo) pair.  Rows of P come dense (nparts == 1) or as
+// column-tile partials (from_parts).
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float* __restrict__ src,
                                                    float* __restrict__ dense_out, int is_q,
-                                                   int from_parts, double* __restrict__ gram_out) {
+                                                   int from_parts, float2* __restrict__ gram_out) {
   __shared__ float tile[kGramTile][RP + 1];
-  __shared__ double red[kThreads];
+  __shared__ float2 red[kThreads];
   constexpr int PAIRS = RP * RP;
   constexpr int PPT = PAIRS > kThreads ? PAIRS / kThreads : 1;   // pairs per thread
   constexpr int GROUPS = PAIRS >= kThreads ? 1 : kThreads / PAIRS;
@@ -79,9 +99,9 @@ __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float
     const long long base = is_q ? td.q_off : td.p_off;
     const int pair0 = (threadIdx.x % (PAIRS >= kThreads ? kThreads : PAIRS)) * PPT;
     const int grp = PAIRS >= kThreads ? 0 : threadIdx.x / PAIRS;
-    double dacc[PPT];
+    float hi[PPT], lo[PPT];
 #pragma unroll
-    for (int u = 0; u < PPT; ++u) dacc[u] = 0.0;
+    for (int u = 0; u < PPT; ++u) { hi[u] = 0.f; lo[u] = 0.f; }
     for (int r0 = 0; r0 < gi.nrows; r0 += kGramTile) {
       const int rows = min(kGramTile, gi.nrows - r0);
       __syncthreads();
@@ -105,158 +125,197 @@ __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float
 #pragma unroll
       for (int u = 0; u < PPT; ++u) {
         const int pa = (pair0 + u) / RP, pb = (pair0 + u) % RP;
-        float facc = 0.f;
-        int cnt = 0;
-        for (int rr = grp; rr < rows; rr += GROUPS) {
-          facc = fmaf(tile[rr][pa], tile[rr][pb], facc);
-          if (++cnt == 8) { dacc[u] += (double)facc; facc = 0.f; cnt = 0; }
-        }
-        dacc[u] += (double)facc;
+        for (int rr = grp; rr < rows; rr += GROUPS) df_add_prod(hi[u], lo[u], tile[rr][pa], tile[rr][pb]);
       }
     }
-    // reduce the row groups
+    // reduce the row groups (in group order)
 #pragma unroll
     for (int u = 0; u < PPT; ++u) {
       __syncthreads();
-      red[threadIdx.x] = dacc[u];
+      red[threadIdx.x] = make_float2(hi[u], lo[u]);
       __syncthreads();
       if (threadIdx.x < (PAIRS >= kThreads ? kThreads : PAIRS)) {
-        double s = 0.0;
-        for (int g = 0; g < GROUPS; ++g) s += red[threadIdx.x + g * (PAIRS >= kThreads ? kThreads : PAIRS)];
+        float2 s = red[threadIdx.x];
+        for (int g = 1; g < GROUPS; ++g) {
+          const float2 x = red[threadIdx.x + g * (PAIRS >= kThreads ? kThreads : PAIRS)];
+          df_add(s.x, s.y, x.x, x.y);
+        }
         gram_out[(long long)it * PAIRS + pair0 + u] = s;
       }
     }
   }
 }
 
-// One CTA per tensor: the whole CTA adds up the item Gram matrices (for
-// ranks up to 8 each entry split over SPLIT threads, for 16 and 32 several
-// entries per thread; four accumulators each, combined in a fixed order),
-// then runs modified Gram-Schmidt with epsilon on the
-// coefficient matrix T (X_out = X T), in fp64 with T and H = G T in shared
-// memory.  Step i, with t_i still unscaled: ||x_i||^2 = t_i . h_i, sc_i =
-// 1 / (||x_i|| + eps); every later column j loses its projection on the
-// normalised x_i: t_j -= c t_i and h_j -= c h_i with c = sc_i^2 (t_i . h_j).
-// The column scalings are applied to T at the end (t_i is not read again
-// after its own step).  Thread (j, p) of the TEAM owns rows [p R, p R + R)
-// of column j; the PARTS threads of a column add their partial dot products
-// with shuffles.  Ranks up to 8 fit one warp (steps end with __syncwarp),
-// larger ones use the whole CTA (__syncthreads).
+// The items' Gram matrices of each tensor added up: CTA (tensor, block of
+// EPC entries), its threads in GROUPS item groups, each summing every
+// GROUPS-th item as double-floats (eight loads in flight), the groups then
+// combined in group order.
+constexpr int kGramSumEntries = 32;
+
 template <int RP>
-__global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const double* __restrict__ gram_in,
+__global__ void __launch_bounds__(kThreads) k_gram_sum(const StepArgs a, int is_q) {
+  constexpr int ENT = RP * RP;
+  constexpr int EPC = ENT < kGramSumEntries ? ENT : kGramSumEntries;
+  constexpr int GROUPS = kThreads / EPC;
+  __shared__ float2 part[kThreads];
+  if (a.ctrl->flag) return;
+  const int t = blockIdx.x;
+  const int e = blockIdx.y * EPC + threadIdx.x % EPC;
+  const int g = threadIdx.x / EPC;
+  const int first = is_q ? a.gsq_first[t] : a.gsp_first[t];
+  const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
+  const float2* src = a.gram + (long long)first * ENT + e;
+  float hi[2] = {0.f, 0.f}, lo[2] = {0.f, 0.f};
+  int it = g;
+  for (; it + 7 * GROUPS < count; it += 8 * GROUPS) {
+    float2 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = src[(long long)(it + u * GROUPS) * ENT];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) df_add(hi[u & 1], lo[u & 1], x[u].x, x[u].y);
+  }
+  for (; it < count; it += GROUPS) {
+    const float2 x = src[(long long)it * ENT];
+    df_add(hi[0], lo[0], x.x, x.y);
+  }
+  df_add(hi[0], lo[0], hi[1], lo[1]);
+  part[threadIdx.x] = make_float2(hi[0], lo[0]);
+  __syncthreads();
+  if (g == 0) {
+    float vh = 0.f, vl = 0.f;
+    for (int q = 0; q < GROUPS; ++q) df_add(vh, vl, part[q * EPC + threadIdx.x].x, part[q * EPC + threadIdx.x].y);
+    a.gram_t[(long long)t * ENT + e] = make_float2(vh, vl);
+  }
+}
+
+// Double-float values (hi + lo, |lo| <= ulp(hi) / 2 after normalisation) for
+// the Gram-Schmidt recurrence.  fp64 runs at a small fraction of the fp32
+// rate on this GPU; these operations keep about 44 bits on the fp32 pipes.
+struct Dd {
+  float hi, lo;
+};
+__device__ __forceinline__ Dd dd_norm(float s, float e) {   // Fast2Sum, |s| >= |e|
+  const float h = __fadd_rn(s, e);
+  return {h, __fsub_rn(e, __fsub_rn(h, s))};
+}
+__device__ __forceinline__ Dd dd_add(Dd a, Dd b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bp = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(b.hi, bp));
+  return dd_norm(s, __fadd_rn(e, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ Dd dd_mul(Dd a, Dd b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return dd_norm(p, e);
+}
+__device__ __forceinline__ Dd dd_neg(Dd a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ Dd dd_of(float2 v) { return dd_norm(v.x, v.y); }
+
+// sc = 1 / (sqrt(nn) + eps) for the squared column norm nn.  For eps = 0 and
+// nn > 0 it is 1 / sqrt(nn): an rsqrtf seed y refined by one Newton step for
+// f(y) = 1 / y^2 - nn, y <- y + y (1 - nn y^2) / 2, with the residual in
+// double-float (the seed's ~23 correct bits become ~44).  Otherwise the
+// square root (sqrtf seed, one Newton step s <- s + (nn - s^2) / (2 s)) and
+// the reciprocal (1 / d seed, one Newton step z <- z + z (1 - d z)) are
+// refined the same way.  A zero denominator gives inf, and then NaN for a
+// zero column with eps = 0, as the oracle.
+__device__ __forceinline__ Dd dd_gs_scale(Dd nn, float eps) {
+  const Dd one = {1.f, 0.f};
+  if (eps == 0.f && nn.hi > 0.f && nn.hi < 3e38f) {
+    const Dd y = {rsqrtf(nn.hi), 0.f};
+    const Dd r = dd_add(one, dd_neg(dd_mul(nn, dd_mul(y, y))));
+    return dd_add(y, dd_mul(y, {0.5f * r.hi, 0.5f * r.lo}));
+  }
+  if (nn.hi != nn.hi) return nn;   // NaN
+  Dd sq = {0.f, 0.f};
+  if (nn.hi > 0.f) {
+    const Dd s0 = {sqrtf(nn.hi), 0.f};
+    if (s0.hi < 3e38f) {
+      const Dd r = dd_add(nn, dd_neg(dd_mul(s0, s0)));
+      sq = dd_add(s0, {__fdiv_rn(r.hi, 2.f * s0.hi), 0.f});
+    } else {
+      sq = s0;
+    }
+  }
+  const Dd den = dd_add(sq, {eps, 0.f});
+  if (den.hi == 0.f) return {__int_as_float(0x7f800000), 0.f};
+  const Dd z = {__frcp_rn(den.hi), 0.f};
+  if (!(z.hi > 0.f)) return z;     // den overflowed: sc rounds to 0
+  const Dd r = dd_add(one, dd_neg(dd_mul(den, z)));
+  return dd_add(z, dd_mul(z, r));
+}
+
+// One CTA per tensor, on the tensor's Gram matrix G (k_gram_sum): modified
+// Gram-Schmidt with epsilon on the coefficient matrix T (X_out = X T), in
+// double-float with T and H = G T in shared memory.  Step i, with t_i still
+// unscaled: ||x_i||^2 = t_i . h_i, sc_i = 1 / (||x_i|| + eps); every later
+// column j loses its projection on the normalised x_i: t_j -= c t_i and
+// h_j -= c h_i with c = sc_i^2 (t_i . h_j).  A step touches only the rows
+// that can be nonzero (t_i has none below row i, H none at or past rank r).
+// Ranks up to 8 run the steps on one warp (__syncwarp between steps), 16 and
+// 32 on the CTA (__syncthreads), the work of a step spread over its threads.
+// The column scalings are applied to T at the end (t_i is not read again
+// after its own step).
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const float2* __restrict__ gram_in,
                                                     int is_q, int only_init) {
   constexpr int ENT = RP * RP;
-  constexpr int SPLIT = ENT >= kThreads ? 1 : kThreads / ENT;
-  constexpr int TEAM = ENT <= 64 ? 32 : kThreads;
-  constexpr int R = ENT > TEAM ? ENT / TEAM : 1;            // rows per thread
-  constexpr int PARTS = RP / R;                             // threads per column
   constexpr int LD = RP + 1;                                // padded column stride
-  __shared__ double H[RP * LD];   // H[j * LD + k] = row k of column j of G T
-  __shared__ double T[RP * LD];   // T[j * LD + k] = row k of column j
-  __shared__ double scal[RP];
-  __shared__ double part[kThreads];
+  // the steps run on one warp for ranks up to 8 and on the CTA above, thread
+  // (j, p) owning rows [p R, p R + R) of column j; the PARTS threads of a
+  // column add their partial dot products with shuffles
+  constexpr int TEAM = ENT <= 64 ? 32 : kThreads;
+  constexpr int R = ENT > TEAM ? ENT / TEAM : 1;
+  constexpr int PARTS = RP / R;
+  __shared__ Dd H[RP * LD];   // H[j * LD + k] = row k of column j of G T
+  __shared__ Dd T[RP * LD];   // T[j * LD + k] = row k of column j
+  __shared__ Dd scal[RP];
   const int t = blockIdx.x;
   if (a.ctrl->flag) return;
   const TensorDesc td = a.tensors[t];
-  const int first = is_q ? a.gsq_first[t] : a.gsp_first[t];
   const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
   if (count == 0) return;
-  if constexpr (ENT >= kThreads) {
-    // EPT entries per thread, four chains each, all in flight together
-    constexpr int EPT = ENT / kThreads;
-    double acc[EPT][4];
-#pragma unroll
-    for (int e = 0; e < EPT; ++e)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) acc[e][u] = 0.0;
-    int it = 0;
-    for (; it + 4 <= count; it += 4) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < EPT; ++e)
-          acc[e][u] += gram_in[(long long)(first + it + u) * ENT + threadIdx.x + e * kThreads];
-    }
-    for (; it < count; ++it)
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) acc[e][0] += gram_in[(long long)(first + it) * ENT + threadIdx.x + e * kThreads];
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const int idx = threadIdx.x + e * kThreads;
-      const int k = idx / RP, j = idx % RP;   // G is symmetric: entry (k, j)
-      H[j * LD + k] = (acc[e][0] + acc[e][1]) + (acc[e][2] + acc[e][3]);
-      T[j * LD + k] = (k == j && j < td.r) ? 1.0 : 0.0;
-    }
-    __syncthreads();
-  } else {
-    // SPLIT threads per entry, four chains each, combined in a fixed order
-    const int idx = threadIdx.x / SPLIT;
-    const int sp = threadIdx.x % SPLIT;
-    double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
-    if (idx < ENT) {
-      int it = sp;
-      for (; it + 3 * SPLIT < count; it += 4 * SPLIT) {
-        s0 += gram_in[(long long)(first + it) * ENT + idx];
-        s1 += gram_in[(long long)(first + it + SPLIT) * ENT + idx];
-        s2 += gram_in[(long long)(first + it + 2 * SPLIT) * ENT + idx];
-        s3 += gram_in[(long long)(first + it + 3 * SPLIT) * ENT + idx];
-      }
-      for (; it < count; it += SPLIT) s0 += gram_in[(long long)(first + it) * ENT + idx];
-    }
-    part[threadIdx.x] = (s0 + s1) + (s2 + s3);
-    __syncthreads();
-    if (sp == 0 && idx < ENT) {
-      double v = 0.0;
-      for (int q = 0; q < SPLIT; ++q) v += part[threadIdx.x + q];
-      const int k = idx / RP, j = idx % RP;   // G is symmetric: entry (k, j)
-      H[j * LD + k] = v;
-      T[j * LD + k] = (k == j && j < td.r) ? 1.0 : 0.0;
-    }
-    __syncthreads();
+  for (int idx = threadIdx.x; idx < ENT; idx += kThreads) {
+    const int k = idx / RP, j = idx % RP;   // G is symmetric: entry (k, j)
+    H[j * LD + k] = dd_of(gram_in[(long long)t * ENT + idx]);
+    T[j * LD + k] = {(k == j && j < td.r) ? 1.f : 0.f, 0.f};
   }
+  __syncthreads();
   if (threadIdx.x >= TEAM) return;
   const int r = td.r;
-  const double eps = (double)a.eps;
   const int lane = threadIdx.x & 31;
   const int j = threadIdx.x / PARTS, p = threadIdx.x % PARTS;
   const bool own = j < RP;
   for (int i = 0; i < r; ++i) {
     // ||x_i||^2 = t_i . h_i, by every warp (t_i has no entries below row i)
-    double nn = (lane <= i) ? T[i * LD + lane] * H[i * LD + lane] : 0.0;
+    Dd nn = (lane <= i && lane < RP) ? dd_mul(T[i * LD + lane], H[i * LD + lane]) : Dd{0.f, 0.f};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nn += __shfl_xor_sync(0xffffffffu, nn, o);
-    // sc = 1 / (sqrt(nn) + eps).  For eps = 0 and nn > 0 it is 1 / sqrt(nn):
-    // an fp32 rsqrtf seed refined by one Newton-Raphson step for
-    // f(y) = 1 / y^2 - nn (y <- y (3 - nn y^2) / 2), which takes the seed's
-    // ~24 correct bits to ~48 with three dependent fp64 operations instead of
-    // an fp64 square root and division.  A zero or negative nn, and eps > 0,
-    // take the direct expression (eps = 0 with a zero column gives inf and
-    // then NaN, as the oracle).
-    double sc;
-    if (eps == 0.0 && nn > 0.0 && nn < 1e300) {
-      const double y = (double)rsqrtf((float)nn);
-      sc = y * (1.5 - 0.5 * nn * y * y);
-    } else {
-      sc = 1.0 / (sqrt(fmax(nn, 0.0)) + eps);
-    }
+    for (int o = 16; o > 0; o >>= 1)
+      nn = dd_add(nn, {__shfl_xor_sync(0xffffffffu, nn.hi, o), __shfl_xor_sync(0xffffffffu, nn.lo, o)});
+    const Dd sc = dd_gs_scale(nn, a.eps);
     if (threadIdx.x == 0) scal[i] = sc;
-    double d = 0.0;
-    if (own && j > i && j < r) {
+    Dd d = {0.f, 0.f};
+    const bool upd = own && j > i && j < r;
+    if (upd) {
 #pragma unroll
       for (int q = 0; q < R; ++q) {
         const int k = p * R + q;
-        d += T[i * LD + k] * H[j * LD + k];
+        if (k <= i) d = dd_add(d, dd_mul(T[i * LD + k], H[j * LD + k]));
       }
     }
 #pragma unroll
-    for (int o = PARTS / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-    if (own && j > i && j < r) {
-      const double c = d * sc * sc;
+    for (int o = PARTS / 2; o > 0; o >>= 1)
+      d = dd_add(d, {__shfl_xor_sync(0xffffffffu, d.hi, o), __shfl_xor_sync(0xffffffffu, d.lo, o)});
+    if (upd) {
+      const Dd nc = dd_neg(dd_mul(dd_mul(d, sc), sc));
 #pragma unroll
       for (int q = 0; q < R; ++q) {
         const int k = p * R + q;
-        T[j * LD + k] -= c * T[i * LD + k];
-        H[j * LD + k] -= c * H[i * LD + k];
+        if (k <= i) T[j * LD + k] = dd_add(T[j * LD + k], dd_mul(nc, T[i * LD + k]));
+        if (k < r) H[j * LD + k] = dd_add(H[j * LD + k], dd_mul(nc, H[i * LD + k]));
       }
     }
     if constexpr (TEAM == 32) __syncwarp(); else __syncthreads();
@@ -264,15 +323,26 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const doub
   float* Tout = a.tmat + (long long)t * RP * RP;
   for (int idx = threadIdx.x; idx < ENT; idx += TEAM) {
     const int k = idx / RP, jj = idx % RP;
-    Tout[idx] = (float)(jj < r ? T[jj * LD + k] * scal[jj] : 0.0);
+    float v = 0.f;
+    if (jj < r) {
+      const Dd x = dd_mul(T[jj * LD + k], scal[jj]);
+      v = __fadd_rn(x.hi, x.lo);
+    }
+    Tout[idx] = v;
   }
 }
 
-// dst rows = src rows x T (thread per row).
+// dst rows = src rows x T.  Each thread computes OPT consecutive output
+// columns of one row (KG threads per row), each as the increasing-l FMA chain
+// over the row's RP inputs.  P (row-major) puts a row's KG threads next to
+// each other; Q (k-major) puts 32 consecutive rows in a warp, so its column
+// reads and writes are coalesced.
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const float* __restrict__ src,
                                                     float* __restrict__ dst, int is_q, int dst_half) {
-  __shared__ float T[RP * RP];
+  constexpr int OPT = RP >= 4 ? 4 : RP;
+  constexpr int KG = RP / OPT;
+  __shared__ __align__(16) float T[RP * RP];
   const GsItem* items = is_q ? a.gsq_items : a.gsp_items;
   const int n_items = is_q ? a.n_gsq : a.n_gsp;
   if (a.ctrl->flag) return;
@@ -286,20 +356,43 @@ __global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const floa
     __syncthreads();
     for (int idx = threadIdx.x; idx < RP * RP; idx += kThreads) T[idx] = a.tmat[(long long)gi.t * RP * RP + idx];
     __syncthreads();
-    for (int rr = threadIdx.x; rr < gi.nrows; rr += kThreads) {
+    const int span = is_q ? (gi.nrows + 31) / 32 * 32 * KG : gi.nrows * KG;
+    for (int idx = threadIdx.x; idx < span; idx += kThreads) {
+      const int rr = is_q ? (idx / (32 * KG)) * 32 + (idx & 31) : idx / KG;
+      const int kg = is_q ? (idx >> 5) % KG : idx % KG;
+      if (rr >= gi.nrows) continue;
       const long long row = gi.row0 + rr;
-      float x[RP], y[RP];
-      // P is row-major (rows x RP); Q is k-major (element (j, k) at k * m + j)
-      const long long rs = is_q ? 1 : RP;
-      const long long ks = is_q ? td.m : 1;
+      float x[RP], y[OPT];
+      if (is_q) {
 #pragma unroll
-      for (int k = 0; k < RP; ++k) { x[k] = src[base + row * rs + k * ks]; y[k] = 0.f; }
+        for (int k = 0; k < RP; ++k) x[k] = src[base + (long long)k * td.m + row];
+      } else {
+        load_row<RP>(src + base + row * RP, x);
+      }
 #pragma unroll
-      for (int l = 0; l < RP; ++l)
+      for (int o = 0; o < OPT; ++o) y[o] = 0.f;
 #pragma unroll
-        for (int k = 0; k < RP; ++k) y[k] = fmaf(x[l], T[l * RP + k], y[k]);
+      for (int l = 0; l < RP; ++l) {
+        if constexpr (OPT == 4) {
+          const float4 tv = *reinterpret_cast<const float4*>(&T[l * RP + kg * 4]);
+          y[0] = fmaf(x[l], tv.x, y[0]);
+          y[1] = fmaf(x[l], tv.y, y[1]);
+          y[2] = fmaf(x[l], tv.z, y[2]);
+          y[3] = fmaf(x[l], tv.w, y[3]);
+        } else {
 #pragma unroll
-      for (int k = 0; k < RP; ++k) dst[half_off + base + row * rs + k * ks] = y[k];
+          for (int o = 0; o < OPT; ++o) y[o] = fmaf(x[l], T[l * RP + o], y[o]);
+        }
+      }
+      if (is_q) {
+#pragma unroll
+        for (int o = 0; o < OPT; ++o) dst[half_off + base + (long long)(kg * OPT + o) * td.m + row] = y[o];
+      } else if constexpr (OPT == 4) {
+        *reinterpret_cast<float4*>(dst + half_off + base + row * RP + kg * 4) = make_float4(y[0], y[1], y[2], y[3]);
+      } else {
+#pragma unroll
+        for (int o = 0; o < OPT; ++o) dst[half_off + base + row * RP + o] = y[o];
+      }
     }
   }
 }

@@ -51,7 +51,8 @@ struct StepArgs {
   float* praw;        // summed P_raw
   float* pgs;         // first Gram-Schmidt sweep output (P and Q share it)
   float* qpart;       // pass-2 partials
-  double* gram;       // per Gram-Schmidt item RP x RP
+  float2* gram;       // per Gram-Schmidt item RP x RP (double-float)
+  float2* gram_t;     // per tensor RP x RP, the items' sum
   float* tmat;        // per tensor RP x RP transform
   const TensorDesc* tensors;
   const Item* items;         // tall (row block) x (column tile) items: pass 2

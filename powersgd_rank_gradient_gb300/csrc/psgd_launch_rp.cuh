@@ -76,12 +76,18 @@ void launch_psum(const StepArgs& a, int grid, cudaStream_t s) {
 
 template <int RP>
 void launch_gram(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts,
-                 double* gram, int grid, cudaStream_t s) {
+                 float2* gram, int grid, cudaStream_t s) {
   k_gram<RP><<<grid, kThreads, 0, s>>>(a, src, dense_out, is_q, from_parts, gram);
 }
 
 template <int RP>
-void launch_solve(const StepArgs& a, const double* gram, int is_q, cudaStream_t s) {
+void launch_gram_sum(const StepArgs& a, int is_q, cudaStream_t s) {
+  constexpr int EPC = RP * RP < kGramSumEntries ? RP * RP : kGramSumEntries;
+  k_gram_sum<RP><<<dim3(a.n_tensors, (RP * RP) / EPC), kThreads, 0, s>>>(a, is_q);
+}
+
+template <int RP>
+void launch_solve(const StepArgs& a, const float2* gram, int is_q, cudaStream_t s) {
   k_solve<RP><<<a.n_tensors, kThreads, 0, s>>>(a, gram, is_q, 0);
 }
 
@@ -135,9 +141,10 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
 #define PSGD_INSTANTIATE(RPV)                                                                   \
   template void launch_pass1<RPV>(const StepArgs&, int, cudaStream_t);                          \
   template void launch_psum<RPV>(const StepArgs&, int, cudaStream_t);                           \
-  template void launch_gram<RPV>(const StepArgs&, const float*, float*, int, int, double*, int, \
+  template void launch_gram<RPV>(const StepArgs&, const float*, float*, int, int, float2*, int, \
                                  cudaStream_t);                                                 \
-  template void launch_solve<RPV>(const StepArgs&, const double*, int, cudaStream_t);           \
+  template void launch_gram_sum<RPV>(const StepArgs&, int, cudaStream_t);                      \
+  template void launch_solve<RPV>(const StepArgs&, const float2*, int, cudaStream_t);           \
   template void launch_apply<RPV>(const StepArgs&, const float*, float*, int, int, int,         \
                                   cudaStream_t);                                                \
   template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
