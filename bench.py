@@ -130,7 +130,7 @@ def kernel_src_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "powersgd_rank_gradient_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if not (f in ("psgd_kernels.cuh", "psgd_tiled.cuh", "psgd_internal.h", "psgd_launch_rp.cuh")
+        if not (f in ("psgd_kernels.cuh", "psgd_mma.cuh", "psgd_internal.h", "psgd_launch_rp.cuh")
                 or (f.startswith("kern_rp") and f.endswith(".cu"))):
             continue
         with open(os.path.join(csrc, f), "rb") as fh:

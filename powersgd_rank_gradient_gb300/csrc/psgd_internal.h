@@ -24,7 +24,7 @@ namespace psgd {
 constexpr int kThreads = 256;      // threads per CTA of the streaming passes
 constexpr int kRowBlock = 512;     // rows per work item of pass 2 (one Q partial each)
 constexpr int kFineRows = 64;      // rows per work item of pass 1 (ranks <= 8)
-constexpr int kRows1Tiled = 128;   // rows per work item of pass 1 (ranks 16 and 32)
+constexpr int kRows1High = 128;   // rows per work item of pass 1 (ranks 16 and 32)
 constexpr int kFineRows3 = 32;     // rows per work item of pass 3 and the error views
 constexpr int kGsRows = 256;       // rows per work item of the Gram-Schmidt kernels
 
@@ -41,7 +41,7 @@ __host__ __device__ constexpr int ctile3_for(int rp) { return kThreads * cpt3_fo
 // for ranks up to 8; 512 columns (sixteen 32-column chunks) for ranks 16 and
 // 32, whose items are 128 rows tall.
 __host__ __device__ constexpr int ctile1_for(int rp) { return rp <= 8 ? 1024 : 512; }
-__host__ __device__ constexpr int rows1_for(int rp) { return rp <= 8 ? kFineRows : kRows1Tiled; }
+__host__ __device__ constexpr int rows1_for(int rp) { return rp <= 8 ? kFineRows : kRows1High; }
 
 struct TensorDesc {
   long long g_off;   // first element in the bucket

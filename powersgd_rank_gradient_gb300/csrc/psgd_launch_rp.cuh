@@ -2,10 +2,12 @@
 // kern_rp<RP>.cu, which instantiates them.
 #pragma once
 
+#include <algorithm>
+
 #include "psgd_gs.cuh"
 #include "psgd_kernels.cuh"
 #include "psgd_launch.h"
-#include "psgd_tiled.cuh"
+#include "psgd_mma.cuh"
 
 namespace psgd {
 
@@ -22,14 +24,14 @@ inline void by_gtype(int gtype, F&& f) {
 }
 
 template <int RP, typename GT>
-void launch_pass1_tiled(const StepArgs& a, int grid, cudaStream_t s) {
-  using T = Pass1Tiled<RP, GT>;
+void launch_pass1_mma(const StepArgs& a, int grid, cudaStream_t s) {
+  using T = Pass1Mma<RP, GT>;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(k_pass1_tiled<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+    cudaFuncSetAttribute(k_pass1_mma<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
     configured = true;
   }
-  if (a.vec_ok && a.has_aligned) k_pass1_tiled<RP, GT><<<grid, kThreads, T::SMEM, s>>>(a);
+  if (a.vec_ok && a.has_aligned) k_pass1_mma<RP, GT><<<grid, kThreads, T::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned) k_pass1_rest<RP, GT><<<grid * 2, kThreads, 0, s>>>(a);
 }
 
@@ -50,7 +52,7 @@ void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
 
 // grid = one CTA per SM; the kernels run MINB CTAs per SM.  Ranks up to 8 use
 // the chunk-stationary kernel (two CTAs per SM for W <= 2, one above); ranks
-// 16 and 32 the register-tiled kernel (one CTA per SM, any W).
+// 16 and 32 the tensor-core kernel (one CTA per SM, any W).
 template <int RP>
 void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
   by_gtype(a.gtype, [&](auto tag) {
@@ -64,7 +66,7 @@ void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
         default: k_pass1<RP, 0, GT, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
       }
     } else {
-      launch_pass1_tiled<RP, GT>(a, grid, s);
+      launch_pass1_mma<RP, GT>(a, grid, s);
     }
   });
 }
