@@ -101,6 +101,20 @@ void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q, int
 
 template <int RP>
 void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s) {
+  if constexpr (RP == 32) {
+    // the Mbar scratch, or the single replica's store half: tensor cores
+    // (at rank 16 the fp32 kernel is faster)
+    if (src_mode == 0 || (src_mode == 1 && a.W == 1)) {
+      using T = Pass2Mma<RP>;
+      static bool configured = false;
+      if (!configured) {
+        cudaFuncSetAttribute(k_pass2_mma<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+        configured = true;
+      }
+      k_pass2_mma<RP><<<std::min(a.n_items, (grid + 2) / 3), kThreads, T::SMEM, s>>>(a);
+      return;
+    }
+  }
   if (src_mode == 0) {
     k_pass2<RP, 0, float, 0><<<grid, kThreads, 0, s>>>(a);
   } else if (src_mode == 1) {

@@ -409,4 +409,133 @@ __global__ void __launch_bounds__(kThreads) k_pass1_rest(const StepArgs a) {
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
 }
 
+// ---------------------------------------------------------------------------
+// Pass 2 for padded rank 32 (16 compiles too; the fp32 kernel is faster
+// there) ("PowerSGD Hooks", powerSGD_hook steps 3.5-3.6, the replica mean
+// folded): the partial Q' = Mbar^T P of one row
+// block on the tensor cores, same items and partial layout (qpart[rb][k][j])
+// as k_pass2.  As an mma the product is D (columns x ranks) = A (columns x
+// rows) B (rows x ranks): warp w owns MB 16-column blocks of the item's tile
+// and all RP ranks, walking the rows 8 at a time.  Each warp streams its
+// columns of Mbar (the Mbar scratch, or the single replica's store half) into
+// a private ring of NS 8-row units with cp.async (row stride 16 MB + 8:
+// conflict-free fragment reads); P rows are staged per 128 rows in shared
+// memory (row stride RP + 8).  Sources have 16-byte aligned rows (stride ld),
+// so every tensor takes this path.
+// ---------------------------------------------------------------------------
+template <int RP>
+struct Pass2Mma {
+  static constexpr int NR = RP / 8;                 // rank blocks
+  static constexpr int MB = RP == 32 ? 2 : 4;       // 16-column blocks per warp
+  static constexpr int WC = 16 * MB;                // columns per warp
+  static constexpr int AS = WC + 8;                 // staged row stride (floats)
+  static constexpr int UNIT = 8 * AS * 4;           // one 8-row unit of a warp
+  static constexpr int NS = RP == 32 ? 12 : 8;      // units in a warp's ring
+  static constexpr int PS = RP + 8;                 // staged P row stride
+  static constexpr int SMEM = 8 * NS * UNIT + kPStage * PS * 4;
+  static_assert(8 * WC == ctile_for(RP), "the 8 warps cover the column tile");
+};
+
+template <int RP>
+__global__ void __launch_bounds__(kThreads, 1) k_pass2_mma(const StepArgs a) {
+  using T = Pass2Mma<RP>;
+  constexpr int NR = T::NR, MB = T::MB, NS = T::NS, AS = T::AS, PS = T::PS;
+  extern __shared__ __align__(128) char p2m_smem[];
+  if (a.ctrl->flag) return;
+  const int nxt = a.ctrl->cur ^ 1;
+  const float* P = a.Pf + (long long)nxt * a.p_total;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  char* const ring = p2m_smem + warp * NS * T::UNIT;
+  float* const ps = reinterpret_cast<float*>(p2m_smem + 8 * NS * T::UNIT);
+  // mbar scratch, or (one replica) the store half pass 1 just wrote
+  const float* srcb = a.mbar ? a.mbar : a.estore + (long long)nxt * a.nc_pad;
+  for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+    const Item item = a.items[it];
+    const TensorDesc td = a.tensors[item.t];
+    const long long ld = td.ld;
+    const int cend = item.col0 + item.ncols;
+    const int wc0 = item.col0 + warp * T::WC;
+    const float* src = srcb + td.c_off;
+    const int nunits = (item.nrows + 7) / 8;
+    // unit u: rows row0 + 8u .. + 7 of this warp's columns, WC / 4 pieces a row
+    auto issue = [&](int u) {
+      if (u < nunits) {
+        char* dst = ring + (u % NS) * T::UNIT;
+#pragma unroll
+        for (int j = 0; j < 8 * (T::WC / 4) / 32; ++j) {
+          const int pc = lane + 32 * j, row = pc / (T::WC / 4), q = pc % (T::WC / 4);
+          const int rr = item.row0 + 8 * u + row, col = wc0 + 4 * q;
+          const bool v = rr < item.row0 + item.nrows && col < cend;
+          cp_async16_z(dst + (row * AS + 4 * q) * 4, src + (v ? (long long)rr * ld + col : 0), v);
+        }
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int u = 0; u < NS - 1; ++u) issue(u);
+    float acc[MB][NR][4];
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+      for (int nr = 0; nr < NR; ++nr) acc[mb][nr][0] = acc[mb][nr][1] = acc[mb][nr][2] = acc[mb][nr][3] = 0.f;
+    for (int u = 0; u < nunits; ++u) {
+      const int ks = (8 * u) % kPStage;             // row of the unit in the staged P block
+      if (ks == 0) {
+        __syncthreads();
+        const int sb = 8 * u, rows = min(kPStage, item.nrows - sb);
+        for (int idx = threadIdx.x; idx < kPStage * RP; idx += kThreads) {
+          const int rr = idx / RP, k = idx - rr * RP;
+          ps[rr * PS + k] = rr < rows ? P[td.p_off + (long long)(item.row0 + sb + rr) * RP + k] : 0.f;
+        }
+        __syncthreads();
+      }
+      cp_async_wait<NS - 2>();
+      __syncwarp();
+      const float* ar = reinterpret_cast<const float*>(ring + (u % NS) * T::UNIT);
+      uint32_t bh[NR][2], bl[NR][2];
+#pragma unroll
+      for (int nr = 0; nr < NR; ++nr) {
+        split_tf32(ps[(ks + c) * PS + nr * 8 + g], bh[nr][0], bl[nr][0]);
+        split_tf32(ps[(ks + c + 4) * PS + nr * 8 + g], bh[nr][1], bl[nr][1]);
+      }
+#pragma unroll
+      for (int mb = 0; mb < MB; ++mb) {
+        // A[m = column][k = row]: a0 (j, r), a1 (j + 8, r), a2 (j, r + 4), a3 (j + 8, r + 4)
+        uint32_t ah[4], al[4];
+        split_tf32(ar[c * AS + mb * 16 + g], ah[0], al[0]);
+        split_tf32(ar[c * AS + mb * 16 + g + 8], ah[1], al[1]);
+        split_tf32(ar[(c + 4) * AS + mb * 16 + g], ah[2], al[2]);
+        split_tf32(ar[(c + 4) * AS + mb * 16 + g + 8], ah[3], al[3]);
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr) mma_tf32(acc[mb][nr], al, bh[nr][0], bh[nr][1]);
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr) mma_tf32(acc[mb][nr], ah, bl[nr][0], bl[nr][1]);
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr) mma_tf32(acc[mb][nr], ah, bh[nr][0], bh[nr][1]);
+      }
+      __syncwarp();                                  // the unit's slot is refilled next
+      issue(u + NS - 1);
+    }
+    cp_async_wait<0>();
+    // D[j][k]: d0 (j = g, k = 2c), d1 (g, 2c + 1), d2 (g + 8, 2c), d3 (g + 8, 2c + 1)
+    float* dst = a.qpart + td.qp_off + (long long)item.rb * RP * td.m;
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb) {
+      const int j = wc0 + mb * 16 + g;
+#pragma unroll
+      for (int nr = 0; nr < NR; ++nr) {
+        const long long k = nr * 8 + 2 * c;
+        if (j < cend) {
+          dst[k * td.m + j] = acc[mb][nr][0];
+          dst[(k + 1) * td.m + j] = acc[mb][nr][1];
+        }
+        if (j + 8 < cend) {
+          dst[k * td.m + j + 8] = acc[mb][nr][2];
+          dst[(k + 1) * td.m + j + 8] = acc[mb][nr][3];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace psgd
