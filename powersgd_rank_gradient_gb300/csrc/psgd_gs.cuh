@@ -14,11 +14,12 @@ namespace psgd {
 // State" item 4 adds epsilon to each column norm.  Every Gram-Schmidt
 // operation is a column operation, so the result is X T for an RP x RP upper
 // triangular T that depends only on the Gram matrix G = X^T X.  The stage
-// therefore (1) reduces G over row blocks in fp64 (k_gram), (2) runs modified
-// Gram-Schmidt with epsilon symbolically on G to get T (k_solve, one CTA per
-// tensor, fp64), (3) applies X T (k_apply).  It runs twice (the second sweep
-// re-orthogonalises the first sweep's output), which keeps P^T P = I to fp32
-// rounding even when X is ill conditioned.
+// therefore (1) forms G per row block (k_gram) and adds the blocks per tensor
+// (k_gram_sum), (2) runs modified Gram-Schmidt with epsilon symbolically on G
+// to get T (k_solve, one CTA per tensor), (3) applies X T (k_apply), all
+// sums and the recurrence in double-float arithmetic on the fp32 pipes.  It
+// runs twice (the second sweep re-orthogonalises the first sweep's output),
+// which keeps P^T P = I to fp32 rounding even when X is ill conditioned.
 // ---------------------------------------------------------------------------
 // P_raw = sum of pass 1's column-tile partials, in tile order (the Gram stage
 // then reads dense rows).  Each work item is a chunk of one tensor's rows x RP
