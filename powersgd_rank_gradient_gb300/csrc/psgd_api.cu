@@ -522,7 +522,7 @@ struct Ops {
     launch_gram_sum<RP>(a, is_q, L.st);
     L.end();
     L.begin(K_SOLVE);
-    launch_solve<RP>(a, s->gram_t, is_q, L.st);
+    launch_solve<RP>(a, s->gram_t, is_q, 0, L.st);
     L.end();
     L.begin(K_APPLY);
     launch_apply<RP>(a, src_dense, s->pgs, is_q, -1, grid, L.st);
@@ -532,7 +532,7 @@ struct Ops {
     launch_gram_sum<RP>(a, is_q, L.st);
     L.end();
     L.begin(K_SOLVE);
-    launch_solve<RP>(a, s->gram_t, is_q, L.st);
+    launch_solve<RP>(a, s->gram_t, is_q, 1, L.st);
     L.end();
     L.begin(K_APPLY);
     if (is_q)

@@ -249,6 +249,10 @@ __device__ __forceinline__ Dd dd_gs_scale(Dd nn, float eps) {
   return dd_add(z, dd_mul(z, r));
 }
 
+// Largest deviation of the first sweep's Gram matrix from I for which the
+// second sweep is skipped (its T would differ from I by about as much).
+constexpr float kGsSkip = 1e-5f;
+
 // One CTA per tensor, on the tensor's Gram matrix G (k_gram_sum): modified
 // Gram-Schmidt with epsilon on the coefficient matrix T (X_out = X T), in
 // double-float with T and H = G T in shared memory.  Step i, with t_i still
@@ -259,10 +263,11 @@ __device__ __forceinline__ Dd dd_gs_scale(Dd nn, float eps) {
 // Ranks up to 8 run the steps on one warp (__syncwarp between steps), 16 and
 // 32 on the CTA (__syncthreads), the work of a step spread over its threads.
 // The column scalings are applied to T at the end (t_i is not read again
-// after its own step).
+// after its own step).  `sweep` is 0 for the first sweep and 1 for the
+// re-orthogonalising one.
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const float2* __restrict__ gram_in,
-                                                    int is_q, int only_init) {
+                                                    int is_q, int sweep) {
   constexpr int ENT = RP * RP;
   constexpr int LD = RP + 1;                                // padded column stride
   // the steps run on one warp for ranks up to 8 and on the CTA above, thread
@@ -279,12 +284,33 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const floa
   const TensorDesc td = a.tensors[t];
   const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
   if (count == 0) return;
+  __shared__ float devw[kThreads / 32];
+  float dev = 0.f;   // max |G - I| over the rank's block
   for (int idx = threadIdx.x; idx < ENT; idx += kThreads) {
     const int k = idx / RP, j = idx % RP;   // G is symmetric: entry (k, j)
     H[j * LD + k] = dd_of(gram_in[(long long)t * ENT + idx]);
     T[j * LD + k] = {(k == j && j < td.r) ? 1.f : 0.f, 0.f};
+    if (k < td.r && j < td.r) dev = fmaxf(dev, fabsf(H[j * LD + k].hi - (k == j ? 1.f : 0.f)));
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, o));
+  if ((threadIdx.x & 31) == 0) devw[threadIdx.x >> 5] = dev;
   __syncthreads();
+  // the second sweep re-orthogonalises only what the first left off: when
+  // the first sweep's output is already orthonormal to kGsSkip, its T is I
+  if (sweep == 1) {
+    float dmax = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) dmax = fmaxf(dmax, devw[w]);
+    if (dmax <= kGsSkip) {
+      float* Tout = a.tmat + (long long)t * RP * RP;
+      for (int idx = threadIdx.x; idx < ENT; idx += kThreads) {
+        const int k = idx / RP, jj = idx % RP;
+        Tout[idx] = (k == jj && jj < td.r) ? 1.f : 0.f;
+      }
+      return;
+    }
+  }
   if (threadIdx.x >= TEAM) return;
   const int r = td.r;
   const int lane = threadIdx.x & 31;

@@ -14,7 +14,7 @@ template <int RP> void launch_psum(const StepArgs& a, int grid, cudaStream_t s);
 template <int RP> void launch_gram(const StepArgs& a, const float* src, float* dense_out, int is_q,
                                    int from_parts, float2* gram, int grid, cudaStream_t s);
 template <int RP> void launch_gram_sum(const StepArgs& a, int is_q, cudaStream_t s);
-template <int RP> void launch_solve(const StepArgs& a, const float2* gram, int is_q, cudaStream_t s);
+template <int RP> void launch_solve(const StepArgs& a, const float2* gram, int is_q, int sweep, cudaStream_t s);
 template <int RP> void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q,
                                     int dst_half, int grid, cudaStream_t s);
 template <int RP> void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s);

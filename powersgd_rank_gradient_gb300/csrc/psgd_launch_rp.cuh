@@ -89,8 +89,8 @@ void launch_gram_sum(const StepArgs& a, int is_q, cudaStream_t s) {
 }
 
 template <int RP>
-void launch_solve(const StepArgs& a, const float2* gram, int is_q, cudaStream_t s) {
-  k_solve<RP><<<a.n_tensors, kThreads, 0, s>>>(a, gram, is_q, 0);
+void launch_solve(const StepArgs& a, const float2* gram, int is_q, int sweep, cudaStream_t s) {
+  k_solve<RP><<<a.n_tensors, kThreads, 0, s>>>(a, gram, is_q, sweep);
 }
 
 template <int RP>
@@ -160,7 +160,7 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
   template void launch_gram<RPV>(const StepArgs&, const float*, float*, int, int, float2*, int, \
                                  cudaStream_t);                                                 \
   template void launch_gram_sum<RPV>(const StepArgs&, int, cudaStream_t);                      \
-  template void launch_solve<RPV>(const StepArgs&, const float2*, int, cudaStream_t);           \
+  template void launch_solve<RPV>(const StepArgs&, const float2*, int, int, cudaStream_t);      \
   template void launch_apply<RPV>(const StepArgs&, const float*, float*, int, int, int,         \
                                   cudaStream_t);                                                \
   template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
