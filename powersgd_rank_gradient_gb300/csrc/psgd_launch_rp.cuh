@@ -31,7 +31,7 @@ void launch_pass1_mma(const StepArgs& a, int grid, cudaStream_t s) {
     cudaFuncSetAttribute(k_pass1_mma<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
     configured = true;
   }
-  if (a.vec_ok && a.has_aligned) k_pass1_mma<RP, GT><<<grid, kThreads, T::SMEM, s>>>(a);
+  if (a.vec_ok && a.has_aligned) k_pass1_mma<RP, GT><<<grid, kThreads1M, T::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned) k_pass1_rest<RP, GT><<<grid * 2, kThreads, 0, s>>>(a);
 }
 

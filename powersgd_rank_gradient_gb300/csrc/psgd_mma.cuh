@@ -113,55 +113,64 @@ __device__ __forceinline__ void mma_pq(const uint32_t (&ahi)[RP / 8][4], const u
 
 // ---------------------------------------------------------------------------
 // The kernel.  Work item: 128 rows x 512 columns of one tensor, walked in
-// 32-column chunks; one CTA (8 warps) per SM over a persistent item list.
+// 32-column chunks; one CTA (16 warps) per SM over a persistent item list.
 // Sources are staged with cp.async, S - 1 (chunk, replica) units ahead,
 // continuing across items; the Q chunks (shared by the CTA) rotate through
-// SQ buffers, published by one CTA barrier per chunk.  Warp w owns rows
-// 16 w .. 16 w + 15 of the item:
-//   correction  P_old (16 x RP, split once per item) x Q_old chunk^T, four
-//               8-column blocks as four accumulator chains (mma_pq).  Pass 3
+// SQ buffers, published by one CTA barrier per chunk.  Warps 2b and 2b + 1
+// own rows 16 b .. 16 b + 15 of the item, each one 16-column half of the
+// chunk (their partial P are added at the end of the item):
+//   correction  P_old (16 x RP, split once per item) x Q_old chunk^T, two
+//               8-column blocks as two accumulator chains (mma_pq).  Pass 3
 //               writes out with the fp32 chain of dot_chain, so here the
 //               residual store - P_old Q_old^T differs from fl(M_w - out) by
 //               the difference of the two roundings of P_old Q_old^T (about
 //               2^-20 of the products' magnitude);
 //   M_w, Mbar   in the accumulator layout: lane (g, c) holds rows g, g + 8
 //               and columns 8 n + 2c, 8 n + 2c + 1 of block n;
-//   projection  P_raw (16 x RP) += Mbar chunk (16 x 32) Q chunk (32 x RP):
+//   projection  P_raw (16 x RP) += Mbar half (16 x 16) Q half (16 x RP):
 //               the Mbar values a lane holds are its A fragment when k slot c
 //               of a block stands for column 2c and slot c + 4 for 2c + 1,
 //               and Q's B fragment takes the same column order.
-// Staging: each warp copies its own 16 rows of every source into its region
-// (row stride 40 floats for fp32, 20 words for 16-bit gradients: conflict-free
-// fragment reads), so only the warp synchronises on them; the Q chunks
-// (k-major, row stride 40) are shared, behind the chunk barrier.
+// Staging: each warp copies its own 16 rows x 16 columns of every source into
+// its region (row stride 24 floats for fp32, 12 words for 16-bit gradients:
+// conflict-free fragment reads), so only the warp synchronises on them; the Q
+// chunks (k-major, row stride 40) are shared, behind the chunk barrier.
 // ---------------------------------------------------------------------------
+constexpr int kThreads1M = 512;   // threads of the tensor-core pass 1 (16 warps)
+
 template <int RP, typename GT>
 struct Pass1Mma {
   static_assert(RP == 16 || RP == 32, "tensor-core pass 1 is for ranks 16 and 32");
-  static constexpr int TR = kRows1High;                       // rows per item (8 warps x 16)
-  static constexpr int CC = 32;                                // columns per chunk
-  static constexpr int GS = sizeof(GT) == 4 ? 40 : 20;         // gradient row stride, 32-bit words
+  static constexpr int NW = kThreads1M / 32;                   // warps
+  static constexpr int TR = kRows1High;                        // rows per item (8 row blocks x 16)
+  static constexpr int CC = 32;                                // columns per chunk (2 halves x 16)
+  static constexpr int GS = sizeof(GT) == 4 ? 24 : 12;         // gradient row stride, 32-bit words
   static constexpr int PB = 4 * (int)sizeof(GT);               // bytes of a 4-column piece
-  static constexpr int ES = 40;                                // store row stride, floats
+  static constexpr int ES = 24;                                // store row stride, floats
   static constexpr int WG_BYTES = 16 * GS * 4;                 // a warp's gradient region
   static constexpr int WE_BYTES = 16 * ES * 4;                 // a warp's store region
-  static constexpr int UNIT_BYTES = 8 * (WG_BYTES + WE_BYTES);
-  static constexpr int S = 4;
+  static constexpr int UNIT_BYTES = NW * (WG_BYTES + WE_BYTES);
+  static constexpr int S = (RP == 32 && sizeof(GT) == 4) ? 3 : 4;   // within 227 KB
   static constexpr int SQ = S;
   static constexpr int QS = 40;                                // Q chunk row stride
   static constexpr int QCH_BYTES = RP * QS * 4;
-  static constexpr int SMEM = S * UNIT_BYTES + 2 * SQ * QCH_BYTES;
-  static_assert(TR == 16 * (kThreads / 32), "one 16-row block per warp");
+  static constexpr int XCH_BYTES = (NW / 2) * 32 * (RP / 2) * 4;   // item-end exchange of the halves
+  static constexpr int SMEM = S * UNIT_BYTES + 2 * SQ * QCH_BYTES + XCH_BYTES;
+  static_assert(TR == 16 * (NW / 2), "one 16-row block per warp pair");
+  static_assert(RP * 8 <= kThreads1M, "one Q piece per thread");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 template <int RP, typename GT>
-__global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
+__global__ void __launch_bounds__(kThreads1M, 1) k_pass1_mma(const StepArgs a) {
   using T = Pass1Mma<RP, GT>;
   constexpr int S = T::S, SQ = T::SQ, NR = RP / 8;
   extern __shared__ __align__(128) char p1m_smem[];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, g = lane >> 2, c = lane & 3;
+  const int rb = warp >> 1, hf = warp & 1;                     // row block, column half
   char* const wsm = p1m_smem + warp * (T::WG_BYTES + T::WE_BYTES);   // + slot * UNIT_BYTES
   char* const qsm = p1m_smem + S * T::UNIT_BYTES;
+  float* const xch = reinterpret_cast<float*>(qsm + 2 * SQ * T::QCH_BYTES);
 
   const int cur = a.ctrl->cur, nxt = cur ^ 1;
   const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
@@ -187,14 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
       char* reg = wsm + i_slot * T::UNIT_BYTES;
       const long long m = i_td.m, ld = i_td.ld;
       const int cend = i_item.col0 + i_item.ncols;
-      const int cc0 = i_item.col0 + i_ch * T::CC;
-      const long long rbase = (long long)i_item.row0 + warp * 16;
-      const int rlim = i_item.nrows - warp * 16;       // rows of this warp in the item
+      const int cc0 = i_item.col0 + i_ch * T::CC + 16 * hf;
+      const long long rbase = (long long)i_item.row0 + rb * 16;
+      const int rlim = i_item.nrows - rb * 16;       // rows of this warp in the item
       const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[i_w]) + i_td.g_off;
-      // 16 rows x 8 pieces of 4 columns (16 bytes fp32, 8 bytes 16-bit)
+      // 16 rows x 4 pieces of 4 columns (16 bytes fp32, 8 bytes 16-bit)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int pc = lane + 32 * j, row = pc >> 3, q = pc & 7;
+      for (int j = 0; j < 2; ++j) {
+        const int pc = lane + 32 * j, row = pc >> 2, q = pc & 3;
         const int col = cc0 + q * 4;
         const bool v = row < rlim && col < cend;
         const GT* src = gsrc + (v ? (rbase + row) * m + col : 0);
@@ -204,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
       if (ef) {
         const float* esrc = a.estore + ecur + (long long)i_w * a.nc_pad + i_td.c_off;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int pc = lane + 32 * j, row = pc >> 3, q = pc & 7;
+        for (int j = 0; j < 2; ++j) {
+          const int pc = lane + 32 * j, row = pc >> 2, q = pc & 3;
           const int col = cc0 + q * 4;
           const bool v = row < rlim && col < cend;
           cp_async16_z(reg + T::WG_BYTES + row * T::ES * 4 + q * 16, esrc + (v ? (rbase + row) * ld + col : 0), v);
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
       }
       if (i_w == 0 && t < RP * 8) {
         const int k = t >> 3, q = t & 7;
-        const int col = cc0 + q * 4;
+        const int col = i_item.col0 + i_ch * T::CC + q * 4;
         const bool v = col < cend;
         const long long off = i_td.q_off + (long long)k * m + (v ? col : 0);
         char* dst = qsm + (i_cs % SQ) * 2 * T::QCH_BYTES + (k * T::QS + q * 4) * 4;
@@ -243,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
   TensorDesc td;
   bool c_ok = tiled_item(a, c_it, item, td);
   if (c_ok) c_nch = (item.ncols + T::CC - 1) / T::CC;
-  uint32_t phi[NR][4], plo[NR][4];      // P_old rows of this warp, split
-  float corr[4][4], mb[4][4], pacc[NR][4];
+  uint32_t phi[NR][4], plo[NR][4];      // P_old rows of this warp's row block, split
+  float corr[2][4], mb[2][4], pacc[NR][4];
 #pragma unroll
   for (int n = 0; n < NR; ++n) pacc[n][0] = pacc[n][1] = pacc[n][2] = pacc[n][3] = 0.f;
   float chk = 0.f;
@@ -254,33 +263,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
     if (c_w == 0) __syncthreads();
     else __syncwarp();
     issue();
-    const long long m = td.m, ld = td.ld;
+    const long long ld = td.ld;
     const int cend = item.col0 + item.ncols;
-    const int cc0 = item.col0 + c_ch * T::CC;
-    const long long r0 = (long long)item.row0 + warp * 16;
+    const int cc0 = item.col0 + c_ch * T::CC + 16 * hf;     // this warp's 16 columns
+    const long long r0 = (long long)item.row0 + rb * 16;
     const char* qbuf = qsm + (c_cs % SQ) * 2 * T::QCH_BYTES;
     const float* qcs = reinterpret_cast<const float*>(qbuf);
     if (c_w == 0) {
       if (c_ch == 0) {
-        va = warp * 16 + g < item.nrows;
-        vb = warp * 16 + g + 8 < item.nrows;
+        va = rb * 16 + g < item.nrows;
+        vb = rb * 16 + g + 8 < item.nrows;
         if (ef) load_afrag<RP>(Pc + td.p_off, r0, va, vb, phi, plo);
       }
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
+      for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) { corr[n][e] = 0.f; mb[n][e] = 0.f; }
       if (ef) {
-        // B fragment of block n: Q_old(col 8 n + g, rank 8 ks + c (+ 4))
-        float qb[4][NR][2];
+        // B fragment of block n: Q_old(col 16 hf + 8 n + g, rank 8 ks + c (+ 4))
+        float qb[2][NR][2];
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+        for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int ks = 0; ks < NR; ++ks) {
-            qb[n][ks][0] = qcs[(ks * 8 + c) * T::QS + n * 8 + g];
-            qb[n][ks][1] = qcs[(ks * 8 + c + 4) * T::QS + n * 8 + g];
+            qb[n][ks][0] = qcs[(ks * 8 + c) * T::QS + 16 * hf + n * 8 + g];
+            qb[n][ks][1] = qcs[(ks * 8 + c + 4) * T::QS + 16 * hf + n * 8 + g];
           }
-        mma_pq<RP, 4>(phi, plo, qb, corr);
+        mma_pq<RP, 2>(phi, plo, qb, corr);
       }
     }
     // M_w of this replica in the accumulator layout
@@ -288,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
       const char* reg = wsm + c_slot * T::UNIT_BYTES;
       float* enxt = a.estore + enx + (long long)c_w * a.nc_pad + td.c_off;
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
+      for (int n = 0; n < 2; ++n) {
         const int col = cc0 + n * 8 + 2 * c;
         const bool cv = col < cend;
 #pragma unroll
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
     if (c_w == W - 1) {
       const float* qps = qcs + pq * (T::QCH_BYTES / 4);
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
+      for (int n = 0; n < 2; ++n) {
         const int col = cc0 + n * 8 + 2 * c;
         const bool cv = col < cend;
 #pragma unroll
@@ -338,10 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
           if (vb) st_stream2(mrow + (r0 + g + 8) * ld, mb[n][2], mb[n][3]);
         }
       }
-      // projection: k step n = chunk columns 8 n .. 8 n + 7, slot c <-> 2c,
-      // slot c + 4 <-> 2c + 1; rank block nr: B = Q_p(rank 8 nr + g, those columns)
+      // projection over this warp's 16 columns: k step n = columns 8 n ..
+      // 8 n + 7 of the half, slot c <-> 2c, slot c + 4 <-> 2c + 1; rank
+      // block nr: B = Q_p(rank 8 nr + g, those columns)
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
+      for (int n = 0; n < 2; ++n) {
         uint32_t ahi[4], alo[4];
         split_tf32(mb[n][0], ahi[0], alo[0]);
         split_tf32(mb[n][2], ahi[1], alo[1]);
@@ -350,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
         uint32_t bh[NR][2], bl[NR][2];
 #pragma unroll
         for (int nr = 0; nr < NR; ++nr) {
-          const float2 x = *reinterpret_cast<const float2*>(qps + (nr * 8 + g) * T::QS + n * 8 + 2 * c);
+          const float2 x = *reinterpret_cast<const float2*>(qps + (nr * 8 + g) * T::QS + 16 * hf + n * 8 + 2 * c);
           split_tf32(x.x, bh[nr][0], bl[nr][0]);
           split_tf32(x.y, bh[nr][1], bl[nr][1]);
         }
@@ -362,16 +372,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_pass1_mma(const StepArgs a) {
         for (int nr = 0; nr < NR; ++nr) mma_tf32(pacc[nr], ahi, bh[nr][0], bh[nr][1]);
       }
       if (c_ch == c_nch - 1) {
-        // end of the item: this warp's 16 rows of the partial P
+        // end of the item: the two halves' partial P of the row block are
+        // added (second half's values through shared memory) and written
+        float* xw = xch + (rb * 32 + lane) * (RP / 2);
+        if (hf == 1) {
 #pragma unroll
-        for (int nr = 0; nr < NR; ++nr) {
+          for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) chk = fmaf(pacc[nr][e], 0.f, chk);
-          float* dst = a.praw_part + td.pp_off + ((long long)item.ct * td.n + r0 + g) * RP + nr * 8 + 2 * c;
-          if (va) *reinterpret_cast<float2*>(dst) = make_float2(pacc[nr][0], pacc[nr][1]);
-          if (vb) *reinterpret_cast<float2*>(dst + 8 * RP) = make_float2(pacc[nr][2], pacc[nr][3]);
-          pacc[nr][0] = pacc[nr][1] = pacc[nr][2] = pacc[nr][3] = 0.f;
+            for (int e = 0; e < 4; ++e) xw[nr * 4 + e] = pacc[nr][e];
         }
+        __syncthreads();
+        if (hf == 0) {
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pacc[nr][e] += xw[nr * 4 + e];
+              chk = fmaf(pacc[nr][e], 0.f, chk);
+            }
+            float* dst = a.praw_part + td.pp_off + ((long long)item.ct * td.n + r0 + g) * RP + nr * 8 + 2 * c;
+            if (va) *reinterpret_cast<float2*>(dst) = make_float2(pacc[nr][0], pacc[nr][1]);
+            if (vb) *reinterpret_cast<float2*>(dst + 8 * RP) = make_float2(pacc[nr][2], pacc[nr][3]);
+          }
+        } else {
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) chk = fmaf(pacc[nr][e], 0.f, chk);
+        }
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr) pacc[nr][0] = pacc[nr][1] = pacc[nr][2] = pacc[nr][3] = 0.f;
       }
     }
     c_slot = (c_slot + 1 == S) ? 0 : c_slot + 1;

@@ -209,6 +209,37 @@ def test_fp16_scaled_with_inf_is_skipped():
     pair.close()
 
 
+@pytest.mark.parametrize("rank", [16, 32])
+def test_fp16_scaled_with_inf_high_ranks(rank):
+    """The tensor-core pass 1 on fp16 gradients pre-scaled by 65536: unscaled
+    in the pass, a step with one +inf is skipped with the state left bit for
+    bit, the next clean step matches the oracle."""
+    world = 2
+    pair = Pair(ALIGNED, world, rank, DEV, grad_dtype=torch.float16, start_powerSGD_iter=0,
+                min_compression_rate=0.25)
+    s = 1.0 / 65536.0
+    g0 = grads_for(ALIGNED, world, 0, std=1e-3, dtype=np.float16, scale=65536.0)
+    skipped, status, out, exp = pair.step(g0, inv_loss_scale=s)
+    assert not skipped
+    pair.compare(out, exp, label=f"fp16 r={rank} step 0")
+    before = ([pair.gpu.get_error(w).cpu().clone() for w in range(world)],
+              [pair.gpu.get_q(t).clone() for t in (0, 3)], [pair.gpu.get_p(t).clone() for t in (0, 3)])
+    g1 = grads_for(ALIGNED, world, 1, std=1e-3, dtype=np.float16, scale=65536.0)
+    g1[0][7] = np.float16(np.inf)   # inside the first (aligned, compressed) tensor
+    skipped, status, out, exp = pair.step(g1, inv_loss_scale=s)
+    assert skipped and status == "skipped"
+    after = ([pair.gpu.get_error(w).cpu() for w in range(world)],
+             [pair.gpu.get_q(t) for t in (0, 3)], [pair.gpu.get_p(t) for t in (0, 3)])
+    for xs, ys in zip(before, after):
+        for x, y in zip(xs, ys):
+            assert torch.equal(x, y)
+    g2 = grads_for(ALIGNED, world, 2, std=1e-3, dtype=np.float16, scale=65536.0)
+    skipped, status, out, exp = pair.step(g2, inv_loss_scale=s)
+    assert not skipped
+    pair.compare(out, exp, label=f"fp16 r={rank} step 2")
+    pair.close()
+
+
 def test_nan_in_fp32_is_skipped():
     shapes = [(300, 200), (7,)]
     pair = Pair(shapes, 2, 2, DEV, start_powerSGD_iter=0, min_compression_rate=1.0)
