@@ -124,13 +124,15 @@ def load_peaks():
 
 
 def kernel_src_hash():
-    """Hash of the sources the streaming passes (passes 1-3) are compiled
-    from: their device code, tiling constants and launchers.  Host code and
-    the other kernels do not change the captured kernels' counters."""
+    """Hash of the sources the captured pass kernels (the chunk-stationary
+    pass 1 of ranks up to 8, passes 2 and 3) are compiled from: their device
+    code, tiling constants and launchers.  Host code and the other kernels
+    (the Gram-Schmidt stage, the rank-16/32 tensor-core kernels) do not change
+    their counters."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "powersgd_rank_gradient_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if not (f in ("psgd_kernels.cuh", "psgd_mma.cuh", "psgd_internal.h", "psgd_launch_rp.cuh")
+        if not (f in ("psgd_kernels.cuh", "psgd_internal.h", "psgd_launch_rp.cuh")
                 or (f.startswith("kern_rp") and f.endswith(".cu"))):
             continue
         with open(os.path.join(csrc, f), "rb") as fh:
