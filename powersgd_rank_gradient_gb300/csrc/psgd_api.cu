@@ -397,7 +397,16 @@ void build_plan(psgd_state* s) {
   };
   make_items(&s->items, s->row_block, CT, false);
   make_items(&s->fitems, kFineRows3, ctile3_for(RP), true);
-  make_items(&s->p1items, rows1_for(RP), CT1, true);
+  // pass 1: half-height items for small buckets (fewer than six items per
+  // SM at full height), so that the last wave over the SMs is short
+  int rows1 = rows1_for(RP);
+  {
+    long long nc = 0;
+    for (auto& h : s->tensors)
+      if (h.compressed) nc += h.numel;
+    if (RP <= 8 && nc < 6LL * s->sms * rows1 * CT1) rows1 /= 2;
+  }
+  make_items(&s->p1items, rows1, CT1, true);
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const long long len = (long long)s->cdesc[c].m * RP;
     for (long long f = 0; f < len; f += 1024)
