@@ -1,6 +1,8 @@
-// Gram-Schmidt stage of the PowerSGD hook step (P and the fresh Q), templated
-// on the padded rank RP.  Kept apart from the streaming passes
-// (psgd_kernels.cuh) so that the two evolve separately.
+// Gram-Schmidt stage of the PowerSGD hook step (P and the fresh Q), and the
+// reductions of the streaming passes' partial sums (k_psum for pass 1's P,
+// k_qreduce for pass 2's Q), templated on the padded rank RP.  Kept apart
+// from the streaming passes (psgd_kernels.cuh) so that the two evolve
+// separately.
 #pragma once
 
 #include "psgd_kernels.cuh"
@@ -54,6 +56,46 @@ __global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
         float v = 0.f;
         for (int c = 0; c < td.ctiles1; ++c) v += src[(long long)c * len + e];
         a.praw[td.p_off + e] = v;
+      }
+    }
+  }
+}
+
+// Q'(j, k) = sum over row blocks of the partials, in row-block order, written
+// k-major into the next half of Qf.  Each work item is a chunk of one
+// tensor's RP * m values, four per thread.
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
+  if (a.ctrl->flag) return;
+  float* Q = a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
+  for (int it = blockIdx.x; it < a.n_qr; it += gridDim.x) {
+    const GsItem gi = a.qr_items[it];
+    const TensorDesc td = a.tensors[gi.t];
+    const long long len = (long long)RP * td.m;
+    const float* src = a.qpart + td.qp_off;
+    const int f = gi.row0 + threadIdx.x * 4;
+    if (f >= gi.row0 + gi.nrows) continue;
+    if (len % 4 == 0) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      int b = 0;
+      // eight row blocks' loads in flight, added in row-block order
+      for (; b + 8 <= td.rblocks; b += 8) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = ld_stream4(src + (long long)(b + u) * len + f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) { s.x += x[u].x; s.y += x[u].y; s.z += x[u].z; s.w += x[u].w; }
+      }
+      for (; b < td.rblocks; ++b) {
+        float4 x = ld_stream4(src + (long long)b * len + f);
+        s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
+      }
+      *reinterpret_cast<float4*>(Q + td.q_off + f) = s;
+    } else {
+      for (int e = f; e < min(f + 4, gi.row0 + gi.nrows); ++e) {
+        float s = 0.f;
+        for (int b = 0; b < td.rblocks; ++b) s += src[(long long)b * len + e];
+        Q[td.q_off + e] = s;
       }
     }
   }

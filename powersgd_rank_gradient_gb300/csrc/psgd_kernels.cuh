@@ -907,45 +907,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_pass2(const StepArgs a) {
   }
 }
 
-// Q'(j, k) = sum over row blocks of the partials, in row-block order, written
-// k-major into the next half of Qf.  Each work item is a chunk of one
-// tensor's RP * m values, four per thread.
-template <int RP>
-__global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
-  if (a.ctrl->flag) return;
-  float* Q = a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
-  for (int it = blockIdx.x; it < a.n_qr; it += gridDim.x) {
-    const GsItem gi = a.qr_items[it];
-    const TensorDesc td = a.tensors[gi.t];
-    const long long len = (long long)RP * td.m;
-    const float* src = a.qpart + td.qp_off;
-    const int f = gi.row0 + threadIdx.x * 4;
-    if (f >= gi.row0 + gi.nrows) continue;
-    if (len % 4 == 0) {
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      int b = 0;
-      for (; b + 4 <= td.rblocks; b += 4) {
-        float4 x[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) x[u] = ld_stream4(src + (long long)(b + u) * len + f);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) { s.x += x[u].x; s.y += x[u].y; s.z += x[u].z; s.w += x[u].w; }
-      }
-      for (; b < td.rblocks; ++b) {
-        float4 x = ld_stream4(src + (long long)b * len + f);
-        s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
-      }
-      *reinterpret_cast<float4*>(Q + td.q_off + f) = s;
-    } else {
-      for (int e = f; e < min(f + 4, gi.row0 + gi.nrows); ++e) {
-        float s = 0.f;
-        for (int b = 0; b < td.rblocks; ++b) s += src[(long long)b * len + e];
-        Q[td.q_off + e] = s;
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Pass 3: out = P Q'^T.  Each thread keeps its CPT3 columns of Q' in registers.
 // MODE 0: write out (bucket layout).  MODE 1: materialise replica `a.replica`'s
