@@ -152,6 +152,7 @@ struct psgd_state {
   long long p_total = 0, q_total = 0, pp_total = 0, qp_total = 0;
   int pass2_src = 0;  // 0 mbar scratch, 1 error store, 2 gradients
   int row_block = kRowBlock;  // rows per pass-2 item
+  int fold_psum = 0;          // the first Gram kernel adds pass 1's P partials itself
   // device memory
   TensorDesc* d_tensors = nullptr;
   Item* d_items = nullptr;
@@ -407,6 +408,17 @@ void build_plan(psgd_state* s) {
     if (RP <= 8 && nc < 6LL * s->sms * rows1 * CT1) rows1 /= 2;
   }
   make_items(&s->p1items, rows1, CT1, true);
+  // P_raw: with at most two column-tile partials per row on average the first
+  // Gram kernel adds them as it reads P (one launch fewer); with more, a
+  // separate reduction with more loads in flight is faster
+  {
+    long long rows = 0, tile_rows = 0;
+    for (const TensorDesc& td : s->cdesc) {
+      rows += td.n;
+      tile_rows += (long long)td.ctiles1 * td.n;
+    }
+    s->fold_psum = tile_rows <= 2 * rows ? 1 : 0;
+  }
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const long long len = (long long)s->cdesc[c].m * RP;
     for (long long f = 0; f < len; f += 1024)
@@ -520,14 +532,20 @@ struct Ops {
     const int n_items = is_q ? a.n_gsq : a.n_gsp;
     const int grid = std::max(1, std::min(n_items, s->sms * 4));
     const float* src_dense = is_q ? s->qdraw : s->praw;
-    if (!is_q) {
+    if (!is_q && !s->fold_psum) {
       // P_raw = sum of pass 1's column-tile partials
       L.begin(K_PSUM);
       launch_psum<RP>(a, std::max(1, std::min(a.n_ps, s->sms * 8)), L.st);
       L.end();
     }
     L.begin(K_GRAM);
-    launch_gram<RP>(a, src_dense, nullptr, is_q, 0, s->gram, grid, L.st);
+    if (is_q || !s->fold_psum) {
+      launch_gram<RP>(a, src_dense, nullptr, is_q, 0, s->gram, grid, L.st);
+    } else {
+      // P_raw = the sum of pass 1's column-tile partials (in tile order),
+      // written dense while its Gram matrices are formed
+      launch_gram<RP>(a, s->praw_part, s->praw, 0, 1, s->gram, grid, L.st);
+    }
     launch_gram_sum<RP>(a, is_q, L.st);
     L.end();
     L.begin(K_SOLVE);

@@ -153,8 +153,19 @@ __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float
         const long long row = gi.row0 + r0 + rr;
         float v;
         if (from_parts) {
+          // the column-tile partials added in tile order, four loads in flight
+          const float* pp = src + td.pp_off + row * RP + k;
+          const long long tstride = (long long)td.n * RP;
           v = 0.f;
-          for (int c = 0; c < td.ctiles1; ++c) v += src[td.pp_off + ((long long)c * td.n + row) * RP + k];
+          int c = 0;
+          for (; c + 4 <= td.ctiles1; c += 4) {
+            float x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = pp[(c + u) * tstride];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v += x[u];
+          }
+          for (; c < td.ctiles1; ++c) v += pp[c * tstride];
         } else if (is_q) {
           v = src[base + (long long)k * td.m + row];
         } else {
