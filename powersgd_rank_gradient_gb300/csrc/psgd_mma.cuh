@@ -33,7 +33,7 @@ __device__ __forceinline__ void cp_async8_z(void* smem, const void* gmem, bool v
 // The items of the tensor-core pass 1: tensors whose rows are 16-byte
 // aligned in the bucket, wholly backed by it.  Advances `it` (stepping by the
 // grid) to the next such item and loads it.
-__device__ __forceinline__ bool tiled_item(const StepArgs& a, int& it, Item& item, TensorDesc& td) {
+__device__ __forceinline__ bool next_mma_item(const StepArgs& a, int& it, Item& item, TensorDesc& td) {
   for (; it < a.n_p1items; it += gridDim.x) {
     item = a.p1items[it];
     td = a.tensors[item.t];
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads1M, 1) k_pass1_mma(const StepArgs a) {
   int i_it = blockIdx.x, i_ch = 0, i_w = 0, i_cs = 0, i_nch = 0, i_slot = 0;
   Item i_item;
   TensorDesc i_td;
-  bool i_ok = tiled_item(a, i_it, i_item, i_td);
+  bool i_ok = next_mma_item(a, i_it, i_item, i_td);
   if (i_ok) i_nch = (i_item.ncols + T::CC - 1) / T::CC;
   auto issue = [&]() {
     if (i_ok) {
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads1M, 1) k_pass1_mma(const StepArgs a) {
         if (++i_ch == i_nch) {
           i_ch = 0;
           i_it += gridDim.x;
-          i_ok = tiled_item(a, i_it, i_item, i_td);
+          i_ok = next_mma_item(a, i_it, i_item, i_td);
           if (i_ok) i_nch = (i_item.ncols + T::CC - 1) / T::CC;
         }
       }
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads1M, 1) k_pass1_mma(const StepArgs a) {
   int c_it = blockIdx.x, c_ch = 0, c_w = 0, c_cs = 0, c_nch = 0, c_slot = 0;
   Item item;
   TensorDesc td;
-  bool c_ok = tiled_item(a, c_it, item, td);
+  bool c_ok = next_mma_item(a, c_it, item, td);
   if (c_ok) c_nch = (item.ncols + T::CC - 1) / T::CC;
   uint32_t phi[NR][4], plo[NR][4];      // P_old rows of this warp's row block, split
   float corr[2][4], mb[2][4], pacc[NR][4];
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kThreads1M, 1) k_pass1_mma(const StepArgs a) {
       if (++c_ch == c_nch) {
         c_ch = 0;
         c_it += gridDim.x;
-        c_ok = tiled_item(a, c_it, item, td);
+        c_ok = next_mma_item(a, c_it, item, td);
         if (c_ok) c_nch = (item.ncols + T::CC - 1) / T::CC;
       }
     }
