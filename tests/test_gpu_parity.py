@@ -72,7 +72,7 @@ def test_mixed_bucket_worlds(world):
     _run(MIXED, world, 4, 3, label=f"W={world}")
 
 
-@pytest.mark.parametrize("rank", [1, 2, 3, 5, 8, 16, 32])
+@pytest.mark.parametrize("rank", [1, 2, 3, 5, 8, 12, 16, 24, 32])
 def test_mixed_bucket_ranks(rank):
     _run(MIXED, 2, rank, 3, min_compression_rate=0.25, label=f"r={rank}")
 
@@ -85,7 +85,7 @@ def test_mixed_bucket_ranks(rank):
 ALIGNED = [(300, 1060), (129, 36), (64,), (1000, 516), (48, 16, 2, 2)]
 
 
-@pytest.mark.parametrize("rank", [16, 32])
+@pytest.mark.parametrize("rank", [12, 16, 24, 32])
 @pytest.mark.parametrize("world,kw", [
     (1, {}),
     (3, {}),
