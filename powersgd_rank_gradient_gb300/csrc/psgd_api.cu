@@ -269,6 +269,27 @@ void build_plan(psgd_state* s) {
   const int RP = s->RP;
   const int CT = ctile_for(RP);
   const int CT1 = ctile1_for(RP);
+  // Column tiles of pass 1.  Ranks up to 8: up to eight 128-column chunks a
+  // tile, the rest of a row split into tiles of 4, 2 and 1 chunks, so that the
+  // chunk-stationary kernel's 8 warps divide every tile's chunks evenly
+  // (a 1600-column tensor: 8 + 4 + 1 chunks rather than 8 + 5).  Ranks 16 and
+  // 32: CT1-column tiles.
+  auto p1_tiles = [&](int m) {
+    std::vector<std::pair<int, int>> v;   // (first column, columns)
+    if (RP > 8) {
+      for (int c0 = 0; c0 < m; c0 += CT1) v.push_back({c0, std::min(CT1, m - c0)});
+      return v;
+    }
+    int left = (m + 127) / 128, done = 0;
+    while (left > 0) {
+      int p = 8;
+      while (p > left) p >>= 1;
+      v.push_back({done * 128, std::min(p * 128, m - done * 128)});
+      done += p;
+      left -= p;
+    }
+    return v;
+  };
   s->cdesc.clear();
   s->items.clear();
   s->fitems.clear();
@@ -314,7 +335,7 @@ void build_plan(psgd_state* s) {
       td.r = h.rank;
       td.valid = h.valid >= 0 ? h.valid : h.numel;
       td.ctiles = (int)((h.cols + CT - 1) / CT);
-      td.ctiles1 = (int)((h.cols + CT1 - 1) / CT1);
+      td.ctiles1 = (int)p1_tiles((int)h.cols).size();
       td.rblocks = (int)((h.rows + s->row_block - 1) / s->row_block);
       td.pp_off = pp_off;
       td.qp_off = qp_off;
@@ -366,10 +387,17 @@ void build_plan(psgd_state* s) {
   // cut: end a row block at the first row the bucket does not wholly back
   // (batched hook), so that the checked kernels get only the rows that need
   // them.  Not for pass 2, whose row blocks index its partial sums.
+  // ctw > 0: uniform column tiles of ctw columns; ctw == 0: pass 1's tiles
   auto make_items = [&](std::vector<Item>* out, int rows_per_item, int ctw, bool cut) {
     for (size_t c = 0; c < s->cdesc.size(); ++c) {
       const TensorDesc& td = s->cdesc[c];
-      const int nct = (td.m + ctw - 1) / ctw;
+      std::vector<std::pair<int, int>> tiles;
+      if (ctw > 0) {
+        for (int c0 = 0; c0 < td.m; c0 += ctw) tiles.push_back({c0, std::min(ctw, td.m - c0)});
+      } else {
+        tiles = p1_tiles(td.m);
+      }
+      const int nct = (int)tiles.size();
       const long long vr = td.valid / td.m;   // rows [0, vr) are wholly backed
       for (int r0 = 0, r1; r0 < td.n; r0 = r1) {
         r1 = std::min(r0 + rows_per_item, td.n);
@@ -379,8 +407,8 @@ void build_plan(psgd_state* s) {
           it.t = (int)c;
           it.row0 = r0;
           it.nrows = r1 - r0;
-          it.col0 = ct * ctw;
-          it.ncols = std::min(ctw, td.m - it.col0);
+          it.col0 = tiles[ct].first;
+          it.ncols = tiles[ct].second;
           it.rb = r0 / s->row_block;
           it.ct = ct;
           it.pad = group_of[c];
@@ -407,7 +435,7 @@ void build_plan(psgd_state* s) {
       if (h.compressed) nc += h.numel;
     if (RP <= 8 && nc < 6LL * s->sms * rows1 * CT1) rows1 /= 2;
   }
-  make_items(&s->p1items, rows1, CT1, true);
+  make_items(&s->p1items, rows1, 0, true);
   // P_raw: with at most two column-tile partials per row on average the first
   // Gram kernel adds them as it reads P (one launch fewer); with more, a
   // separate reduction with more loads in flight is faster

@@ -268,6 +268,22 @@ __device__ __forceinline__ float dot_chain(const float (&a)[RP], const float (&b
   return acc;
 }
 
+// Packed pairs of fp32 values for fma.rn.f32x2: each half is an independent
+// IEEE fused multiply-add (the bits of fmaf), two per instruction.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // Reduce RP per-lane values over the warp by recursive halving: each step
 // exchanges half of the remaining values with the lane `o` apart, so after
 // log2(RP) steps every lane holds one partial value, which the remaining
@@ -537,6 +553,15 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       if (a.ef) load_qcols<RP, 4, !SH>(Qc + td.q_off, m, c, qc, ncv);
       if (!(a.ef && same_q)) load_qcols<RP, 4, !SH>(Qp + td.q_off, m, c, qp, ncv);
     }
+    // the same values as column pairs (0, 1) and (2, 3) for fma.rn.f32x2
+    uint64_t qc2[2][RP], qp2[2][RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) {
+      qc2[0][k] = f2pack(qc[0][k], qc[1][k]);
+      qc2[1][k] = f2pack(qc[2][k], qc[3][k]);
+      qp2[0][k] = f2pack(qp[0][k], qp[1][k]);
+      qp2[1][k] = f2pack(qp[2][k], qp[3][k]);
+    }
     // units are issued and consumed in order, wpc rows apart, the issued one
     // S - 1 units ahead of the consumed one: running offsets of the consumed
     // unit (bucket position, store offset) and rotating stage slots replace
@@ -621,8 +646,16 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       if (cin) {
         float corr[4] = {0.f, 0.f, 0.f, 0.f};
         if (a.ef) {
+          // dot_chain of each column, two columns per instruction (same bits)
+          uint64_t c01 = f2pack(0.f, 0.f), c23 = f2pack(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) corr[cc] = dot_chain<RP>(po, qc[cc]);
+          for (int k = 0; k < RP; ++k) {
+            const uint64_t pk = f2pack(po[k], po[k]);
+            c01 = fma2(pk, qc2[0][k], c01);
+            c23 = fma2(pk, qc2[1][k], c23);
+          }
+          f2unpack(c01, corr[0], corr[1]);
+          f2unpack(c23, corr[2], corr[3]);
         }
         float mb[4] = {0.f, 0.f, 0.f, 0.f};
         float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + r_off;
@@ -682,11 +715,15 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) mb[cc] *= a.invW;
         if (a.mbar) store_f<4>(a.mbar + r_off, mb);
-        const float (*qq)[RP] = (a.ef && same_q) ? qc : qp;
+        // projection: rank k gets (mb0 q0 + mb2 q2) + (mb1 q1 + mb3 q3)
+        const uint64_t (*qq)[RP] = (a.ef && same_q) ? qc2 : qp2;
+        const uint64_t m01 = f2pack(mb[0], mb[1]), m23 = f2pack(mb[2], mb[3]);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int k = 0; k < RP; ++k) pacc[k] = fmaf(mb[cc], qq[cc][k], pacc[k]);
+        for (int k = 0; k < RP; ++k) {
+          float x, y;
+          f2unpack(fma2(m23, qq[1][k], fma2(m01, qq[0][k], f2pack(0.f, 0.f))), x, y);
+          pacc[k] = x + y;
+        }
       }
       const float tot = warp_reduce_scatter<RP>(pacc);
       chk = fmaf(tot, 0.f, chk);   // inf/NaN in the row's inputs reach the sums
