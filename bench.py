@@ -42,10 +42,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="bert-large",
-                    choices=["bert-large", "gpt2-xl", "resnet50", "rank-sweep"])
+                    choices=["bert-large", "gpt2-xl", "resnet50", "rank-sweep", "fp16-scaled"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--extra", default="gpt2-xl",
-                    help="comma-separated workloads also measured and reported under 'workloads'")
+    ap.add_argument("--extra", default="gpt2-xl,bert-large:bf16,gpt2-xl:bf16,fp16-scaled",
+                    help="comma-separated workloads also measured and reported under 'workloads' "
+                         "(NAME or NAME:DTYPE; fp16-scaled = the 8192 x 8192 rank-4 matrix in fp16 "
+                         "pre-scaled by 65536 and unscaled by 2^-16 in pass 1; 'none' for none)")
+    ap.add_argument("--grad-dtype", default="f32", choices=["f32", "f16", "bf16"],
+                    help="type of the replica gradient buckets of the main workload (the pages' "
+                         "fp16/bf16 compress wrappers hand the hook 16-bit buckets)")
     ap.add_argument("--rank", type=int, default=None, help="rank of the rank-sweep workload")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling cases: only this many transformer layers, no embeddings")
@@ -66,20 +71,62 @@ def parse():
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-def workload_spec(name, rank_override=None, layers=None):
+GSIZE = {"f32": 4, "f16": 2, "bf16": 2}
+LOSS_SCALE = 65536.0   # GradScaler's default initial scale
+
+
+def workload_spec(name, rank_override=None, layers=None, dtype="f32"):
+    """A workload: the bucket's tensor shapes, replicas, rank and input
+    recipe; `dtype` is the type of the replica buckets (f32, f16, bf16).
+    fp16-scaled is the 8192 x 8192 rank-4 matrix whose N(0, 1e-3) gradients
+    are multiplied by 65536 and stored in fp16, as GradScaler-scaled
+    half-precision training produces them; pass 1 unscales by 2^-16."""
     from powersgd_rank_gradient_gb300 import workloads as wl
 
     if name == "rank-sweep":
-        return dict(name=f"rank-sweep-8192-r{rank_override or 8}", shapes=[(8192, 8192)], world_size=1,
+        spec = dict(name=f"rank-sweep-8192-r{rank_override or 8}", shapes=[(8192, 8192)], world_size=1,
                     rank=rank_override or 8, mcr=2.0, std=1.0, heavy=0.0, batch_same_shape=False)
-    w = wl.WORKLOADS[name]
-    if layers is not None and name in ("bert-large", "gpt2-xl"):
-        shapes = w["shapes"](layers=layers, embeddings=False)
-        name = f"{name}-{layers}layers"
+    elif name == "fp16-scaled":
+        spec = dict(name="fp16-scaled-8192-r4", shapes=[(8192, 8192)], world_size=1, rank=4, mcr=2.0,
+                    std=1e-3, heavy=0.0, batch_same_shape=False)
+        dtype = "f16"
+        spec["loss_scale"] = LOSS_SCALE
     else:
-        shapes = w["shapes"]()
-    return dict(name=name, shapes=shapes, world_size=w["world_size"], rank=w["rank"],
-                mcr=w["mcr"], std=w["std"], heavy=w["heavy"], batch_same_shape=w["batch_same_shape"])
+        w = wl.WORKLOADS[name]
+        if layers is not None and name in ("bert-large", "gpt2-xl"):
+            shapes = w["shapes"](layers=layers, embeddings=False)
+            name = f"{name}-{layers}layers"
+        else:
+            shapes = w["shapes"]()
+        spec = dict(name=name, shapes=shapes, world_size=w["world_size"], rank=w["rank"],
+                    mcr=w["mcr"], std=w["std"], heavy=w["heavy"], batch_same_shape=w["batch_same_shape"])
+    spec.setdefault("loss_scale", 1.0)
+    spec["dtype"] = dtype
+    if dtype != "f32" and not spec["name"].endswith(dtype) and name != "fp16-scaled":
+        spec["name"] = f"{spec['name']}-{dtype}"
+    return spec
+
+
+def make_bucket(spec, seed, device):
+    """One replica's bucket of the workload, in its gradient type."""
+    import torch
+
+    from powersgd_rank_gradient_gb300 import workloads as wl
+
+    g = wl.gaussian_bucket_torch(spec["shapes"], spec["std"], seed, device, heavy_fraction=spec["heavy"])
+    if spec["loss_scale"] != 1.0:
+        g.mul_(spec["loss_scale"])
+    if spec["dtype"] == "f16":
+        return g.half()
+    if spec["dtype"] == "bf16":
+        return g.bfloat16()
+    return g
+
+
+def torch_dtype(spec):
+    import torch
+
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[spec["dtype"]]
 
 
 def plan_counts(spec):
@@ -98,19 +145,26 @@ def plan_counts(spec):
                 pq=sum((r + c) * k for r, c, k, cc in zip(rows, cols, ranks, comp) if cc))
 
 
-def step_bytes(spec, counts, gsz=4):
+def step_bytes(spec, counts):
     """Bytes one step must move.  'design' is this implementation's
     three-pass schedule with the factored residual; 'survey_min' is the
-    explicit-residual minimum min(6W+1, 5W+3) * 4 bytes per compressed element
-    (the bound the targets are quoted against)."""
+    explicit-residual minimum per compressed element, the smaller of the
+    scheme that overwrites e_w with M_w in pass 1 (W s_g + 20 W + 4) and the
+    one that re-reads g and e in pass 3 (2 W s_g + 12 W + 12) -- the bound
+    the targets are quoted against (for fp32, min(6W+1, 5W+3) * 4)."""
     W = spec["world_size"]
+    gsz = GSIZE[spec["dtype"]]
     nc, nu = counts["Nc"], counts["Nunc"]
-    mbar = W * 4 > 8
+    reread = W * 4
+    mbar = reread > 8
     p1 = W * (gsz + 8) + (4 if mbar else 0)
-    p2 = 4 if mbar else 4 * W
+    p2 = 4 if mbar else reread
     design = nc * (p1 + p2 + 4) + nu * (W * gsz + 4)
-    survey = nc * min(6 * W + 1, 5 * W + 3) * 4 + nu * (W * gsz + 4) + (W + 1) * counts["pq"] * 4
-    return dict(design=design, survey_min=survey)
+    per_el = min(W * gsz + 20 * W + 4, 2 * W * gsz + 12 * W + 12)
+    survey = nc * per_el + nu * (W * gsz + 4) + (W + 1) * counts["pq"] * 4
+    # pass 1 of the explicit-residual scheme: read g_w and e_w, write M_w
+    survey_pass1 = nc * W * (gsz + 8)
+    return dict(design=design, survey_min=survey, survey_pass1=survey_pass1)
 
 
 def load_peaks():
@@ -242,7 +296,9 @@ def job_throughput(bytes_per_rank_step, steps, ranks, max_ms):
 # ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
-def run_native(spec, args, dist, rank_id, world, device):
+def run_native(spec, args, dist, rank_id, world, device, light=False):
+    """Times the workload's warm-started compressed step.  light: the step
+    alone (no vanilla/first-call rows, batched hook, bucket groups or e2e)."""
     import torch
 
     from powersgd_rank_gradient_gb300 import PowerSGDState, workloads as wl
@@ -250,15 +306,16 @@ def run_native(spec, args, dist, rank_id, world, device):
     W = spec["world_size"]
     counts = plan_counts(spec)
     N = counts["N"]
+    gsz = GSIZE[spec["dtype"]]
+    inv_scale = 1.0 / spec["loss_scale"]
     st = PowerSGDState(spec["shapes"], W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
                        min_compression_rate=spec["mcr"], use_error_feedback=True, warm_start=True,
                        batch_tensors_with_same_shape=spec["batch_same_shape"], random_seed=0,
-                       device=device)
+                       grad_dtype=torch_dtype(spec), device=device)
     # two resident input sets (W replica buckets each), alternated step to step
     sets = []
     for k in range(2):
-        sets.append([wl.gaussian_bucket_torch(spec["shapes"], spec["std"], wl.replica_seed(w, k), device,
-                                              heavy_fraction=spec["heavy"]) for w in range(W)])
+        sets.append([make_bucket(spec, wl.replica_seed(w, k), device) for w in range(W)])
     out = torch.empty(N, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     # the clock sampler runs from the warm-up through the timed region
@@ -266,7 +323,7 @@ def run_native(spec, args, dist, rank_id, world, device):
     if rank_id == 0:
         clocks.start()
     for i in range(args.warmup):
-        st.step(sets[i % 2], out=out)
+        st.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
     if st.status():
         raise RuntimeError("warm-up step was skipped (non-finite input)")
     torch.cuda.synchronize(device)
@@ -279,7 +336,7 @@ def run_native(spec, args, dist, rank_id, world, device):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        st.step(sets[i % 2], out=out)
+        st.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
     e1.record(stream)
     torch.cuda.synchronize(device)
     if dist is not None:
@@ -291,39 +348,54 @@ def run_native(spec, args, dist, rank_id, world, device):
         raise RuntimeError("timed step was skipped (non-finite input)")
     prof = st.profile_read()
     ms_step = ms / args.steps
-    grad_bytes = W * N * 4
+    grad_bytes = W * N * gsz
     value = job_throughput(grad_bytes, args.steps, world, ms)
     launches = sum(v[0] for v in prof.values())
     # dominant kernel by device time
     kern = max((k for k in prof if prof[k][0] > 0), key=lambda k: prof[k][1])
     n_l, tot_ms, bpl = prof[kern]
     peak, peak_kind = load_peaks()
-    achieved = bpl / (tot_ms / n_l / 1e3) / 1e9 if n_l and bpl else None
+    launch_s = tot_ms / n_l / 1e3 if n_l else None
+    achieved = bpl / launch_s / 1e9 if n_l and bpl else None
     kernels = {k: {"launches": v[0], "avg_us": (v[1] / v[0] * 1e3) if v[0] else None,
                    "share": v[1] / max(1e-12, sum(x[1] for x in prof.values())),
                    "algo_bytes_per_launch": v[2] or None,
                    "gbs": (v[2] / (v[1] / v[0] / 1e3) / 1e9) if v[0] and v[2] else None}
                for k, v in prof.items() if v[0]}
     sb = step_bytes(spec, counts)
+    roof = {"bound": "hbm", "kernel": kern, "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": (achieved / peak) if achieved else None, "peak_source": peak_kind,
+            "traffic": ncu_traffic(spec["name"], kern),
+            "bytes_basis": "the kernel's own algorithmic bytes per launch"}
+    roof["frac_design"] = roof["frac"]
+    if kern == "pass1" and launch_s:
+        # the explicit-residual scheme's pass 1 (read g_w and e_w, write M_w:
+        # W (s_g + 8) bytes per compressed element), on the same launch time
+        roof["achieved_survey_pass1"] = sb["survey_pass1"] / launch_s / 1e9
+        roof["frac_survey_pass1"] = roof["achieved_survey_pass1"] / peak
+    step_gbs = sb["design"] / (ms_step / 1e3) / 1e9
+    survey_gbs = sb["survey_min"] / (ms_step / 1e3) / 1e9
     res = dict(
         value=value, ms_per_step=ms_step, grad_bytes=grad_bytes, launches=launches, clocks=clk,
-        roofline={"bound": "hbm", "kernel": kern, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                  "frac": (achieved / peak) if achieved else None, "peak_source": peak_kind,
-                  "traffic": ncu_traffic(spec["name"], kern)},
-        step_roofline={"design_bytes": sb["design"], "design_gbs": sb["design"] / (ms_step / 1e3) / 1e9,
-                       "design_frac_of_measured": sb["design"] / (ms_step / 1e3) / 1e9 / peak,
+        roofline=roof,
+        step_roofline={"design_bytes": sb["design"], "design_gbs": step_gbs,
+                       "design_frac_of_measured": step_gbs / peak,
                        "survey_min_bytes": sb["survey_min"],
-                       "survey_min_frac_of_nominal_8tbs": sb["survey_min"] / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-                       "survey_min_frac_of_measured": sb["survey_min"] / (ms_step / 1e3) / 1e9 / peak},
-        kernels=kernels, counts=counts)
-    res["rows"] = run_rows(spec, args, dist, device, sets, out, W, N)
-    if args.batched:
-        res["rows"]["next_batched_hook"] = run_batched(spec, args, dist, device, sets, out, W, N)
-    if args.buckets > 0:
-        res["rows"]["next_bucket_overlap"] = run_buckets(spec, args, dist, device, sets, W, N)
+                       "survey_min_note": "explicit-residual equivalent: the bytes a design that writes "
+                                          "e_w would move; the factored residual moves fewer, so this "
+                                          "fraction can exceed 1",
+                       "survey_min_frac_of_nominal_8tbs": survey_gbs / NOMINAL_HBM_GBS,
+                       "survey_min_frac_of_measured": survey_gbs / peak},
+        kernels=kernels, counts=counts, dtype=spec["dtype"], loss_scale=spec["loss_scale"])
+    if not light:
+        res["rows"] = run_rows(spec, args, dist, device, sets, out, W, N)
+        if args.batched:
+            res["rows"]["next_batched_hook"] = run_batched(spec, args, dist, device, sets, out, W, N)
+        if args.buckets > 0:
+            res["rows"]["next_bucket_overlap"] = run_buckets(spec, args, dist, device, sets, W, N)
     del sets
     torch.cuda.empty_cache()
-    if not args.no_e2e:
+    if not args.no_e2e and not light:
         res["e2e"] = run_e2e(st, spec, args, dist, device, N, W)
     st.close()
     return res
@@ -340,27 +412,29 @@ def run_rows(spec, args, dist, device, sets, out, W, N):
 
     stream = torch.cuda.current_stream(device)
     rows = {}
+    gsz = GSIZE[spec["dtype"]]
+    inv_scale = 1.0 / spec["loss_scale"]
     van = PowerSGDState(spec["shapes"], W, matrix_approximation_rank=spec["rank"],
                         start_powerSGD_iter=1 << 60, min_compression_rate=spec["mcr"],
-                        use_error_feedback=False, device=device)
+                        use_error_feedback=False, grad_dtype=torch_dtype(spec), device=device)
     for i in range(3):
-        van.step(sets[i % 2], out=out)
+        van.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
     torch.cuda.synchronize(device)
     van.profile(True)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        van.step(sets[i % 2], out=out)
+        van.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
     e1.record(stream)
     torch.cuda.synchronize(device)
     ms = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
     prof = van.profile_read()
     n_l, tot_ms, _ = prof["mean"]
-    mean_bytes = N * (W * 4 + 4)
+    mean_bytes = N * (W * gsz + 4)
     peak, _ = load_peaks()
     rows["A1_vanilla_phase"] = {
-        "ms_per_step": ms, "gradient_gbs": W * N * 4 / (ms / 1e3) / 1e9,
+        "ms_per_step": ms, "gradient_gbs": W * N * gsz / (ms / 1e3) / 1e9,
         "kernel": "mean", "algo_bytes_per_launch": mean_bytes,
         "achieved_gbs": mean_bytes / (tot_ms / n_l / 1e3) / 1e9,
         "frac_of_measured": mean_bytes / (tot_ms / n_l / 1e3) / 1e9 / peak}
@@ -368,11 +442,12 @@ def run_rows(spec, args, dist, device, sets, out, W, N):
     # A3: a fresh state's first compressed call (Q draw + orthogonalisation)
     fresh = PowerSGDState(spec["shapes"], W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
                           min_compression_rate=spec["mcr"],
-                          batch_tensors_with_same_shape=spec["batch_same_shape"], device=device)
+                          batch_tensors_with_same_shape=spec["batch_same_shape"],
+                          grad_dtype=torch_dtype(spec), device=device)
     times = []
     for i in range(3):
         e0.record(stream)
-        fresh.step(sets[i % 2], out=out)
+        fresh.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
         e1.record(stream)
         torch.cuda.synchronize(device)
         times.append(e0.elapsed_time(e1))
@@ -390,16 +465,18 @@ def run_batched(spec, args, dist, device, sets, out, W, N):
     from powersgd_rank_gradient_gb300 import BatchedPowerSGDState
 
     stream = torch.cuda.current_stream(device)
+    gsz = GSIZE[spec["dtype"]]
+    inv_scale = 1.0 / spec["loss_scale"]
     st = BatchedPowerSGDState(N, W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
-                              device=device)
+                              grad_dtype=torch_dtype(spec), device=device)
     for i in range(3):
-        st.step(sets[i % 2], out=out)
+        st.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
     torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        st.step(sets[i % 2], out=out)
+        st.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
     e1.record(stream)
     torch.cuda.synchronize(device)
     ms = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
@@ -407,14 +484,14 @@ def run_batched(spec, args, dist, device, sets, out, W, N):
     st.profile(True)
     st.profile_read()
     for i in range(args.steps):
-        st.step(sets[i % 2], out=out)
+        st.step(sets[i % 2], out=out, inv_loss_scale=inv_scale)
     torch.cuda.synchronize(device)
     kinds = {k: round(v[1] / args.steps, 4) for k, v in st.profile_read().items() if v[0]}
     st.profile(False)
     side = st.side
     st.close()
     return {"side": side, "vector_path": side % 4 == 0, "ms_per_step": ms,
-            "gradient_gbs": W * N * 4 / (ms / 1e3) / 1e9, "kernel_ms_per_step": kinds}
+            "gradient_gbs": W * N * gsz / (ms / 1e3) / 1e9, "kernel_ms_per_step": kinds}
 
 
 def ddp_buckets(shapes, cap_mb, elem_bytes=4):
@@ -445,7 +522,7 @@ def run_buckets(spec, args, dist, device, sets, W, N):
     from powersgd_rank_gradient_gb300 import PowerSGDGroup, workloads as wl
 
     shapes = spec["shapes"]
-    idx = ddp_buckets(shapes, args.buckets)
+    idx = ddp_buckets(shapes, args.buckets, GSIZE[spec["dtype"]])
     off = [0]
     for s_ in shapes:
         off.append(off[-1] + wl.numel(s_))
@@ -454,19 +531,21 @@ def run_buckets(spec, args, dist, device, sets, W, N):
     grads = [[torch.cat([sets[0][w][off[i]:off[i + 1]] for i in b]) for w in range(W)] for b in idx]
     outs = [torch.empty(g[0].numel(), dtype=torch.float32, device=device) for g in grads]
     stream = torch.cuda.current_stream(device)
+    gsz = GSIZE[spec["dtype"]]
+    inv_scale = 1.0 / spec["loss_scale"]
     res = {"cap_mb": args.buckets, "n_buckets": len(idx),
-           "largest_bucket_mb": max(g[0].numel() for g in grads) * 4 / 2**20}
+           "largest_bucket_mb": max(g[0].numel() for g in grads) * gsz / 2**20}
     S = args.bucket_streams
     for label, n_streams, graphs in (("serial", 1, False), (f"streams_{S}", S, False),
                                      (f"streams_{S}_graphs", S, True)):
         grp = PowerSGDGroup(bucket_shapes, W, matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0,
                             min_compression_rate=spec["mcr"],
                             batch_tensors_with_same_shape=spec["batch_same_shape"], n_streams=n_streams,
-                            graphs=graphs, device=device)
+                            graphs=graphs, grad_dtype=torch_dtype(spec), device=device)
 
         def iteration():
             for b in range(len(idx)):
-                grp.step(b, grads[b], out=outs[b])
+                grp.step(b, grads[b], out=outs[b], inv_loss_scale=inv_scale)
             grp.wait()
 
         for _ in range(max(3, args.warmup)):
@@ -482,7 +561,7 @@ def run_buckets(spec, args, dist, device, sets, W, N):
         e1.record(stream)
         torch.cuda.synchronize(device)
         ms = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
-        res[label] = {"ms_per_step": ms, "gradient_gbs": W * N * 4 / (ms / 1e3) / 1e9}
+        res[label] = {"ms_per_step": ms, "gradient_gbs": W * N * gsz / (ms / 1e3) / 1e9}
         grp.close()
     del grads, outs
     torch.cuda.empty_cache()
@@ -496,17 +575,18 @@ def run_e2e(st, spec, args, dist, device, N, W):
 
     from powersgd_rank_gradient_gb300 import workloads as wl
 
+    gsz = GSIZE[spec["dtype"]]
+    inv_scale = 1.0 / spec["loss_scale"]
     host = []
     for w in range(W):
-        g = wl.gaussian_bucket_torch(spec["shapes"], spec["std"], wl.replica_seed(w, 7), device,
-                                     heavy_fraction=spec["heavy"])
-        h = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        g = make_bucket(spec, wl.replica_seed(w, 7), device)
+        h = torch.empty(N, dtype=g.dtype, pin_memory=True)
         h.copy_(g)
         host.append(h)
         del g
     host_out = torch.empty(N, dtype=torch.float32, pin_memory=True)
     stream = torch.cuda.current_stream(device)
-    st.step_host(host, host_out)  # allocates the staging buffers
+    st.step_host(host, host_out, inv_loss_scale=inv_scale)  # allocates the staging buffers
     torch.cuda.synchronize(device)
     k = max(3, min(args.steps, 10))
     if dist is not None:
@@ -515,13 +595,13 @@ def run_e2e(st, spec, args, dist, device, N, W):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(k):
-        st.step_host(host, host_out)
+        st.step_host(host, host_out, inv_loss_scale=inv_scale)
     e1.record(stream)
     torch.cuda.synchronize(device)
     ms = reduce_max(e0.elapsed_time(e1), dist, device)
     ws = dist.get_world_size() if dist is not None else 1
-    return {"value": job_throughput(W * N * 4, k, ws, ms), "unit": UNIT,
-            "h2d_bytes_per_step": W * N * 4, "d2h_bytes_per_step": N * 4, "ms_per_step": ms / k}
+    return {"value": job_throughput(W * N * gsz, k, ws, ms), "unit": UNIT,
+            "h2d_bytes_per_step": W * N * gsz, "d2h_bytes_per_step": N * 4, "ms_per_step": ms / k}
 
 
 # ---------------------------------------------------------------------------
@@ -574,7 +654,7 @@ def time_oracle(spec, steps, budget=None, target_s=None, warmup=1):
         if target_s is not None and time.perf_counter() - t_start > target_s:
             break
     t = statistics.median(times)
-    return dict(value=W * n * 4 / t / 1e9, unit=UNIT, cores=os.cpu_count(), kind="oracle",
+    return dict(value=W * n * GSIZE[spec["dtype"]] / t / 1e9, unit=UNIT, cores=os.cpu_count(), kind="oracle",
                 sample=f"{len(shapes)} tensors ({n} elements per replica, W={W}) of the {spec['name']} "
                        f"bucket, fp64 NumPy, median of {len(times)} steps",
                 s_per_step=t)
@@ -586,12 +666,13 @@ def main():
     rank_id = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    spec = workload_spec(args.workload, rank_override=args.rank, layers=args.layers)
+    spec = workload_spec(args.workload, rank_override=args.rank, layers=args.layers, dtype=args.grad_dtype)
     base_cfg = {"workload": spec["name"], "world_size_W": spec["world_size"],
                 "matrix_approximation_rank": spec["rank"], "min_compression_rate": spec["mcr"],
                 "start_powerSGD_iter": 0, "use_error_feedback": True, "warm_start": True,
                 "batch_tensors_with_same_shape": spec["batch_same_shape"],
-                "gradients": f"N(0,{spec['std']}) fp32" + (f", {spec['heavy']:.0%} heavy rows x100" if spec["heavy"] else ""),
+                "gradients": f"N(0,{spec['std']}) {spec['dtype']}" + (f", {spec['heavy']:.0%} heavy rows x100" if spec["heavy"] else "")
+                             + (f", x{spec['loss_scale']:g} (unscaled in pass 1)" if spec["loss_scale"] != 1.0 else ""),
                 "l2": "inputs larger than L2 (each step reads >10 GB)" if spec["name"] != "resnet50" else "inputs larger than L2",
                 "parallelism": f"replicas x{world}"}
 
@@ -624,11 +705,22 @@ def main():
 
     res = run_native(spec, args, dist, rank_id, world, device)
     extras = {}
-    for name in [x for x in args.extra.split(",") if x and x not in ("none", args.workload)]:
-        sp = workload_spec(name, layers=args.layers)
-        r = run_native(sp, args, dist, rank_id, world, device)
-        extras[sp["name"]] = {"value": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
-                              "step_roofline": r["step_roofline"], "e2e": r.get("e2e"), "clocks": r["clocks"],
+    for item in [x for x in args.extra.split(",") if x and x != "none"]:
+        name, _, dt = item.partition(":")
+        sp = workload_spec(name, layers=args.layers, dtype=dt or "f32")
+        if sp["name"] == spec["name"]:
+            continue
+        # the main workload's fp32 companions get every row; 16-bit lines the step alone
+        r = run_native(sp, args, dist, rank_id, world, device, light=sp["dtype"] != "f32")
+        extras[sp["name"]] = {"metric": METRIC, "value": r["value"], "unit": UNIT,
+                              "ms_per_step": r["ms_per_step"], "dtype": sp["dtype"],
+                              "loss_scale": sp["loss_scale"], "gpu_launches": r["launches"],
+                              "config": {"workload": sp["name"], "world_size_W": sp["world_size"],
+                                         "matrix_approximation_rank": sp["rank"],
+                                         "gradients": f"N(0,{sp['std']}) {sp['dtype']}"
+                                         + (f" x{sp['loss_scale']:g}" if sp["loss_scale"] != 1.0 else "")},
+                              "roofline": r["roofline"], "step_roofline": r["step_roofline"],
+                              "e2e": r.get("e2e"), "clocks": r["clocks"],
                               "kernels": r["kernels"], "rows": r.get("rows")}
     cpu = None
     if rank_id == 0 and world == 1 and not args.no_cpu:
@@ -639,7 +731,8 @@ def main():
     if rank_id == 0:
         line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "grad_dtype": spec["dtype"],
+                "data": "synthetic",
                 "config": base_cfg, "clocks": res["clocks"], "gpu_launches": res["launches"],
                 "roofline": res["roofline"], "step_roofline": res["step_roofline"],
                 "e2e": res.get("e2e"), "cpu_baseline": cpu, "kernels": res["kernels"],

@@ -373,6 +373,106 @@ int psgd_group_bucket(psgd_group* g, int32_t bucket, psgd_state** out);
 /* Number of buckets (0 for NULL). */
 int32_t psgd_group_size(const psgd_group* g);
 
+/*
+ * Data-parallel split of the step -- one replica per process.
+ *
+ * [DDP] "PowerSGD Hooks", powerSGD_hook: each worker computes its own
+ * P = M_w Q and Q = M_w^T P, and the hook allreduces the uncompressed batch
+ * (step 2), the Ps (step 3.3) and the Qs (step 3.6) across the workers;
+ * "Default Communication Hooks", allreduce_hook: the result is the mean.
+ * When each process (typically one per GPU) holds ONE replica, the linearity
+ * fold that psgd_step uses for its W simulated replicas no longer applies,
+ * and the step is split at its two exchanges:
+ *
+ *   psgd_dp_begin    pass 1 on the local replica: M = g * s + e, the local
+ *                    P = M Q, the local uncompressed values and a skip flag,
+ *                    all packed into one exchange buffer;
+ *   (caller)         SUM-allreduce that buffer across the W processes;
+ *   psgd_dp_project  P = sum / W, orthogonalise P, local Q = M^T P into a
+ *                    second exchange buffer;
+ *   (caller)         SUM-allreduce that buffer;
+ *   psgd_dp_finish   Q = sum / W, out = P Q^T, uncompressed out = sum / W,
+ *                    residual kept (factored), commit.
+ *
+ * The exchange buffers are library-owned device memory at fixed addresses
+ * (psgd_dp_begin / psgd_dp_project return them with their float counts), so
+ * the caller's collective (NCCL on device memory, or a host exchange through
+ * a copy) reads and writes them in place; a SUM reduction with any
+ * association order is expected.  The library itself makes no collective
+ * call and reads no peer memory.  Every process must call the three stages
+ * in order, step after step, with the same bucket layout and
+ * hyper-parameters (random_seed included: the initial Q is drawn the same
+ * on every process).  A non-finite input on any process raises that
+ * process's flag in the exchanged buffer, so after the sum every process
+ * skips the same step ([AMP]) and keeps its state bit-identical.  Before
+ * start_powerSGD_iter the exchange buffer of psgd_dp_begin is `out` itself,
+ * holding this replica's unscaled gradient (psgd_dp_project then returns
+ * count 0), and psgd_dp_finish divides it by W; a non-finite sum skips.
+ */
+
+/*
+ * psgd_dp_create -- the state of ONE process of a W-process data-parallel job
+ * (W = world_size in [1, 64]).  Arguments as psgd_state_create; the state
+ * holds this process's error-feedback residual (one replica) and the shared
+ * factors.  psgd_step on it returns PSGD_EINVAL (use the three stages);
+ * psgd_step_status, psgd_get_stats, psgd_tensor_info, psgd_set_q, psgd_get_q,
+ * psgd_get_p, psgd_get_error / psgd_set_error (replica 0 = this process's),
+ * psgd_workspace_bytes, psgd_profile* and psgd_state_destroy work as for any
+ * state.  Errors: as psgd_state_create.
+ */
+int psgd_dp_create(const int64_t* dims, const int32_t* ndims, int32_t n_tensors, int32_t world_size,
+                   int32_t matrix_approximation_rank, int64_t start_powerSGD_iter,
+                   double min_compression_rate, int32_t use_error_feedback, int32_t warm_start,
+                   float orthogonalization_epsilon, uint64_t random_seed,
+                   int32_t batch_tensors_with_same_shape, psgd_dtype grad_dtype, int32_t device,
+                   psgd_state** out);
+
+/*
+ * psgd_dp_begin -- first stage of one hook call on this process's replica.
+ *   grad  : device pointer, this replica's flat bucket (N elements of
+ *           grad_dtype); read here and, without error feedback, again by
+ *           psgd_dp_project's kernels: keep it valid and unchanged until
+ *           that call's work has run on `stream`.
+ *   out   : device pointer, N floats, the bucket the hook returns (written
+ *           by psgd_dp_finish; before start_powerSGD_iter also the exchange
+ *           buffer).  Must not overlap grad unless grad == out (F32).
+ *   inv_loss_scale, stream : as psgd_step.
+ *   exchange, count : out; the device buffer (`count` floats) to
+ *           SUM-allreduce across the W processes before psgd_dp_project.
+ * Enqueues only.  Errors: PSGD_EINVAL (NULL pointers, stage out of order,
+ * not a data-parallel state), PSGD_ECUDA.
+ */
+int psgd_dp_begin(psgd_state* s, const void* grad, float* out, float inv_loss_scale, void* stream,
+                  float** exchange, int64_t* count);
+
+/*
+ * psgd_dp_project -- second stage, after the caller's SUM-allreduce of the
+ * first exchange buffer: P = sum / W, Gram-Schmidt, local Q = M^T P.
+ * exchange, count : out; the device buffer to SUM-allreduce before
+ * psgd_dp_finish (count 0: nothing to exchange, as before
+ * start_powerSGD_iter).  Enqueues only.  Errors: PSGD_EINVAL (stage out of
+ * order), PSGD_ECUDA.
+ */
+int psgd_dp_project(psgd_state* s, void* stream, float** exchange, int64_t* count);
+
+/*
+ * psgd_dp_finish -- last stage, after the caller's SUM-allreduce of the
+ * second exchange buffer (if any): Q = sum / W (the next warm-start Q),
+ * out = P Q^T for the compressed tensors and the replica mean for the rest,
+ * then the commit (or the skip).  psgd_step_status reports the outcome, the
+ * same on every process.  Enqueues only.  Errors: PSGD_EINVAL (stage out of
+ * order), PSGD_ECUDA.
+ */
+int psgd_dp_finish(psgd_state* s, void* stream);
+
+/*
+ * psgd_build_id -- "psgd-source-hash:" followed by the SHA-256 (32 hex
+ * digits) of the sources, header, flags and compiler version this library
+ * was built from, so that a caller can check that the loaded binary matches
+ * its sources.  The string is static.
+ */
+const char* psgd_build_id(void);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* psgd_last_error(void);
 

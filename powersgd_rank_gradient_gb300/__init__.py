@@ -12,4 +12,8 @@ def __getattr__(name):
         from . import hook
 
         return getattr(hook, name)
+    if name in ("DataParallelPowerSGDState", "dp_powerSGD_hook"):
+        from . import dp
+
+        return getattr(dp, name)
     raise AttributeError(name)

@@ -34,6 +34,7 @@ EXPORTS = [
     "psgd_project_q_static",
     "psgd_group_create", "psgd_group_destroy", "psgd_group_step", "psgd_group_wait",
     "psgd_group_status", "psgd_group_bucket", "psgd_group_size", "psgd_set_graph", "psgd_graph_stats",
+    "psgd_dp_create", "psgd_dp_begin", "psgd_dp_project", "psgd_dp_finish", "psgd_build_id",
 ]
 
 _lib = None
@@ -122,6 +123,17 @@ def lib():
     L.psgd_set_graph.restype = ctypes.c_int
     L.psgd_graph_stats.argtypes = [P, pi64, pi64]
     L.psgd_graph_stats.restype = ctypes.c_int
+    L.psgd_dp_create.argtypes = L.psgd_state_create.argtypes
+    L.psgd_dp_create.restype = ctypes.c_int
+    pf = ctypes.POINTER(ctypes.c_void_p)
+    L.psgd_dp_begin.argtypes = [P, P, P, ctypes.c_float, P, pf, pi64]
+    L.psgd_dp_begin.restype = ctypes.c_int
+    L.psgd_dp_project.argtypes = [P, P, pf, pi64]
+    L.psgd_dp_project.restype = ctypes.c_int
+    L.psgd_dp_finish.argtypes = [P, P]
+    L.psgd_dp_finish.restype = ctypes.c_int
+    L.psgd_build_id.argtypes = []
+    L.psgd_build_id.restype = ctypes.c_char_p
     L.psgd_last_error.argtypes = []
     L.psgd_last_error.restype = ctypes.c_char_p
     _lib = L

@@ -109,9 +109,9 @@ int plan_tensors(const int64_t* dims, const int32_t* ndims, int32_t n, int32_t r
 }
 
 enum Kind { K_MEAN = 0, K_PASS1, K_GRAM, K_SOLVE, K_APPLY, K_PASS2, K_QREDUCE, K_PASS3, K_COMMIT, K_RANDN,
-            K_PSUM, K_COUNT };
+            K_PSUM, K_DP, K_COUNT };
 const char* kKindNames[K_COUNT] = {"mean", "pass1", "gs_gram", "gs_solve", "gs_apply",
-                                   "pass2", "qreduce", "pass3", "commit", "randn", "psum"};
+                                   "pass2", "qreduce", "pass3", "commit", "randn", "psum", "dp_exchange"};
 
 struct EventPair {
   cudaEvent_t a, b;
@@ -201,6 +201,20 @@ struct psgd_state {
   const void* gkey_out = nullptr;
   float gkey_scale = 0.f;
   long long graph_captures = 0, graph_replays = 0;
+  // data-parallel split (psgd_dp_*): this process holds one replica of a
+  // dp_world-process job (0: not a data-parallel state)
+  int dp_world = 0;
+  float* xp = nullptr;        // first exchange: [P_raw | pad | uncompressed | flag]
+  long long xp_count = 0;
+  long long xp_unc = 0;       // first uncompressed value in xp
+  float* xq = nullptr;        // second exchange: Q (Qf layout)
+  long long* d_unc_pos = nullptr;  // packed position of each uncompressed segment
+  long long* d_all_pos = nullptr;  // position of each whole-bucket segment (= its offset)
+  int dp_stage = 0;           // 0 idle, 1 after begin, 2 after project
+  const void* dp_grad = nullptr;
+  float* dp_out = nullptr;
+  float dp_scale = 1.f;
+  bool dp_vanilla = false, dp_compressed = false;
   // counters
   long long iter = 0;
   long long compressed_launched = 0;
@@ -556,11 +570,13 @@ struct Launcher {
 
 template <int RP>
 struct Ops {
-  static void gs(psgd_state* s, const StepArgs& a, Launcher& L, int is_q) {
+  // do_psum: P_raw still has to be summed from pass 1's partials (the
+  // data-parallel split sums them before its exchange instead)
+  static void gs(psgd_state* s, const StepArgs& a, Launcher& L, int is_q, bool do_psum = true) {
     const int n_items = is_q ? a.n_gsq : a.n_gsp;
     const int grid = std::max(1, std::min(n_items, s->sms * 4));
     const float* src_dense = is_q ? s->qdraw : s->praw;
-    if (!is_q && !s->fold_psum) {
+    if (!is_q && !s->fold_psum && do_psum) {
       // P_raw = sum of pass 1's column-tile partials
       L.begin(K_PSUM);
       launch_psum<RP>(a, std::max(1, std::min(a.n_ps, s->sms * 8)), L.st);
@@ -627,6 +643,51 @@ struct Ops {
     L.end();
   }
 
+  // Data-parallel split, stage 1: a fresh Q when needed, pass 1 on the one
+  // local replica, and this process's P_raw summed densely into the
+  // exchange buffer (a.praw points into it).
+  static void dp_begin(psgd_state* s, const StepArgs& a, Launcher& L, bool need_fresh,
+                       const std::vector<int>& mask) {
+    const int grid_p1 = std::max(1, std::min(a.n_p1items, s->sms));
+    const int grid_ps = std::max(1, std::min(a.n_ps, s->sms * 8));
+    const int grid_q = std::max(1, std::min(a.n_gsq, s->sms * 4));
+    if (need_fresh) {
+      cudaMemcpyAsync(s->d_mask, mask.data(), mask.size() * sizeof(int), cudaMemcpyHostToDevice, L.st);
+      L.begin(K_RANDN);
+      launch_randn(a, s->d_mask, s->seed, (unsigned long long)s->iter, s->tensor_base, RP, grid_q, L.st);
+      L.end();
+      gs(s, a, L, 1);
+    }
+    L.begin(K_PASS1);
+    launch_pass1<RP>(a, grid_p1, L.st);
+    L.end();
+    L.begin(K_PSUM);
+    launch_psum<RP>(a, grid_ps, L.st);
+    L.end();
+  }
+
+  // Stage 2 (after the exchanged P sum became the mean): orthogonalise P,
+  // then this process's Q = M^T P into the second exchange buffer (a.qx).
+  static void dp_project(psgd_state* s, const StepArgs& a, Launcher& L) {
+    const int grid_items = std::max(1, std::min(a.n_items, s->sms * 3));
+    const int grid_qr = std::max(1, std::min(a.n_qr, s->sms * 8));
+    gs(s, a, L, 0, false);
+    L.begin(K_PASS2);
+    launch_pass2<RP>(a, s->pass2_src, grid_items, L.st);
+    L.end();
+    L.begin(K_QREDUCE);
+    launch_qreduce<RP>(a, grid_qr, L.st);
+    L.end();
+  }
+
+  // Stage 3 (after the exchanged Q sum became the mean): out = P Q^T.
+  static void dp_finish(psgd_state* s, const StepArgs& a, Launcher& L) {
+    const int grid_fine = std::max(1, std::min(a.n_fitems, s->sms * 2));
+    L.begin(K_PASS3);
+    launch_pass3<RP>(a, 0, grid_fine, L.st);
+    L.end();
+  }
+
   static void errview(psgd_state* s, const StepArgs& a, int mode, cudaStream_t st) {
     const int grid_fine = std::max(1, std::min(a.n_fitems, s->sms * 2));
     launch_pass3<RP>(a, mode, grid_fine, st);
@@ -652,6 +713,20 @@ struct RunCompressed {
   }
 };
 template <int RP>
+struct RunDpBegin {
+  static void run(psgd_state* s, const StepArgs& a, Launcher& L, bool need_fresh, const std::vector<int>& mask) {
+    Ops<RP>::dp_begin(s, a, L, need_fresh, mask);
+  }
+};
+template <int RP>
+struct RunDpProject {
+  static void run(psgd_state* s, const StepArgs& a, Launcher& L) { Ops<RP>::dp_project(s, a, L); }
+};
+template <int RP>
+struct RunDpFinish {
+  static void run(psgd_state* s, const StepArgs& a, Launcher& L) { Ops<RP>::dp_finish(s, a, L); }
+};
+template <int RP>
 struct RunErrView {
   static void run(psgd_state* s, const StepArgs& a, int mode, cudaStream_t st) { Ops<RP>::errview(s, a, mode, st); }
 };
@@ -670,9 +745,15 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
                   int32_t batch, psgd_dtype grad_dtype, int32_t device, psgd_state** out);
 }  // namespace
 
+#ifndef PSGD_SOURCE_HASH
+#define PSGD_SOURCE_HASH "unknown"
+#endif
+
 extern "C" {
 
 const char* psgd_last_error(void) { return g_last_error.c_str(); }
+
+const char* psgd_build_id(void) { return "psgd-source-hash:" PSGD_SOURCE_HASH; }
 
 int psgd_plan(const int64_t* dims, const int32_t* ndims, int32_t n_tensors, int32_t rank, double mcr,
               int32_t* compressed, int32_t* ranks, int64_t* rows, int64_t* cols) {
@@ -809,6 +890,7 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   s->pass2_src = (reread <= 8) ? (s->ef ? 1 : 2) : 0;
   if (s->W == 1 && s->ef) s->pass2_src = 1;
 
+  if (s->dp_world) s->fold_psum = 0;   // P_raw must be dense before the exchange
   const size_t RP = s->RP;
   const int nt = (int)s->cdesc.size();
   std::vector<int> gs_index;
@@ -843,7 +925,26 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   TRY(dalloc(s, (void**)&s->qinit, (size_t)s->q_total * sizeof(float)));
   TRY(dalloc(s, (void**)&s->qdraw, (size_t)s->q_total * sizeof(float)));
   TRY(dalloc(s, (void**)&s->praw_part, (size_t)s->pp_total * sizeof(float)));
-  TRY(dalloc(s, (void**)&s->praw, (size_t)s->p_total * sizeof(float)));
+  if (s->dp_world) {
+    // first exchange: [P_raw | pad to 32 | uncompressed values | flag]; P_raw
+    // is summed straight into it.  Second exchange: Q in the Qf layout.
+    s->xp_unc = (s->p_total + 31) / 32 * 32;
+    s->xp_count = s->xp_unc + s->Nunc + 1;
+    TRY(dalloc(s, (void**)&s->xp, (size_t)s->xp_count * sizeof(float)));
+    s->praw = s->xp;
+    TRY(dalloc(s, (void**)&s->xq, std::max<size_t>(1, (size_t)s->q_total) * sizeof(float)));
+    std::vector<long long> upos, apos;
+    long long acc = 0;
+    for (const Segment& sg : s->unc_segs) {
+      upos.push_back(acc);
+      acc += sg.len;
+    }
+    for (const Segment& sg : s->all_segs) apos.push_back(sg.off);
+    TRY(dupload(s, &s->d_unc_pos, upos));
+    TRY(dupload(s, &s->d_all_pos, apos));
+  } else {
+    TRY(dalloc(s, (void**)&s->praw, (size_t)s->p_total * sizeof(float)));
+  }
   TRY(dalloc(s, (void**)&s->pgs, (size_t)std::max(s->p_total, s->q_total) * sizeof(float)));
   TRY(dalloc(s, (void**)&s->qpart, (size_t)s->qp_total * sizeof(float)));
   TRY(dalloc(s, (void**)&s->tmat, std::max(1, nt) * RP * RP * sizeof(float)));
@@ -870,7 +971,12 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   TRY(zero(s->qinit, (size_t)s->q_total * sizeof(float)));
   TRY(zero(s->qdraw, (size_t)s->q_total * sizeof(float)));
   TRY(zero(s->praw_part, (size_t)s->pp_total * sizeof(float)));
-  TRY(zero(s->praw, (size_t)s->p_total * sizeof(float)));
+  if (s->dp_world) {
+    TRY(zero(s->xp, (size_t)s->xp_count * sizeof(float)));
+    TRY(zero(s->xq, (size_t)s->q_total * sizeof(float)));
+  } else {
+    TRY(zero(s->praw, (size_t)s->p_total * sizeof(float)));
+  }
   TRY(zero(s->ctrl, sizeof(Ctrl)));
   TRY(zero(s->d_status, sizeof(int)));
   s->pending_draw.assign(nt, 0);
@@ -977,6 +1083,7 @@ extern "C" {
 
 int psgd_step(psgd_state* s, const void* const* grads, float* out, float inv_loss_scale, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (s->dp_world) return fail(PSGD_EINVAL, "psgd_step: a data-parallel state steps with psgd_dp_begin/project/finish");
   if (!grads || !out) return fail(PSGD_EINVAL, "grads/out is NULL");
   const size_t gsz = s->dtype == PSGD_F32 ? 4 : 2;
   for (int w = 0; w < s->W; ++w) {
@@ -1109,6 +1216,165 @@ int psgd_step_host(psgd_state* s, const void* const* host_grads, float* host_out
   PSGD_CUDA_TRY(cudaStreamWaitEvent(st, s->ev_free[k], 0));
   s->set_used[k] = 1;
   s->host_calls++;
+  return PSGD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Data-parallel split: one replica per process, the caller's collective sums
+// the two exchange buffers between the three stages ("PowerSGD Hooks",
+// powerSGD_hook steps 2, 3.3 and 3.6).
+// ---------------------------------------------------------------------------
+int psgd_dp_create(const int64_t* dims, const int32_t* ndims, int32_t n_tensors, int32_t world_size,
+                   int32_t rank, int64_t start_iter, double mcr, int32_t use_error_feedback,
+                   int32_t warm_start, float eps, uint64_t random_seed, int32_t batch,
+                   psgd_dtype grad_dtype, int32_t device, psgd_state** out) {
+  if (!out) return fail(PSGD_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (world_size < 1 || world_size > PSGD_MAX_WORLD) return fail(PSGD_EINVAL, "world_size must be in [1, 64]");
+  if (start_iter < 0) return fail(PSGD_EINVAL, "start_powerSGD_iter < 0");
+  if (!(eps >= 0.f)) return fail(PSGD_EINVAL, "orthogonalization_epsilon must be >= 0");
+  if (grad_dtype != PSGD_F32 && grad_dtype != PSGD_F16 && grad_dtype != PSGD_BF16)
+    return fail(PSGD_EINVAL, "grad_dtype");
+  psgd_state* s = new psgd_state();
+  int rc = plan_tensors(dims, ndims, n_tensors, rank, mcr, &s->tensors);
+  if (rc) {
+    delete s;
+    return rc;
+  }
+  for (auto& h : s->tensors) s->N += h.numel;
+  s->dp_world = world_size;
+  // the kernels see one replica (this process's); the W processes' means are
+  // formed from the exchanged sums
+  return create_common(s, 1, rank, start_iter, mcr, use_error_feedback, warm_start, eps, random_seed, batch,
+                       grad_dtype, device, out);
+}
+
+namespace {
+int dp_check(psgd_state* s, int stage, const char* who) {
+  if (!s) return fail(PSGD_EINVAL, std::string(who) + ": state is NULL");
+  if (!s->dp_world) return fail(PSGD_EINVAL, std::string(who) + ": not a data-parallel state (psgd_dp_create)");
+  if (s->dp_stage != stage)
+    return fail(PSGD_EINVAL, std::string(who) + ": called out of order (begin, project, finish, step after step)");
+  return PSGD_OK;
+}
+
+StepArgs dp_args(psgd_state* s) {
+  StepArgs a = make_args(s);
+  a.grads.p[0] = s->dp_grad;
+  a.out = s->dp_out;
+  a.scale = s->dp_scale;
+  a.vec_ok = ((uintptr_t)s->dp_out % 16 == 0) &&
+             ((uintptr_t)s->dp_grad % (s->dtype == PSGD_F32 ? 16 : 8) == 0);
+  return a;
+}
+
+int dp_grid(psgd_state* s, long long work) {
+  return (int)std::max(1LL, std::min<long long>((work + kThreads - 1) / kThreads, (long long)s->sms * 4));
+}
+}  // namespace
+
+int psgd_dp_begin(psgd_state* s, const void* grad, float* out, float inv_loss_scale, void* stream, float** exchange,
+                  int64_t* count) {
+  int rc = dp_check(s, 0, "psgd_dp_begin");
+  if (rc) return rc;
+  if (!grad || !out || !exchange || !count) return fail(PSGD_EINVAL, "psgd_dp_begin: NULL pointer");
+  const size_t gsz = s->dtype == PSGD_F32 ? 4 : 2;
+  if (ranges_overlap(grad, s->N * gsz, out, s->N * 4) && !(grad == (const void*)out && s->dtype == PSGD_F32))
+    return fail(PSGD_EINVAL, "psgd_dp_begin: out overlaps grad (only out == grad for F32 is allowed)");
+  DeviceGuard g(s->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  s->dp_grad = grad;
+  s->dp_out = out;
+  s->dp_scale = inv_loss_scale;
+  s->dp_vanilla = s->iter < s->start_iter;
+  s->dp_compressed = !s->dp_vanilla && !s->cdesc.empty();
+  const bool need_fresh = s->dp_compressed && ((!s->warm) || s->compressed_launched == 0);
+  std::vector<int> mask(s->cdesc.size(), 0);
+  if (need_fresh) {
+    for (size_t c = 0; c < s->cdesc.size(); ++c) {
+      mask[c] = s->pending_draw[c] ? 0 : 1;
+      s->pending_draw[c] = 0;
+    }
+  }
+  StepArgs a = dp_args(s);
+  Launcher L{s, st};
+  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, sizeof(int), st));
+  if (s->dp_vanilla) {
+    // before start_powerSGD_iter the hook allreduces the whole bucket: the
+    // exchange buffer is `out`, holding this replica's unscaled gradient
+    L.begin(K_DP);
+    launch_dp_pack(a, s->d_all, s->d_all_pos, (int)s->all_segs.size(), out, nullptr, dp_grid(s, s->N), st);
+    L.end();
+    *exchange = out;
+    *count = s->N;
+  } else {
+    PSGD_CUDA_TRY(cudaMemsetAsync(s->xp + s->xp_count - 1, 0, sizeof(float), st));
+    if (s->dp_compressed) by_rp<RunDpBegin>(s->RP, s, a, L, need_fresh, mask);
+    L.begin(K_DP);
+    launch_dp_pack(a, s->d_unc, s->d_unc_pos, (int)s->unc_segs.size(), s->xp + s->xp_unc,
+                   s->xp + s->xp_count - 1, dp_grid(s, s->Nunc), st);
+    L.end();
+    *exchange = s->xp;
+    *count = s->xp_count;
+  }
+  PSGD_CUDA_TRY(cudaGetLastError());
+  if (s->dp_compressed) s->compressed_launched++;
+  s->dp_stage = 1;
+  return PSGD_OK;
+}
+
+int psgd_dp_project(psgd_state* s, void* stream, float** exchange, int64_t* count) {
+  int rc = dp_check(s, 1, "psgd_dp_project");
+  if (rc) return rc;
+  if (!exchange || !count) return fail(PSGD_EINVAL, "psgd_dp_project: NULL pointer");
+  DeviceGuard g(s->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  *exchange = nullptr;
+  *count = 0;
+  if (!s->dp_vanilla) {
+    StepArgs a = dp_args(s);
+    a.qx = s->xq;
+    Launcher L{s, st};
+    L.begin(K_DP);
+    launch_dp_open(a, s->xp, s->p_total, s->xp + s->xp_count - 1, 1.f / (float)s->dp_world,
+                   dp_grid(s, s->p_total), st);
+    L.end();
+    if (s->dp_compressed) {
+      by_rp<RunDpProject>(s->RP, s, a, L);
+      *exchange = s->xq;
+      *count = s->q_total;
+    }
+    PSGD_CUDA_TRY(cudaGetLastError());
+  }
+  s->dp_stage = 2;
+  return PSGD_OK;
+}
+
+int psgd_dp_finish(psgd_state* s, void* stream) {
+  int rc = dp_check(s, 2, "psgd_dp_finish");
+  if (rc) return rc;
+  DeviceGuard g(s->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  StepArgs a = dp_args(s);
+  Launcher L{s, st};
+  const float invW = 1.f / (float)s->dp_world;
+  L.begin(K_DP);
+  if (s->dp_vanilla) {
+    launch_dp_close(a, nullptr, s->d_all, s->d_all_pos, (int)s->all_segs.size(), s->dp_out, invW, 1,
+                    dp_grid(s, s->N), st);
+  } else {
+    launch_dp_close(a, s->dp_compressed ? s->xq : nullptr, s->d_unc, s->d_unc_pos, (int)s->unc_segs.size(),
+                    s->xp + s->xp_unc, invW, 0, dp_grid(s, std::max(s->q_total, s->Nunc)), st);
+  }
+  L.end();
+  if (s->dp_compressed) by_rp<RunDpFinish>(s->RP, s, a, L);
+  L.begin(K_COMMIT);
+  launch_commit(s->ctrl, s->dp_compressed ? 1 : 0, s->d_status, st);
+  L.end();
+  PSGD_CUDA_TRY(cudaGetLastError());
+  PSGD_CUDA_TRY(cudaMemcpyAsync(s->h_status, s->d_status, sizeof(int), cudaMemcpyDeviceToHost, st));
+  s->iter++;
+  s->dp_stage = 0;
   return PSGD_OK;
 }
 

@@ -62,12 +62,13 @@ __global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
 }
 
 // Q'(j, k) = sum over row blocks of the partials, in row-block order, written
-// k-major into the next half of Qf.  Each work item is a chunk of one
+// k-major into the next half of Qf (or, in the data-parallel split, into the
+// exchange buffer a.qx, same layout).  Each work item is a chunk of one
 // tensor's RP * m values, four per thread.
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
   if (a.ctrl->flag) return;
-  float* Q = a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
+  float* Q = a.qx ? a.qx : a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
   for (int it = blockIdx.x; it < a.n_qr; it += gridDim.x) {
     const GsItem gi = a.qr_items[it];
     const TensorDesc td = a.tensors[gi.t];

@@ -51,6 +51,8 @@ struct StepArgs {
   float* praw;        // summed P_raw
   float* pgs;         // first Gram-Schmidt sweep output (P and Q share it)
   float* qpart;       // pass-2 partials
+  float* qx;          // data-parallel split: k_qreduce writes this process's Q
+                      // here (the exchange buffer, Q layout) instead of Qf
   float2* gram;       // per Gram-Schmidt item RP x RP (double-float)
   float2* gram_t;     // per tensor RP x RP, the items' sum
   float* tmat;        // per tensor RP x RP transform

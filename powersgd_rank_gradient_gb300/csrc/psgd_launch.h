@@ -25,5 +25,13 @@ void launch_mean(const StepArgs& a, const Segment* segs, int nsegs, int grid, cu
 void launch_commit(Ctrl* ctrl, int compressed, int* status, cudaStream_t s);
 void launch_randn(const StepArgs& a, const int* mask, unsigned long long seed,
                   unsigned long long counter, int tbase, int rp, int grid, cudaStream_t s);
+// data-parallel split: pack this replica's values for the exchange, turn the
+// exchanged sums into means
+void launch_dp_pack(const StepArgs& a, const Segment* segs, const long long* pos, int nsegs, float* dst,
+                    float* xflag, int grid, cudaStream_t s);
+void launch_dp_open(const StepArgs& a, float* xp, long long n, const float* xflag, float invW, int grid,
+                    cudaStream_t s);
+void launch_dp_close(const StepArgs& a, const float* xq, const Segment* segs, const long long* pos, int nsegs,
+                     const float* src, float invW, int check_finite, int grid, cudaStream_t s);
 
 }  // namespace psgd

@@ -96,6 +96,102 @@ void launch_commit(Ctrl* ctrl, int compressed, int* status, cudaStream_t s) {
   k_commit<<<1, 32, 0, s>>>(ctrl, compressed, status);
 }
 
+// ---------------------------------------------------------------------------
+// Data-parallel split (one replica per process).  "PowerSGD Hooks": the hook
+// allreduces the uncompressed batch (step 2), the Ps (step 3.3) and the Qs
+// (step 3.6); the caller sums the exchange buffers across the processes and
+// these kernels turn the sums into means ("Default Communication Hooks",
+// allreduce_hook: the mean).
+// ---------------------------------------------------------------------------
+
+// dst[pos[i] + j] = g[seg_i.off + j] * s over the listed segments (this
+// replica's unscaled values, packed); a non-finite value, or the pass-1 flag
+// of this process (ctrl->flag), raises *xflag to 1 (when xflag is given).
+template <typename GT>
+__global__ void __launch_bounds__(kThreads) k_dp_pack(const StepArgs a, const Segment* __restrict__ segs,
+                                                      const long long* __restrict__ pos, int nsegs,
+                                                      float* __restrict__ dst, float* xflag) {
+  const GT* g = reinterpret_cast<const GT*>(a.grads.p[0]);
+  int bad = 0;
+  for (int it = blockIdx.x; it < nsegs; it += gridDim.x) {
+    const Segment sg = segs[it];
+    const long long p0 = pos[it];
+    for (int j = threadIdx.x; j < sg.len; j += kThreads) {
+      float v[1];
+      load_grad<1, GT>(g + sg.off + j, v);
+      const float x = v[0] * a.scale;
+      bad |= !isfinite(x);
+      dst[p0 + j] = x;
+    }
+  }
+  if (xflag) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.ctrl->flag) bad = 1;
+    if (bad) *xflag = 1.f;
+  }
+}
+
+// After the caller's sum of the first exchange: a raised flag on any process
+// skips the step here too; otherwise P_raw = sum / W in place.
+__global__ void __launch_bounds__(kThreads) k_dp_open(const StepArgs a, float* __restrict__ xp, long long n,
+                                                      const float* __restrict__ xflag, float invW) {
+  if (*xflag != 0.f) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.ctrl->flag = 1;
+    return;
+  }
+  for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < n; i += (long long)gridDim.x * kThreads)
+    xp[i] *= invW;
+}
+
+// After the caller's sum of the second exchange: Q = sum / W into the next
+// half of Qf (when xq is given), and out = sum / W over the listed segments
+// from the packed sums.  check_finite (the vanilla phase, whose exchange is
+// `out` itself): a non-finite mean raises the flag, so every process skips.
+__global__ void __launch_bounds__(kThreads) k_dp_close(const StepArgs a, const float* __restrict__ xq,
+                                                       const Segment* __restrict__ segs,
+                                                       const long long* __restrict__ pos, int nsegs,
+                                                       const float* src, float invW, int check_finite) {
+  if (a.ctrl->flag) return;
+  if (xq) {
+    float* Q = a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
+    for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < a.q_total;
+         i += (long long)gridDim.x * kThreads)
+      Q[i] = xq[i] * invW;
+  }
+  int bad = 0;
+  for (int it = blockIdx.x; it < nsegs; it += gridDim.x) {
+    const Segment sg = segs[it];
+    const long long p0 = pos[it];
+    for (int j = threadIdx.x; j < sg.len; j += kThreads) {
+      const float x = src[p0 + j] * invW;
+      bad |= !isfinite(x);
+      a.out[sg.off + j] = x;
+    }
+  }
+  if (check_finite && __any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
+}
+
+void launch_dp_pack(const StepArgs& a, const Segment* segs, const long long* pos, int nsegs, float* dst,
+                    float* xflag, int grid, cudaStream_t s) {
+  if (nsegs == 0 && !xflag) return;
+  grid = nsegs > 0 ? grid : 1;
+  if (a.gtype == 1)
+    k_dp_pack<__half><<<grid, kThreads, 0, s>>>(a, segs, pos, nsegs, dst, xflag);
+  else if (a.gtype == 2)
+    k_dp_pack<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a, segs, pos, nsegs, dst, xflag);
+  else
+    k_dp_pack<float><<<grid, kThreads, 0, s>>>(a, segs, pos, nsegs, dst, xflag);
+}
+
+void launch_dp_open(const StepArgs& a, float* xp, long long n, const float* xflag, float invW, int grid,
+                    cudaStream_t s) {
+  k_dp_open<<<grid, kThreads, 0, s>>>(a, xp, n, xflag, invW);
+}
+
+void launch_dp_close(const StepArgs& a, const float* xq, const Segment* segs, const long long* pos, int nsegs,
+                     const float* src, float invW, int check_finite, int grid, cudaStream_t s) {
+  k_dp_close<<<grid, kThreads, 0, s>>>(a, xq, segs, pos, nsegs, src, invW, check_finite);
+}
+
 // Philox4x32 with 10 rounds (Salmon, Moraes, Dror and Shaw, "Parallel random
 // numbers: as easy as 1, 2, 3", SC 2011): each round multiplies counter
 // words 0 and 2 by the round constants, swaps the halves crosswise and mixes

@@ -25,8 +25,11 @@ static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
 
 namespace {
 
+// Device ordinals this entry point serves (one looked-up address each).
+constexpr int kMaxDevices = 64;
+
 std::mutex g_static_mu;
-float* g_static_ptr[PSGD_MAX_WORLD] = {nullptr};  // per device ordinal
+float* g_static_ptr[kMaxDevices] = {nullptr};  // per device ordinal
 
 constexpr int kStaticRows = kRowBlock;
 
@@ -134,17 +137,22 @@ extern "C" int psgd_project_q_static(const float* dev_m, const float* dev_p, flo
   int rp = 1;
   while (rp < rank) rp <<= 1;
   const long long rblocks = (rows + kStaticRows - 1) / kStaticRows;
-  if (rblocks * rp * cols > kStaticScratchFloats) {
-    const std::string msg = "psgd_project_q_static: ceil(rows / 512) * " + std::to_string(rp) + " * cols = " +
-                            std::to_string(rblocks * rp * cols) + " partial sums exceed the static scratch of " +
+  // ceil(rows / 512) * rp * cols <= kStaticScratchFloats, tested by division
+  // so that no product of caller-supplied sizes can overflow
+  if (cols > kStaticScratchFloats / rp || rblocks > kStaticScratchFloats / (rp * cols)) {
+    const std::string msg = "psgd_project_q_static: ceil(rows / 512) = " + std::to_string(rblocks) + " row blocks x " +
+                            std::to_string(rp) + " x " + std::to_string(cols) +
+                            " cols of partial sums exceed the static scratch of " +
                             std::to_string(kStaticScratchFloats) + " floats";
     return psgd_internal_set_error(PSGD_EINVAL, msg.c_str());
   }
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= PSGD_MAX_WORLD) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return psgd_internal_set_error(PSGD_ECUDA, "psgd_project_q_static: no current CUDA device");
   }
+  if (dev < 0 || dev >= kMaxDevices)
+    return psgd_internal_set_error(PSGD_EINVAL, "psgd_project_q_static: device ordinals above 63 are not served");
   float* scratch = nullptr;
   {
     // First call on this device: look up the device address of the static

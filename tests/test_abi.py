@@ -31,6 +31,17 @@ def test_header_symbols_are_exported():
     assert sorted(_lib.EXPORTS) == names
 
 
+def test_loaded_library_matches_its_sources():
+    """The library carries the hash of the sources, header, flags and compiler
+    it was built from; the loaded one must match the files in this tree (no
+    stale binary)."""
+    from powersgd_rank_gradient_gb300 import build
+
+    bid = _lib.lib().psgd_build_id().decode()
+    assert bid == "psgd-source-hash:" + build.source_hash()
+    assert build.library_hash() == build.source_hash()
+
+
 def test_plan_matches_gate_golden():
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "gate_cases.json")))
     for case in g["cases"]:

@@ -177,6 +177,77 @@ def test_zero_columns_with_epsilon():
     st.close()
 
 
+def test_zero_p_column_eps0_gives_nan_like_oracle():
+    """"PowerSGD State" item 4: with orthogonalization_epsilon = 0 an all-zero
+    column of P divides zero by zero.  The first column of Q lies on a
+    coordinate where the gradient is zero, so column 0 of P = M Q is exactly
+    zero; the oracle's Gram-Schmidt then gives NaN in that column, and the NaN
+    reaches every later column through the projections (the golden case
+    "zero column, eps=0").  The GPU must give NaN in the same positions of P
+    and of the output, while the uncompressed vector in the same bucket keeps
+    its finite mean.  Data only: nothing traps."""
+    import oracle
+
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    n, m, r = 1024, 512, 4
+    shapes = [(n, m), (300,)]
+    rng = np.random.default_rng(11)
+    zc = 37
+    g = rng.standard_normal((n, m)).astype(np.float32)
+    g[:, zc] = 0.0
+    vec = rng.standard_normal(300).astype(np.float32)
+    bucket = np.concatenate([g.reshape(-1), vec])
+    draw = rng.standard_normal((m, r)).astype(np.float32)
+    draw[:, 0] = 0.0
+    draw[zc, 0] = 1.0
+    st = PowerSGDState(shapes, 1, matrix_approximation_rank=r, start_powerSGD_iter=0,
+                       orthogonalization_epsilon=0.0, device=DEV)
+    ref = oracle.PowerSGDOracle(shapes=shapes, world_size=1, matrix_approximation_rank=r,
+                                start_powerSGD_iter=0, orthogonalization_epsilon=0.0)
+    st.set_q(0, draw, is_draw=True)
+    ref.set_q_draw(0, draw.astype(np.float64))
+    out = st.step([torch.from_numpy(bucket).to(DEV)])
+    assert not st.status()      # the inputs are finite: the step is not skipped
+    _, exp = ref.step([bucket.astype(np.float64)])
+    got = out.double().cpu().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(exp))
+    assert np.isnan(exp[:n * m]).all()            # every P column is NaN -> so is P Q^T
+    fin = ~np.isnan(exp)
+    assert rel(got[fin], exp[fin]) <= 1e-4        # the vector's plain mean
+    p_gpu = st.get_p(0).double().numpy()
+    assert np.array_equal(np.isnan(p_gpu), np.isnan(ref.last_p[0]))
+    st.close()
+
+
+@pytest.mark.parametrize("rank,eps", [(8, 0.0), (8, 1e-8), (32, 0.0)])
+def test_zero_gradient_columns_pass_through(rank, eps):
+    """The second reading of the edge case with three all-zero columns: the
+    gradient matrix itself has three zero columns (4096 x 1024, Q drawn at
+    random).  Then Q' = M^T P has zero rows there, P Q'^T zero columns and the
+    residual M - P Q'^T stays zero there, in exact arithmetic and on the GPU
+    (0 * x sums to exactly 0), step after step; everything else matches the
+    oracle."""
+    shapes = [(4096, 1024)]
+    n, m = shapes[0]
+    rng = np.random.default_rng(21)
+    zero_cols = np.sort(rng.permutation(m)[:3])
+    pair = Pair(shapes, 1, rank, DEV, start_powerSGD_iter=0, orthogonalization_epsilon=eps)
+    for step in range(3):
+        g = grads_for(shapes, 1, step)[0].reshape(n, m)
+        g[:, zero_cols] = 0.0
+        skipped, status, out, exp = pair.step([g.reshape(-1)])
+        assert not skipped
+        pair.compare(out, exp, label=f"zero cols r={rank} eps={eps} step {step}")
+        got = out.cpu().numpy().reshape(n, m)
+        assert np.all(got[:, zero_cols] == 0.0)
+        e = pair.gpu.get_error(0).cpu().numpy().reshape(n, m)
+        assert np.all(e[:, zero_cols] == 0.0)
+        q = pair.gpu.get_q(0).numpy()
+        assert np.all(q[zero_cols, :] == 0.0)
+    pair.close()
+
+
 def test_fp16_scaled_with_inf_is_skipped():
     """fp16 gradients pre-scaled by 65536 and unscaled in pass 1; a step with
     one +inf is skipped with the state left bit for bit, the next clean step
@@ -366,8 +437,8 @@ def test_empty_and_vector_only_buckets():
 
 @pytest.mark.parametrize("rank", [1, 2, 4, 8, 16, 32])
 def test_rank_sweep_8192(rank):
-    """8192 x 8192, W=1, N(0,1): two warm-started steps per rank."""
-    _run([(8192, 8192)], 1, rank, 2, min_compression_rate=2.0, label=f"8192 r={rank}")
+    """8192 x 8192, W=1, N(0,1): three warm-started steps per rank."""
+    _run([(8192, 8192)], 1, rank, 3, min_compression_rate=2.0, label=f"8192 r={rank}")
 
 
 def test_step_host_matches_device_path():

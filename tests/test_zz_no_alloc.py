@@ -34,7 +34,20 @@ def _static_q(L, m_dev, p_host, rows, cols, rank):
     return q_dev.cpu().numpy()
 
 
-@pytest.mark.parametrize("rows,cols,rank", [(1100, 700, 4), (777, 1030, 3)])
+# Every padded-rank instantiation of the kernel (1, 2, 4, 8, 16, 32 -- 4, 2
+# and 1 columns per thread), each with a column count that is not a multiple
+# of 4 (the element-by-element path) and a partial last row block; ranks 4
+# and 32 also with aligned columns (the vector path), rank 16 with a column
+# tile narrower than one thread's share at the edge.
+@pytest.mark.parametrize("rows,cols,rank", [
+    (513, 130, 1), (513, 131, 1),
+    (650, 1001, 2),
+    (1100, 700, 4), (777, 1030, 3),
+    (900, 517, 5),
+    (700, 333, 8),
+    (1100, 900, 16), (1100, 901, 16),
+    (600, 2000, 32), (600, 2001, 32),
+])
 def test_static_projection_matches_step(rows, cols, rank):
     from powersgd_rank_gradient_gb300 import PowerSGDState, _lib
 
@@ -63,6 +76,10 @@ def test_static_projection_rejects_oversize():
     ptr = ctypes.c_void_p(x.data_ptr())
     # ceil(5000 / 512) * 32 * 8192 partial sums exceed the 2 Mi-float array
     rc = L.psgd_project_q_static(ptr, ptr, ptr, 5000, 8192, 32, None)
+    assert rc == _lib.PSGD_EINVAL
+    assert b"static scratch" in L.psgd_last_error()
+    # sizes whose product would overflow 64 bits are rejected, not launched
+    rc = L.psgd_project_q_static(ptr, ptr, ptr, 2**62, 2**40, 32, None)
     assert rc == _lib.PSGD_EINVAL
     assert b"static scratch" in L.psgd_last_error()
     assert L.psgd_project_q_static(None, ptr, ptr, 4, 4, 1, None) == _lib.PSGD_EINVAL
