@@ -109,9 +109,10 @@ int plan_tensors(const int64_t* dims, const int32_t* ndims, int32_t n, int32_t r
 }
 
 enum Kind { K_MEAN = 0, K_PASS1, K_GRAM, K_SOLVE, K_APPLY, K_PASS2, K_QREDUCE, K_PASS3, K_COMMIT, K_RANDN,
-            K_PSUM, K_DP, K_COUNT };
+            K_PSUM, K_DP, K_IMG, K_COUNT };
 const char* kKindNames[K_COUNT] = {"mean", "pass1", "gs_gram", "gs_solve", "gs_apply",
-                                   "pass2", "qreduce", "pass3", "commit", "randn", "psum", "dp_exchange"};
+                                   "pass2", "qreduce", "pass3", "commit", "randn", "psum", "dp_exchange",
+                                   "images"};
 
 struct EventPair {
   cudaEvent_t a, b;
@@ -141,6 +142,9 @@ struct psgd_state {
   std::vector<Item> items;    // pass 2
   std::vector<Item> fitems;   // pass 3, error views
   std::vector<Item> p1items;  // pass 1
+  std::vector<Item> t3items;  // tensor-core pass 3 (ranks 16 and 32)
+  std::vector<Item> t2items;  // tensor-core pass 2 (ranks 16 and 32)
+  std::vector<Item> t1items;  // tensor-core pass 1 (ranks 16 and 32)
   std::vector<GsItem> ps;     // P partial reduction chunks
   std::vector<GsItem> qr;     // Q partial reduction chunks
   std::vector<GsItem> gsp, gsq;
@@ -158,6 +162,11 @@ struct psgd_state {
   Item* d_items = nullptr;
   Item* d_fitems = nullptr;
   Item* d_p1items = nullptr;
+  Item* d_t3items = nullptr;
+  Item* d_t2items = nullptr;
+  Item* d_t1items = nullptr;
+  float* img = nullptr;        // tensor-core operand images (ranks 16 and 32)
+  long long img_total = 0;
   GsItem* d_ps = nullptr;
   GsItem* d_qr = nullptr;
   GsItem* d_gsp = nullptr;
@@ -308,6 +317,9 @@ void build_plan(psgd_state* s) {
   s->items.clear();
   s->fitems.clear();
   s->p1items.clear();
+  s->t3items.clear();
+  s->t2items.clear();
+  s->t1items.clear();
   s->qr.clear();
   s->ps.clear();
   s->gsp.clear();
@@ -318,7 +330,7 @@ void build_plan(psgd_state* s) {
   s->gsq_count.clear();
   s->unc_segs.clear();
   s->all_segs.clear();
-  long long c_off = 0, p_off = 0, q_off = 0, pp_off = 0, qp_off = 0, e_off = 0;
+  long long c_off = 0, p_off = 0, q_off = 0, pp_off = 0, qp_off = 0, e_off = 0, i_off = 0;
   long long unc = 0;
   // pass 2: row blocks of kRowBlock rows, shorter for small buckets so that
   // there are several items per resident CTA (one Q partial per item)
@@ -355,6 +367,21 @@ void build_plan(psgd_state* s) {
       td.qp_off = qp_off;
       td.e_off = e_off;
       td.vec = (h.cols % 4 == 0) && (h.offset % 4 == 0);
+      // operand images (ranks 16 and 32): hi and lo of P's and Q's row
+      // images (rows padded to 128) and chunk images (RP x 32 per 32 rows)
+      td.pi_off = td.qi_off = td.pti_off = td.qti_off = 0;
+      if (RP >= 16) {
+        const long long npad = (h.rows + 127) / 128 * 128, mpad = (h.cols + 127) / 128 * 128;
+        const long long nch = (h.rows + 31) / 32, mch = (h.cols + 31) / 32;
+        td.pi_off = i_off;
+        i_off += 2 * npad * 32;
+        td.qi_off = i_off;
+        i_off += 2 * mpad * 32;
+        td.pti_off = i_off;
+        i_off += 2 * nch * RP * 32;
+        td.qti_off = i_off;
+        i_off += 2 * mch * RP * 32;
+      }
       if (td.vec) s->any_aligned = 1;
       if (!td.vec || td.valid < (long long)td.n * td.m) s->any_unaligned = 1;
       h.cidx = (int)s->cdesc.size();
@@ -382,6 +409,7 @@ void build_plan(psgd_state* s) {
   s->Nc = s->N - unc;
   s->p_total = p_off;
   s->q_total = q_off;
+  s->img_total = i_off;
   s->pp_total = pp_off;
   s->qp_total = qp_off;
 
@@ -450,6 +478,60 @@ void build_plan(psgd_state* s) {
     if (RP <= 8 && nc < 6LL * s->sms * rows1 * CT1) rows1 /= 2;
   }
   make_items(&s->p1items, rows1, 0, true);
+  // tensor-core pass 3 (ranks 16 and 32): 128 x 256 items of the tensors
+  // whose rows are 16-byte aligned in the bucket and which the bucket wholly
+  // backs, in (tensor, row block, column tile) order so that a CTA's
+  // contiguous range of items shares row blocks of P
+  if (RP >= 16) {
+    for (size_t c = 0; c < s->cdesc.size(); ++c) {
+      const TensorDesc& td = s->cdesc[c];
+      if (!td.vec || td.valid != (long long)td.n * td.m) continue;
+      for (int r0 = 0; r0 < td.n; r0 += 128)
+        for (int c0 = 0; c0 < td.m; c0 += 256) {
+          Item it;
+          it.t = (int)c;
+          it.row0 = r0;
+          it.nrows = std::min(128, td.n - r0);
+          it.col0 = c0;
+          it.ncols = std::min(256, td.m - c0);
+          it.rb = 0;
+          it.ct = 0;
+          it.pad = 0;
+          s->t3items.push_back(it);
+        }
+    }
+    // tensor-core pass 1: the pass-1 items whose rows are 16-byte aligned in
+    // the bucket and which the bucket wholly backs, in (tensor, row block,
+    // column tile) order; the element kernel takes the rest
+    for (const Item& it : s->p1items) {
+      const TensorDesc& td = s->cdesc[it.t];
+      if (td.vec && (long long)(it.row0 + it.nrows) * td.m <= td.valid) s->t1items.push_back(it);
+    }
+    std::stable_sort(s->t1items.begin(), s->t1items.end(), [](const Item& x, const Item& y) {
+      if (x.t != y.t) return x.t < y.t;
+      if (x.row0 != y.row0) return x.row0 < y.row0;
+      return x.col0 < y.col0;
+    });
+    // tensor-core pass 2: one row block x 128 columns of every compressed
+    // tensor (its sources, the Mbar scratch and the store, always have
+    // 16-byte aligned rows)
+    for (size_t c = 0; c < s->cdesc.size(); ++c) {
+      const TensorDesc& td = s->cdesc[c];
+      for (int r0 = 0; r0 < td.n; r0 += s->row_block)
+        for (int c0 = 0; c0 < td.m; c0 += 128) {
+          Item it;
+          it.t = (int)c;
+          it.row0 = r0;
+          it.nrows = std::min(s->row_block, td.n - r0);
+          it.col0 = c0;
+          it.ncols = std::min(128, td.m - c0);
+          it.rb = r0 / s->row_block;
+          it.ct = 0;
+          it.pad = 0;
+          s->t2items.push_back(it);
+        }
+    }
+  }
   // P_raw: with at most two column-tile partials per row on average the first
   // Gram kernel adds them as it reads P (one launch fewer); with more, a
   // separate reduction with more loads in flight is faster
@@ -515,6 +597,13 @@ StepArgs make_args(psgd_state* s) {
   a.n_fitems = (int)s->fitems.size();
   a.p1items = s->d_p1items;
   a.n_p1items = (int)s->p1items.size();
+  a.img = s->img;
+  a.t3items = s->d_t3items;
+  a.n_t3 = (int)s->t3items.size();
+  a.t2items = s->d_t2items;
+  a.n_t2 = (int)s->t2items.size();
+  a.t1items = s->d_t1items;
+  a.n_t1 = (int)s->t1items.size();
   a.ps_items = s->d_ps;
   a.n_ps = (int)s->ps.size();
   a.qr_items = s->d_qr;
@@ -613,6 +702,16 @@ struct Ops {
     L.end();
   }
 
+  // ranks 16 and 32: the factor images the tensor-core passes read
+  static void images(psgd_state* s, const StepArgs& a, Launcher& L, int mode) {
+    if constexpr (RP >= 16) {
+      const int n = (mode == 0) ? a.n_gsp : (mode == 3 ? a.n_gsp + a.n_gsq : a.n_gsq);
+      L.begin(K_IMG);
+      launch_images<RP>(a, mode, std::max(1, std::min(n, s->sms * 4)), L.st);
+      L.end();
+    }
+  }
+
   static void compressed(psgd_state* s, const StepArgs& a, Launcher& L, bool need_fresh,
                          const std::vector<int>& mask) {
     const int grid_items = std::max(1, std::min(a.n_items, s->sms * 3));
@@ -628,16 +727,19 @@ struct Ops {
       L.end();
       gs(s, a, L, 1);
     }
+    images(s, a, L, 2);
     L.begin(K_PASS1);
     launch_pass1<RP>(a, grid_p1, L.st);
     L.end();
     gs(s, a, L, 0);
+    images(s, a, L, 0);
     L.begin(K_PASS2);
     launch_pass2<RP>(a, s->pass2_src, grid_items, L.st);
     L.end();
     L.begin(K_QREDUCE);
     launch_qreduce<RP>(a, grid_qr, L.st);
     L.end();
+    images(s, a, L, 1);
     L.begin(K_PASS3);
     launch_pass3<RP>(a, 0, grid_fine, L.st);
     L.end();
@@ -658,6 +760,7 @@ struct Ops {
       L.end();
       gs(s, a, L, 1);
     }
+    images(s, a, L, 2);
     L.begin(K_PASS1);
     launch_pass1<RP>(a, grid_p1, L.st);
     L.end();
@@ -672,6 +775,7 @@ struct Ops {
     const int grid_items = std::max(1, std::min(a.n_items, s->sms * 3));
     const int grid_qr = std::max(1, std::min(a.n_qr, s->sms * 8));
     gs(s, a, L, 0, false);
+    images(s, a, L, 0);
     L.begin(K_PASS2);
     launch_pass2<RP>(a, s->pass2_src, grid_items, L.st);
     L.end();
@@ -683,6 +787,7 @@ struct Ops {
   // Stage 3 (after the exchanged Q sum became the mean): out = P Q^T.
   static void dp_finish(psgd_state* s, const StepArgs& a, Launcher& L) {
     const int grid_fine = std::max(1, std::min(a.n_fitems, s->sms * 2));
+    images(s, a, L, 1);
     L.begin(K_PASS3);
     launch_pass3<RP>(a, 0, grid_fine, L.st);
     L.end();
@@ -725,6 +830,10 @@ struct RunDpProject {
 template <int RP>
 struct RunDpFinish {
   static void run(psgd_state* s, const StepArgs& a, Launcher& L) { Ops<RP>::dp_finish(s, a, L); }
+};
+template <int RP>
+struct RunImages {
+  static void run(psgd_state* s, const StepArgs& a, Launcher& L, int mode) { Ops<RP>::images(s, a, L, mode); }
 };
 template <int RP>
 struct RunErrView {
@@ -898,6 +1007,10 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   gs_index.insert(gs_index.end(), s->gsp_count.begin(), s->gsp_count.end());
   gs_index.insert(gs_index.end(), s->gsq_first.begin(), s->gsq_first.end());
   gs_index.insert(gs_index.end(), s->gsq_count.begin(), s->gsq_count.end());
+  auto zero_now = [&](void* p, size_t n) -> int {
+    if (p && n) PSGD_CUDA_TRY(cudaMemset(p, 0, n));
+    return PSGD_OK;
+  };
 #define TRY(x)                  \
   do {                          \
     int rc_ = (x);              \
@@ -910,6 +1023,13 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   TRY(dupload(s, &s->d_items, s->items));
   TRY(dupload(s, &s->d_fitems, s->fitems));
   TRY(dupload(s, &s->d_p1items, s->p1items));
+  TRY(dupload(s, &s->d_t3items, s->t3items));
+  TRY(dupload(s, &s->d_t2items, s->t2items));
+  TRY(dupload(s, &s->d_t1items, s->t1items));
+  if (s->img_total) {
+    TRY(dalloc(s, (void**)&s->img, (size_t)s->img_total * sizeof(float)));
+    TRY(zero_now(s->img, (size_t)s->img_total * sizeof(float)));
+  }
   TRY(dupload(s, &s->d_ps, s->ps));
   TRY(dupload(s, &s->d_qr, s->qr));
   TRY(dupload(s, &s->d_gsp, s->gsp));
@@ -1009,7 +1129,7 @@ namespace {
 int enqueue_step(psgd_state* s, const StepArgs& a, cudaStream_t st, bool vanilla, bool compressed_step,
                  bool need_fresh, const std::vector<int>& mask) {
   Launcher L{s, st};
-  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, sizeof(int), st));
+  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, 2 * sizeof(int), st));   // flag, timeout
   const int grid_seg = std::max(1, std::min<int>((int)s->all_segs.size(), s->sms * 4));
   if (vanilla) {
     // before start_powerSGD_iter calls the hook only averages the replicas
@@ -1298,7 +1418,7 @@ int psgd_dp_begin(psgd_state* s, const void* grad, float* out, float inv_loss_sc
   }
   StepArgs a = dp_args(s);
   Launcher L{s, st};
-  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, sizeof(int), st));
+  PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, 2 * sizeof(int), st));   // flag, timeout
   if (s->dp_vanilla) {
     // before start_powerSGD_iter the hook allreduces the whole bucket: the
     // exchange buffer is `out`, holding this replica's unscaled gradient
@@ -1392,6 +1512,7 @@ int psgd_step_status(psgd_state* s, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
   DeviceGuard g(s->device);
   PSGD_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+  if (*s->h_status == 2) return fail(PSGD_ETIMEOUT, "a bounded device-side wait gave up; the step was not committed");
   return *s->h_status ? PSGD_SKIPPED_NONFINITE : PSGD_OK;
 }
 
@@ -1471,6 +1592,12 @@ int psgd_set_q(psgd_state* s, int32_t t, const float* host_in, int32_t is_draw) 
   PSGD_CUDA_TRY(cudaMemset(s->Pf + (size_t)cur * s->p_total, 0, (size_t)s->p_total * 4));
   PSGD_CUDA_TRY(cudaMemcpy(s->Qf + (size_t)cur * s->q_total + td.q_off, buf.data(), buf.size() * 4,
                            cudaMemcpyHostToDevice));
+  if (s->img) {
+    // the tensor-core pass 1 reads the committed factors through their images
+    Launcher L{s, (cudaStream_t)0};
+    by_rp<RunImages>(s->RP, s, a, L, 3);
+    PSGD_CUDA_TRY(cudaGetLastError());
+  }
   int one = 1;
   PSGD_CUDA_TRY(cudaMemcpy(&s->ctrl->warm_valid, &one, sizeof(int), cudaMemcpyHostToDevice));
   if (s->compressed_launched == 0) s->compressed_launched = 1;

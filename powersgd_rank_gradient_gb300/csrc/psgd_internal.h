@@ -14,7 +14,10 @@
 //   praw_part    : pass-1 partial P = Mbar Q, one slice per column tile.
 //   qpart        : pass-2 partial Q = Mbar^T P, one k-major slice per row block.
 //   mbar         : optional scratch holding the replica mean of M (W >= 3).
-//   ctrl         : device integers: cur, warm_valid, nonfinite flag.
+//   img          : ranks 16 and 32 only: P and Q split into tf32 hi and lo
+//                  parts in the swizzled layout the tensor-core passes read
+//                  (see psgd_tc.cuh).
+//   ctrl         : device integers: cur, warm_valid, nonfinite flag, timeout.
 #pragma once
 
 #include <stdint.h>
@@ -53,6 +56,10 @@ struct TensorDesc {
   long long e_off;   // first element in the user-visible packed error (no padding)
   long long valid;   // elements of the view backed by the bucket (n * m, or the bucket
                      // length for the batched hook's zero-padded square)
+  // ranks 16 and 32: first floats of the tensor-core operand images (hi half;
+  // the lo half follows it): P's and Q's row images (rows padded to 128) and
+  // chunk images (one RP x 32 block per 32 rows)
+  long long pi_off, qi_off, pti_off, qti_off;
   int n, m, r;       // rows, cols, effective rank
   int ld;            // row stride in the error store and mbar: m rounded up to a
                      // multiple of 4, so their rows are 16-byte aligned; the
@@ -92,7 +99,7 @@ struct Ctrl {
   int cur;        // which half of the double-buffered state is current
   int warm_valid; // a committed compressed step exists (warm Q available)
   int flag;       // non-finite input seen in this step
-  int timeout;    // reserved: a bounded device-side wait gave up
+  int timeout;    // a bounded device-side wait gave up in this step
 };
 
 constexpr int kMaxWorld = 64;

@@ -53,6 +53,13 @@ struct StepArgs {
   float* qpart;       // pass-2 partials
   float* qx;          // data-parallel split: k_qreduce writes this process's Q
                       // here (the exchange buffer, Q layout) instead of Qf
+  float* img;         // ranks 16 and 32: tensor-core operand images of P and Q
+  const Item* t3items;  // tensor-core pass 3 items (128 x 256; aligned, backed tensors)
+  int n_t3;
+  const Item* t2items;  // tensor-core pass 2 items (one row block x 128 columns)
+  int n_t2;
+  const Item* t1items;  // tensor-core pass 1 items (aligned rows, wholly backed)
+  int n_t1;
   float2* gram;       // per Gram-Schmidt item RP x RP (double-float)
   float2* gram_t;     // per tensor RP x RP, the items' sum
   float* tmat;        // per tensor RP x RP transform
@@ -1061,6 +1068,8 @@ __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
     const Item item = a.fitems[it];
     const TensorDesc td = a.tensors[item.t];
     const bool vec = (MODE == 0) ? (td.vec && a.vec_ok) : (td.m % 4 == 0);
+    // ranks 16 and 32: the tensor-core pass 3 wrote the aligned, backed tensors
+    if (MODE == 0 && RP >= 16 && a.n_t3 > 0 && vec && td.valid == (long long)td.n * td.m) continue;
     // BND: the view may end inside the item (batched hook's padding)
     const bool inside = (long long)(item.row0 + item.nrows) * td.m <= td.valid;
     if (vec && CPT == 4 && inside)

@@ -20,6 +20,7 @@ template <int RP> void launch_apply(const StepArgs& a, const float* src, float* 
 template <int RP> void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s);
 template <int RP> void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s);
 template <int RP> void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s);
+template <int RP> void launch_images(const StepArgs& a, int mode, int grid, cudaStream_t s);
 
 void launch_mean(const StepArgs& a, const Segment* segs, int nsegs, int grid, cudaStream_t s);
 void launch_commit(Ctrl* ctrl, int compressed, int* status, cudaStream_t s);

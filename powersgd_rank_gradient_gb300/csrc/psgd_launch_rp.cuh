@@ -8,6 +8,7 @@
 #include "psgd_kernels.cuh"
 #include "psgd_launch.h"
 #include "psgd_mma.cuh"
+#include "psgd_tc.cuh"
 
 namespace psgd {
 
@@ -25,13 +26,15 @@ inline void by_gtype(int gtype, F&& f) {
 
 template <int RP, typename GT>
 void launch_pass1_mma(const StepArgs& a, int grid, cudaStream_t s) {
-  using T = Pass1Mma<RP, GT>;
+  // the aligned, wholly backed items on the tensor cores (tcgen05), the rest
+  // on the element kernel
+  using T = Pass1Tc<RP, GT>;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(k_pass1_mma<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+    cudaFuncSetAttribute(k_pass1_tc<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
     configured = true;
   }
-  if (a.vec_ok && a.has_aligned) k_pass1_mma<RP, GT><<<grid, kThreads1M, T::SMEM, s>>>(a);
+  if (a.vec_ok && a.n_t1 > 0) k_pass1_tc<RP, GT><<<std::min(grid, a.n_t1), T::THREADS, T::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned) k_pass1_rest<RP, GT><<<grid * 2, kThreads, 0, s>>>(a);
 }
 
@@ -99,8 +102,34 @@ void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q, int
   k_apply<RP><<<grid, kThreads, 0, s>>>(a, src, dst, is_q, dst_half);
 }
 
+template <int RP, int NSRC>
+void launch_pass2_tc(const StepArgs& a, int src_mode, cudaStream_t s) {
+  using T = Pass2Tc<RP, NSRC>;
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(k_pass2_tc<RP, NSRC>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+    configured = true;
+  }
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  k_pass2_tc<RP, NSRC><<<std::min(a.n_t2, sms), T::THREADS, T::SMEM, s>>>(a, src_mode);
+}
+
 template <int RP>
 void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s) {
+  if constexpr (RP >= 16) {
+    // rank 32: the Mbar scratch, or the store halves of one or two replicas,
+    // on the tensor cores (src_mode 1 is chosen only for W <= 2); at rank 16
+    // the fp32 kernel is faster
+    if (RP == 32 && a.n_t2 > 0 && (src_mode == 0 || (src_mode == 1 && a.W <= 2))) {
+      if (src_mode == 1 && a.W == 2)
+        launch_pass2_tc<RP, 2>(a, src_mode, s);
+      else
+        launch_pass2_tc<RP, 1>(a, src_mode, s);
+      return;
+    }
+  }
   if constexpr (RP == 32) {
     // the Mbar scratch, or the single replica's store half: tensor cores
     // (at rank 16 the fp32 kernel is faster)
@@ -143,7 +172,29 @@ void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s) {
 }
 
 template <int RP>
+void launch_images(const StepArgs& a, int mode, int grid, cudaStream_t s) {
+  if constexpr (RP >= 16) k_images<RP><<<grid, kThreads, 0, s>>>(a, mode);
+}
+
+template <int RP>
 void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
+  if constexpr (RP >= 16) {
+    // the aligned, backed tensors on the tensor cores (one CTA per SM); the
+    // fp32 kernel below skips them and takes the rest
+    if (mode == 0 && a.vec_ok && a.n_t3 > 0) {
+      using T = Pass3Tc<RP>;
+      static bool configured = false;
+      if (!configured) {
+        cudaFuncSetAttribute(k_pass3_tc<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+        configured = true;
+      }
+      int dev = 0, sms = 148;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      k_pass3_tc<RP><<<std::min(a.n_t3, sms), T::THREADS, T::SMEM, s>>>(a);
+      if (!a.has_unaligned) return;   // every tensor was written
+    }
+  }
   if (mode == 0)
     k_pass3<RP, 0><<<grid, kThreads, 0, s>>>(a);
   else if (mode == 1)
@@ -165,6 +216,7 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
                                   cudaStream_t);                                                \
   template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
   template void launch_qreduce<RPV>(const StepArgs&, int, cudaStream_t);                        \
-  template void launch_pass3<RPV>(const StepArgs&, int, int, cudaStream_t);
+  template void launch_pass3<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
+  template void launch_images<RPV>(const StepArgs&, int, int, cudaStream_t);
 
 }  // namespace psgd

@@ -81,14 +81,17 @@ void launch_mean(const StepArgs& a, const Segment* segs, int nsegs, int grid, cu
 // End of a step: a step that saw no inf/NaN makes the next half of the
 // double-buffered state current; a skipped step leaves everything as it was
 // (torch.cuda.amp GradScaler: a step with inf/NaN gradients is skipped).
+// A bounded wait that gave up (ctrl->timeout) also leaves the state as it was
+// and reports status 2.
 __global__ void k_commit(Ctrl* ctrl, int compressed, int* status) {
   if (threadIdx.x == 0 && blockIdx.x == 0) {
     const int bad = ctrl->flag;
-    if (!bad && compressed) {
+    const int late = ctrl->timeout;
+    if (!bad && !late && compressed) {
       ctrl->cur ^= 1;
       ctrl->warm_valid = 1;
     }
-    *status = bad ? 1 : 0;
+    *status = late ? 2 : (bad ? 1 : 0);
   }
 }
 

@@ -36,7 +36,7 @@ def test_two_rank_max_and_job_throughput():
     world = 2
     times = [100.0, 125.0]
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.start_processes(_worker, args=(world, port, times, results), nprocs=world, join=True,
                            start_method="spawn")

@@ -154,7 +154,7 @@ def _worker(rank_id, world, port, rank, steps, start, inf_at, results):
 
 def _run(rank, steps, start=0, inf_at=None, world=2):
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.start_processes(_worker, args=(world, port, rank, steps, start, inf_at, results), nprocs=world,
                            join=True, start_method="spawn")

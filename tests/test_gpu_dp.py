@@ -93,7 +93,7 @@ def _run(shapes, rank, steps, start=0, ef=True, eps=0.0, dtype="f32", inf_at=Non
     cfg = dict(shapes=shapes, rank=rank, steps=steps, start=start, ef=ef, eps=eps, dtype=dtype,
                inf_at=inf_at, scale=scale, draws=draws)
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.start_processes(_worker, args=(world, port, cfg, results), nprocs=world, join=True,
                            start_method="spawn")
