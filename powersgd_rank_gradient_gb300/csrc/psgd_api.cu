@@ -157,6 +157,7 @@ struct psgd_state {
   int pass2_src = 0;  // 0 mbar scratch, 1 error store, 2 gradients
   int row_block = kRowBlock;  // rows per pass-2 item
   int fold_psum = 0;          // the first Gram kernel adds pass 1's P partials itself
+  int gs_fused = 0;           // Gram-Schmidt stage in three launches (few row items per tensor)
   // device memory
   TensorDesc* d_tensors = nullptr;
   Item* d_items = nullptr;
@@ -186,6 +187,8 @@ struct psgd_state {
   float* pgs = nullptr;
   float* qpart = nullptr;
   float* tmat = nullptr;
+  float* tmat2 = nullptr;   // fused Gram-Schmidt stage: second sweep's transforms
+  int* gs_cnt = nullptr;    // fused Gram-Schmidt stage: per-tensor partial counters
   float2* gram = nullptr;   // per Gram-Schmidt item RP x RP double-float partials
   float2* gram_t = nullptr; // per tensor RP x RP summed Gram matrix (double-float)
   Ctrl* ctrl = nullptr;
@@ -565,6 +568,13 @@ void build_plan(psgd_state* s) {
     for (int r0 = 0; r0 < td.m; r0 += per_q) s->gsq.push_back({(int)c, r0, std::min(per_q, td.m - r0), 0});
     s->gsq_count.push_back((int)s->gsq.size() - s->gsq_first.back());
   }
+  // the fused Gram-Schmidt stage: ranks up to 8 and at most 128 row items
+  // per tensor (the completing CTA adds a tensor's partials by itself)
+  {
+    int most = 0;
+    for (size_t c = 0; c < s->cdesc.size(); ++c) most = std::max(most, std::max(s->gsp_count[c], s->gsq_count[c]));
+    s->gs_fused = (RP <= 8 && most <= 128) ? 1 : 0;
+  }
 }
 
 StepArgs make_args(psgd_state* s) {
@@ -590,6 +600,8 @@ StepArgs make_args(psgd_state* s) {
   a.gram = s->gram;
   a.gram_t = s->gram_t;
   a.tmat = s->tmat;
+  a.tmat2 = s->tmat2;
+  a.gs_cnt = s->gs_cnt;
   a.tensors = s->d_tensors;
   a.items = s->d_items;
   a.n_items = (int)s->items.size();
@@ -670,6 +682,25 @@ struct Ops {
       L.begin(K_PSUM);
       launch_psum<RP>(a, std::max(1, std::min(a.n_ps, s->sms * 8)), L.st);
       L.end();
+    }
+    if (s->gs_fused) {
+      // Gram + solve, apply + Gram + solve, apply: three launches
+      L.begin(K_GRAM);
+      if (is_q || !s->fold_psum)
+        launch_gs_first<RP>(a, src_dense, nullptr, is_q, 0, grid, L.st);
+      else
+        launch_gs_first<RP>(a, s->praw_part, s->praw, 0, 1, grid, L.st);
+      L.end();
+      L.begin(K_SOLVE);
+      launch_gs_second<RP>(a, src_dense, s->pgs, is_q, grid, L.st);
+      L.end();
+      L.begin(K_APPLY);
+      if (is_q)
+        launch_apply<RP>(a, s->pgs, s->qinit, 1, -1, grid, L.st, s->tmat2);
+      else
+        launch_apply<RP>(a, s->pgs, s->Pf, 0, 1, grid, L.st, s->tmat2);
+      L.end();
+      return;
     }
     L.begin(K_GRAM);
     if (is_q || !s->fold_psum) {
@@ -1068,6 +1099,9 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   TRY(dalloc(s, (void**)&s->pgs, (size_t)std::max(s->p_total, s->q_total) * sizeof(float)));
   TRY(dalloc(s, (void**)&s->qpart, (size_t)s->qp_total * sizeof(float)));
   TRY(dalloc(s, (void**)&s->tmat, std::max(1, nt) * RP * RP * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->tmat2, std::max(1, nt) * RP * RP * sizeof(float)));
+  TRY(dalloc(s, (void**)&s->gs_cnt, std::max(1, nt) * sizeof(int)));
+  TRY(zero_now(s->gs_cnt, std::max(1, nt) * sizeof(int)));
   TRY(dalloc(s, (void**)&s->gram, std::max<size_t>(1, std::max(s->gsp.size(), s->gsq.size())) * RP * RP * sizeof(float2)));
   TRY(dalloc(s, (void**)&s->gram_t, std::max(1, nt) * RP * RP * sizeof(float2)));
   TRY(dalloc(s, (void**)&s->ctrl, sizeof(Ctrl)));

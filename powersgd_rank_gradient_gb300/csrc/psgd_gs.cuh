@@ -124,81 +124,88 @@ __device__ __forceinline__ void df_add_prod(float& hi, float& lo, float a, float
 
 // Per Gram-Schmidt item: the Gram matrix X^T X of its rows, each entry a
 // double-float (hi, lo) pair.  Rows of P come dense (nparts == 1) or as
-// column-tile partials (from_parts).
+// column-tile partials (from_parts).  gram_item does one item with the
+// whole CTA (tile and red are the CTA's shared buffers).
+template <int RP>
+__device__ __forceinline__ void gram_item(const StepArgs& a, int it, const float* __restrict__ src,
+                                          float* __restrict__ dense_out, int is_q, int from_parts,
+                                          float2* __restrict__ gram_out, float (*tile)[RP + 1], float2* red) {
+  constexpr int PAIRS = RP * RP;
+  constexpr int PPT = PAIRS > kThreads ? PAIRS / kThreads : 1;   // pairs per thread
+  constexpr int GROUPS = PAIRS >= kThreads ? 1 : kThreads / PAIRS;
+  const GsItem* items = is_q ? a.gsq_items : a.gsp_items;
+  const GsItem gi = items[it];
+  const TensorDesc td = a.tensors[gi.t];
+  const long long base = is_q ? td.q_off : td.p_off;
+  const int pair0 = (threadIdx.x % (PAIRS >= kThreads ? kThreads : PAIRS)) * PPT;
+  const int grp = PAIRS >= kThreads ? 0 : threadIdx.x / PAIRS;
+  float hi[PPT], lo[PPT];
+#pragma unroll
+  for (int u = 0; u < PPT; ++u) { hi[u] = 0.f; lo[u] = 0.f; }
+  for (int r0 = 0; r0 < gi.nrows; r0 += kGramTile) {
+    const int rows = min(kGramTile, gi.nrows - r0);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * RP; idx += kThreads) {
+      const int rr = idx / RP, k = idx % RP;
+      const long long row = gi.row0 + r0 + rr;
+      float v;
+      if (from_parts) {
+        // the column-tile partials added in tile order, four loads in flight
+        const float* pp = src + td.pp_off + row * RP + k;
+        const long long tstride = (long long)td.n * RP;
+        v = 0.f;
+        int c = 0;
+        for (; c + 4 <= td.ctiles1; c += 4) {
+          float x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) x[u] = pp[(c + u) * tstride];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v += x[u];
+        }
+        for (; c < td.ctiles1; ++c) v += pp[c * tstride];
+      } else if (is_q) {
+        v = src[base + (long long)k * td.m + row];
+      } else {
+        v = src[base + row * RP + k];
+      }
+      if (k >= td.r) v = 0.f;
+      tile[rr][k] = v;
+      if (dense_out) dense_out[base + row * RP + k] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < PPT; ++u) {
+      const int pa = (pair0 + u) / RP, pb = (pair0 + u) % RP;
+      for (int rr = grp; rr < rows; rr += GROUPS) df_add_prod(hi[u], lo[u], tile[rr][pa], tile[rr][pb]);
+    }
+  }
+  // reduce the row groups (in group order)
+#pragma unroll
+  for (int u = 0; u < PPT; ++u) {
+    __syncthreads();
+    red[threadIdx.x] = make_float2(hi[u], lo[u]);
+    __syncthreads();
+    if (threadIdx.x < (PAIRS >= kThreads ? kThreads : PAIRS)) {
+      float2 s = red[threadIdx.x];
+      for (int g = 1; g < GROUPS; ++g) {
+        const float2 x = red[threadIdx.x + g * (PAIRS >= kThreads ? kThreads : PAIRS)];
+        df_add(s.x, s.y, x.x, x.y);
+      }
+      gram_out[(long long)it * PAIRS + pair0 + u] = s;
+    }
+  }
+}
+
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_gram(const StepArgs a, const float* __restrict__ src,
                                                    float* __restrict__ dense_out, int is_q,
                                                    int from_parts, float2* __restrict__ gram_out) {
   __shared__ float tile[kGramTile][RP + 1];
   __shared__ float2 red[kThreads];
-  constexpr int PAIRS = RP * RP;
-  constexpr int PPT = PAIRS > kThreads ? PAIRS / kThreads : 1;   // pairs per thread
-  constexpr int GROUPS = PAIRS >= kThreads ? 1 : kThreads / PAIRS;
-  const GsItem* items = is_q ? a.gsq_items : a.gsp_items;
   const int n_items = is_q ? a.n_gsq : a.n_gsp;
   if (a.ctrl->flag) return;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const GsItem gi = items[it];
-    const TensorDesc td = a.tensors[gi.t];
-    const long long base = is_q ? td.q_off : td.p_off;
-    const int pair0 = (threadIdx.x % (PAIRS >= kThreads ? kThreads : PAIRS)) * PPT;
-    const int grp = PAIRS >= kThreads ? 0 : threadIdx.x / PAIRS;
-    float hi[PPT], lo[PPT];
-#pragma unroll
-    for (int u = 0; u < PPT; ++u) { hi[u] = 0.f; lo[u] = 0.f; }
-    for (int r0 = 0; r0 < gi.nrows; r0 += kGramTile) {
-      const int rows = min(kGramTile, gi.nrows - r0);
-      __syncthreads();
-      for (int idx = threadIdx.x; idx < rows * RP; idx += kThreads) {
-        const int rr = idx / RP, k = idx % RP;
-        const long long row = gi.row0 + r0 + rr;
-        float v;
-        if (from_parts) {
-          // the column-tile partials added in tile order, four loads in flight
-          const float* pp = src + td.pp_off + row * RP + k;
-          const long long tstride = (long long)td.n * RP;
-          v = 0.f;
-          int c = 0;
-          for (; c + 4 <= td.ctiles1; c += 4) {
-            float x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) x[u] = pp[(c + u) * tstride];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) v += x[u];
-          }
-          for (; c < td.ctiles1; ++c) v += pp[c * tstride];
-        } else if (is_q) {
-          v = src[base + (long long)k * td.m + row];
-        } else {
-          v = src[base + row * RP + k];
-        }
-        if (k >= td.r) v = 0.f;
-        tile[rr][k] = v;
-        if (dense_out) dense_out[base + row * RP + k] = v;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int u = 0; u < PPT; ++u) {
-        const int pa = (pair0 + u) / RP, pb = (pair0 + u) % RP;
-        for (int rr = grp; rr < rows; rr += GROUPS) df_add_prod(hi[u], lo[u], tile[rr][pa], tile[rr][pb]);
-      }
-    }
-    // reduce the row groups (in group order)
-#pragma unroll
-    for (int u = 0; u < PPT; ++u) {
-      __syncthreads();
-      red[threadIdx.x] = make_float2(hi[u], lo[u]);
-      __syncthreads();
-      if (threadIdx.x < (PAIRS >= kThreads ? kThreads : PAIRS)) {
-        float2 s = red[threadIdx.x];
-        for (int g = 1; g < GROUPS; ++g) {
-          const float2 x = red[threadIdx.x + g * (PAIRS >= kThreads ? kThreads : PAIRS)];
-          df_add(s.x, s.y, x.x, x.y);
-        }
-        gram_out[(long long)it * PAIRS + pair0 + u] = s;
-      }
-    }
-  }
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x)
+    gram_item<RP>(a, it, src, dense_out, is_q, from_parts, gram_out, tile, red);
 }
 
 // The items' Gram matrices of each tensor added up: CTA (tensor, block of
@@ -320,8 +327,8 @@ constexpr float kGsSkip = 1e-5f;
 // after its own step).  `sweep` is 0 for the first sweep and 1 for the
 // re-orthogonalising one.
 template <int RP>
-__global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const float2* __restrict__ gram_in,
-                                                    int is_q, int sweep) {
+__device__ __forceinline__ void solve_tensor(const StepArgs& a, const float2* __restrict__ gram_in, int t,
+                                             int is_q, int sweep, float* __restrict__ tout) {
   constexpr int ENT = RP * RP;
   constexpr int LD = RP + 1;                                // padded column stride
   // the steps run on one warp for ranks up to 8 and on the CTA above, thread
@@ -333,8 +340,6 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const floa
   __shared__ Dd H[RP * LD];   // H[j * LD + k] = row k of column j of G T
   __shared__ Dd T[RP * LD];   // T[j * LD + k] = row k of column j
   __shared__ Dd scal[RP];
-  const int t = blockIdx.x;
-  if (a.ctrl->flag) return;
   const TensorDesc td = a.tensors[t];
   const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
   if (count == 0) return;
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const floa
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) dmax = fmaxf(dmax, devw[w]);
     if (dmax <= kGsSkip) {
-      float* Tout = a.tmat + (long long)t * RP * RP;
+      float* Tout = tout + (long long)t * RP * RP;
       for (int idx = threadIdx.x; idx < ENT; idx += kThreads) {
         const int k = idx / RP, jj = idx % RP;
         Tout[idx] = (k == jj && jj < td.r) ? 1.f : 0.f;
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const floa
     }
     if constexpr (TEAM == 32) __syncwarp(); else __syncthreads();
   }
-  float* Tout = a.tmat + (long long)t * RP * RP;
+  float* Tout = tout + (long long)t * RP * RP;
   for (int idx = threadIdx.x; idx < ENT; idx += TEAM) {
     const int k = idx / RP, jj = idx % RP;
     float v = 0.f;
@@ -413,68 +418,155 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const floa
   }
 }
 
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const float2* __restrict__ gram_in,
+                                                    int is_q, int sweep) {
+  if (a.ctrl->flag) return;
+  solve_tensor<RP>(a, gram_in, blockIdx.x, is_q, sweep, a.tmat);
+}
+
 // dst rows = src rows x T.  Each thread computes OPT consecutive output
 // columns of one row (KG threads per row), each as the increasing-l FMA chain
 // over the row's RP inputs.  P (row-major) puts a row's KG threads next to
 // each other; Q (k-major) puts 32 consecutive rows in a warp, so its column
 // reads and writes are coalesced.
 template <int RP>
-__global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const float* __restrict__ src,
-                                                    float* __restrict__ dst, int is_q, int dst_half) {
+__device__ __forceinline__ void apply_item(const StepArgs& a, int it, const float* __restrict__ src,
+                                           float* __restrict__ dst, int is_q, long long half_off,
+                                           const float* __restrict__ tsrc, float* T) {
   constexpr int OPT = RP >= 4 ? 4 : RP;
   constexpr int KG = RP / OPT;
-  __shared__ __align__(16) float T[RP * RP];
   const GsItem* items = is_q ? a.gsq_items : a.gsp_items;
-  const int n_items = is_q ? a.n_gsq : a.n_gsp;
-  if (a.ctrl->flag) return;
-  // dst_half >= 0: write into half (cur ^ 1) of Pf/Qf (dst is the base)
-  long long half_off = 0;
-  if (dst_half >= 0) half_off = (long long)(a.ctrl->cur ^ 1) * (is_q ? a.q_total : a.p_total);
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const GsItem gi = items[it];
-    const TensorDesc td = a.tensors[gi.t];
-    const long long base = is_q ? td.q_off : td.p_off;
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < RP * RP; idx += kThreads) T[idx] = a.tmat[(long long)gi.t * RP * RP + idx];
-    __syncthreads();
-    const int span = is_q ? (gi.nrows + 31) / 32 * 32 * KG : gi.nrows * KG;
-    for (int idx = threadIdx.x; idx < span; idx += kThreads) {
-      const int rr = is_q ? (idx / (32 * KG)) * 32 + (idx & 31) : idx / KG;
-      const int kg = is_q ? (idx >> 5) % KG : idx % KG;
-      if (rr >= gi.nrows) continue;
-      const long long row = gi.row0 + rr;
-      float x[RP], y[OPT];
-      if (is_q) {
+  const GsItem gi = items[it];
+  const TensorDesc td = a.tensors[gi.t];
+  const long long base = is_q ? td.q_off : td.p_off;
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < RP * RP; idx += kThreads) T[idx] = tsrc[(long long)gi.t * RP * RP + idx];
+  __syncthreads();
+  const int span = is_q ? (gi.nrows + 31) / 32 * 32 * KG : gi.nrows * KG;
+  for (int idx = threadIdx.x; idx < span; idx += kThreads) {
+    const int rr = is_q ? (idx / (32 * KG)) * 32 + (idx & 31) : idx / KG;
+    const int kg = is_q ? (idx >> 5) % KG : idx % KG;
+    if (rr >= gi.nrows) continue;
+    const long long row = gi.row0 + rr;
+    float x[RP], y[OPT];
+    if (is_q) {
 #pragma unroll
-        for (int k = 0; k < RP; ++k) x[k] = src[base + (long long)k * td.m + row];
-      } else {
-        load_row<RP>(src + base + row * RP, x);
-      }
+      for (int k = 0; k < RP; ++k) x[k] = src[base + (long long)k * td.m + row];
+    } else {
+      load_row<RP>(src + base + row * RP, x);
+    }
 #pragma unroll
-      for (int o = 0; o < OPT; ++o) y[o] = 0.f;
+    for (int o = 0; o < OPT; ++o) y[o] = 0.f;
 #pragma unroll
-      for (int l = 0; l < RP; ++l) {
-        if constexpr (OPT == 4) {
-          const float4 tv = *reinterpret_cast<const float4*>(&T[l * RP + kg * 4]);
-          y[0] = fmaf(x[l], tv.x, y[0]);
-          y[1] = fmaf(x[l], tv.y, y[1]);
-          y[2] = fmaf(x[l], tv.z, y[2]);
-          y[3] = fmaf(x[l], tv.w, y[3]);
-        } else {
-#pragma unroll
-          for (int o = 0; o < OPT; ++o) y[o] = fmaf(x[l], T[l * RP + o], y[o]);
-        }
-      }
-      if (is_q) {
-#pragma unroll
-        for (int o = 0; o < OPT; ++o) dst[half_off + base + (long long)(kg * OPT + o) * td.m + row] = y[o];
-      } else if constexpr (OPT == 4) {
-        *reinterpret_cast<float4*>(dst + half_off + base + row * RP + kg * 4) = make_float4(y[0], y[1], y[2], y[3]);
+    for (int l = 0; l < RP; ++l) {
+      if constexpr (OPT == 4) {
+        const float4 tv = *reinterpret_cast<const float4*>(&T[l * RP + kg * 4]);
+        y[0] = fmaf(x[l], tv.x, y[0]);
+        y[1] = fmaf(x[l], tv.y, y[1]);
+        y[2] = fmaf(x[l], tv.z, y[2]);
+        y[3] = fmaf(x[l], tv.w, y[3]);
       } else {
 #pragma unroll
-        for (int o = 0; o < OPT; ++o) dst[half_off + base + row * RP + o] = y[o];
+        for (int o = 0; o < OPT; ++o) y[o] = fmaf(x[l], T[l * RP + o], y[o]);
       }
     }
+    if (is_q) {
+#pragma unroll
+      for (int o = 0; o < OPT; ++o) dst[half_off + base + (long long)(kg * OPT + o) * td.m + row] = y[o];
+    } else if constexpr (OPT == 4) {
+      *reinterpret_cast<float4*>(dst + half_off + base + row * RP + kg * 4) = make_float4(y[0], y[1], y[2], y[3]);
+    } else {
+#pragma unroll
+      for (int o = 0; o < OPT; ++o) dst[half_off + base + row * RP + o] = y[o];
+    }
+  }
+}
+
+// dst_half >= 0: write into half (cur ^ 1) of Pf/Qf (dst is the base).
+// tsrc: the transforms (a.tmat when NULL).
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const float* __restrict__ src,
+                                                    float* __restrict__ dst, int is_q, int dst_half,
+                                                    const float* __restrict__ tsrc) {
+  __shared__ __align__(16) float T[RP * RP];
+  const int n_items = is_q ? a.n_gsq : a.n_gsp;
+  if (a.ctrl->flag) return;
+  long long half_off = 0;
+  if (dst_half >= 0) half_off = (long long)(a.ctrl->cur ^ 1) * (is_q ? a.q_total : a.p_total);
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x)
+    apply_item<RP>(a, it, src, dst, is_q, half_off, tsrc ? tsrc : a.tmat, T);
+}
+
+// ---------------------------------------------------------------------------
+// Fused Gram-Schmidt stage, for buckets whose tensors have few row items
+// (small buckets, where the stage is a chain of short launches): every CTA
+// writes its items' Gram partials and counts them per tensor with an atomic;
+// the CTA whose count completes a tensor (no CTA waits for another) adds the
+// tensor's partials in item order and runs the solve.  The stage is then
+// three launches instead of eight: k_gs_first (Gram of X, solve of sweep 0),
+// k_gs_second (X T into the scratch, its Gram, solve of sweep 1 into tmat2),
+// and k_apply with tmat2.  Counters are left at zero for the next launch.
+// ---------------------------------------------------------------------------
+template <int RP>
+__device__ __forceinline__ void gs_count_and_solve(const StepArgs& a, int it, int is_q, int sweep,
+                                                   float* __restrict__ tout, int* last_s) {
+  constexpr int ENT = RP * RP;
+  const GsItem gi = (is_q ? a.gsq_items : a.gsp_items)[it];
+  const int t = gi.t;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int cnt = is_q ? a.gsq_count[t] : a.gsp_count[t];
+    *last_s = (atomicAdd(&a.gs_cnt[t], 1) == cnt - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!*last_s) return;
+  __threadfence();
+  const int first = is_q ? a.gsq_first[t] : a.gsp_first[t];
+  const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
+  for (int e = threadIdx.x; e < ENT; e += kThreads) {
+    float hi = 0.f, lo = 0.f;
+    for (int i = 0; i < count; ++i) {
+      const float2 x = __ldcg(a.gram + (long long)(first + i) * ENT + e);
+      df_add(hi, lo, x.x, x.y);
+    }
+    a.gram_t[(long long)t * ENT + e] = make_float2(hi, lo);
+  }
+  __syncthreads();
+  solve_tensor<RP>(a, a.gram_t, t, is_q, sweep, tout);
+  __syncthreads();
+  if (threadIdx.x == 0) a.gs_cnt[t] = 0;
+}
+
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_gs_first(const StepArgs a, const float* __restrict__ src,
+                                                       float* __restrict__ dense_out, int is_q, int from_parts) {
+  __shared__ float tile[kGramTile][RP + 1];
+  __shared__ float2 red[kThreads];
+  __shared__ int last_s;
+  const int n_items = is_q ? a.n_gsq : a.n_gsp;
+  if (a.ctrl->flag) return;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    gram_item<RP>(a, it, src, dense_out, is_q, from_parts, a.gram, tile, red);
+    gs_count_and_solve<RP>(a, it, is_q, 0, a.tmat, &last_s);
+  }
+}
+
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_gs_second(const StepArgs a, const float* __restrict__ src,
+                                                        float* __restrict__ mid, int is_q) {
+  __shared__ float tile[kGramTile][RP + 1];
+  __shared__ float2 red[kThreads];
+  __shared__ __align__(16) float T[RP * RP];
+  __shared__ int last_s;
+  const int n_items = is_q ? a.n_gsq : a.n_gsp;
+  if (a.ctrl->flag) return;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    apply_item<RP>(a, it, src, mid, is_q, 0, a.tmat, T);
+    __syncthreads();   // the CTA's rows of X T are visible to its Gram
+    gram_item<RP>(a, it, mid, nullptr, is_q, 0, a.gram, tile, red);
+    gs_count_and_solve<RP>(a, it, is_q, 1, a.tmat2, &last_s);
   }
 }
 

@@ -63,6 +63,8 @@ struct StepArgs {
   float2* gram;       // per Gram-Schmidt item RP x RP (double-float)
   float2* gram_t;     // per tensor RP x RP, the items' sum
   float* tmat;        // per tensor RP x RP transform
+  float* tmat2;       // fused Gram-Schmidt stage: the second sweep's transforms
+  int* gs_cnt;        // fused Gram-Schmidt stage: Gram partials counted per tensor
   const TensorDesc* tensors;
   const Item* items;         // tall (row block) x (column tile) items: pass 2
   int n_items;

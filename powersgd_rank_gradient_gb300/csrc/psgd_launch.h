@@ -16,7 +16,11 @@ template <int RP> void launch_gram(const StepArgs& a, const float* src, float* d
 template <int RP> void launch_gram_sum(const StepArgs& a, int is_q, cudaStream_t s);
 template <int RP> void launch_solve(const StepArgs& a, const float2* gram, int is_q, int sweep, cudaStream_t s);
 template <int RP> void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q,
-                                    int dst_half, int grid, cudaStream_t s);
+                                    int dst_half, int grid, cudaStream_t s, const float* tsrc = nullptr);
+template <int RP> void launch_gs_first(const StepArgs& a, const float* src, float* dense_out, int is_q,
+                                       int from_parts, int grid, cudaStream_t s);
+template <int RP> void launch_gs_second(const StepArgs& a, const float* src, float* mid, int is_q, int grid,
+                                        cudaStream_t s);
 template <int RP> void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s);
 template <int RP> void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s);
 template <int RP> void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s);

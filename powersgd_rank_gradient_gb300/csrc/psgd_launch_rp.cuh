@@ -98,8 +98,19 @@ void launch_solve(const StepArgs& a, const float2* gram, int is_q, int sweep, cu
 
 template <int RP>
 void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q, int dst_half, int grid,
-                  cudaStream_t s) {
-  k_apply<RP><<<grid, kThreads, 0, s>>>(a, src, dst, is_q, dst_half);
+                  cudaStream_t s, const float* tsrc) {
+  k_apply<RP><<<grid, kThreads, 0, s>>>(a, src, dst, is_q, dst_half, tsrc);
+}
+
+template <int RP>
+void launch_gs_first(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts, int grid,
+                     cudaStream_t s) {
+  k_gs_first<RP><<<grid, kThreads, 0, s>>>(a, src, dense_out, is_q, from_parts);
+}
+
+template <int RP>
+void launch_gs_second(const StepArgs& a, const float* src, float* mid, int is_q, int grid, cudaStream_t s) {
+  k_gs_second<RP><<<grid, kThreads, 0, s>>>(a, src, mid, is_q);
 }
 
 template <int RP, int NSRC>
@@ -213,7 +224,11 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
   template void launch_gram_sum<RPV>(const StepArgs&, int, cudaStream_t);                      \
   template void launch_solve<RPV>(const StepArgs&, const float2*, int, int, cudaStream_t);      \
   template void launch_apply<RPV>(const StepArgs&, const float*, float*, int, int, int,         \
-                                  cudaStream_t);                                                \
+                                  cudaStream_t, const float*);                                  \
+  template void launch_gs_first<RPV>(const StepArgs&, const float*, float*, int, int, int,      \
+                                     cudaStream_t);                                             \
+  template void launch_gs_second<RPV>(const StepArgs&, const float*, float*, int, int,          \
+                                      cudaStream_t);                                            \
   template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
   template void launch_qreduce<RPV>(const StepArgs&, int, cudaStream_t);                        \
   template void launch_pass3<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
