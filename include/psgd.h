@@ -1,11 +1,13 @@
 /*
  * psgd.h -- C ABI of the GB300-native PowerSGD communication-hook step.
  *
- * One process, one GPU.  A data-parallel job of W workers is simulated by W
- * replica gradient buckets resident in the same HBM; the "allreduce" of the
- * pages is a mean over those W buckets, folded into the kernels that read
- * them.  Every step of the method runs in CUDA kernels of this library; the
- * host side only plans, allocates (at create time) and enqueues.
+ * A data-parallel job of W workers is either simulated inside one GPU by W
+ * replica gradient buckets resident in the same HBM -- the "allreduce" of the
+ * pages is then a mean over those W buckets, folded into the kernels that read
+ * them (psgd_step) -- or spread over W processes with one replica each, the
+ * pages' two exchanges left to the caller's collective on library-owned
+ * buffers (psgd_dp_*).  Every step of the method runs in CUDA kernels of this
+ * library; the host side only plans, allocates (at create time) and enqueues.
  *
  * Sources (web pages; the operations are restated here, not copied):
  *   [DDP]  "DDP Communication Hooks" (PyTorch 1.11 documentation):
@@ -197,7 +199,9 @@ int psgd_graph_stats(const psgd_state* s, int64_t* captures, int64_t* replays);
 
 /*
  * psgd_step_status -- synchronises `stream` and returns the outcome of the
- * last step enqueued: PSGD_OK, PSGD_SKIPPED_NONFINITE, or PSGD_ECUDA.
+ * last step enqueued: PSGD_OK, PSGD_SKIPPED_NONFINITE, PSGD_ETIMEOUT (a
+ * bounded wait inside a tensor-core kernel gave up; the step was not
+ * committed and the state is as before it), or PSGD_ECUDA.
  */
 int psgd_step_status(psgd_state* s, void* stream);
 

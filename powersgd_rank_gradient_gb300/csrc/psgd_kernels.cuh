@@ -592,9 +592,45 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
           }
         }
       } else {
-        // aligned chunk (element offset in the bucket) holding this lane's first column
-        const long long gp = go;
+        const long long gp = go;   // this lane's first element in the bucket
         const int rg = (int)(gp & 3);
+        if (GB == 16 || (rg & 1) == 0) {
+          // the lane's own four values straight into its slot, in pieces sized
+          // to the row's offset modulo 4 (16, 8 or 4 bytes; 8 or 4 for 16-bit
+          // values at an even offset), so the math reads an aligned slot as
+          // in kind 0 (the bucket's last values element by element)
+          if (c < cend) {
+#pragma unroll
+            for (int w = 0; w < WT; ++w) {
+              const GT* g = reinterpret_cast<const GT*>(a.grads.p[w]);
+              char* dst = slot + w * St::GSEG + lane * GB;
+              if (gp + 4 <= a.gn) {
+                if (rg == 0) {
+                  if constexpr (GB == 16) cp_async16(dst, g + gp); else cp_async8(dst, g + gp);
+                } else if (rg == 2) {
+                  if constexpr (GB == 16) {
+                    cp_async8(dst, g + gp);
+                    cp_async8(dst + 8, g + gp + 2);
+                  } else {
+                    cp_async4(dst, g + gp);
+                    cp_async4(dst + 4, g + gp + 2);
+                  }
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) cp_async4(dst + 4 * e, g + gp + e);
+                }
+              } else {
+                for (int e = 0; e < 4; ++e)
+                  reinterpret_cast<GT*>(dst)[e] = (gp + e < a.gn) ? g[gp + e] : GT(0.f);
+              }
+              if (a.ef) cp_async16(slot + WT * St::GSEG + w * St::ESEG + lane * 16, a.estore + eo + (long long)w * a.nc_pad);
+            }
+          }
+          cp_async_commit();
+          return;
+        }
+        // 16-bit values at an odd offset: the aligned chunk holding this
+        // lane's first column, and the next lane's, select the four values
         const bool gneed = c - rg < cend;
         const bool gx = lane == 31 && rg > 0 && c + 4 - rg < cend;
         auto gcopy = [&](char* dst, const GT* g, long long at) {
@@ -677,7 +713,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
           float gv[4];
-          if constexpr (SH) {
+          if (SH && !(GB == 16 || (rg & 1) == 0)) {
             float lo[4], hi[4];
             const char* own = slot + w * St::GSEG + lane * GB;
             const char* nx = lane < 31 ? own + GB : slot + St::XOFF + w * 16;
@@ -699,6 +735,10 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
               gv[0] = x.x; gv[1] = x.y; gv[2] = x.z; gv[3] = x.w;
             } else {
               cvt4<GT>(*reinterpret_cast<const uint2*>(slot + w * St::GSEG + lane * GB), gv);
+            }
+            if constexpr (SH) {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) gv[cc] = cc < nvg ? gv[cc] : 0.f;
             }
           }
           float mv[4];
