@@ -52,6 +52,9 @@ def parse():
                     help="type of the replica gradient buckets of the main workload (the pages' "
                          "fp16/bf16 compress wrappers hand the hook 16-bit buckets)")
     ap.add_argument("--rank", type=int, default=None, help="rank of the rank-sweep workload")
+    ap.add_argument("--replicas", type=int, default=None,
+                    help="replica count W of the main workload instead of its own (e.g. 3 or 6 on "
+                         "the BERT-large bucket)")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling cases: only this many transformer layers, no embeddings")
     ap.add_argument("--batched", dest="batched", action="store_true", default=True,
@@ -75,7 +78,7 @@ GSIZE = {"f32": 4, "f16": 2, "bf16": 2}
 LOSS_SCALE = 65536.0   # GradScaler's default initial scale
 
 
-def workload_spec(name, rank_override=None, layers=None, dtype="f32"):
+def workload_spec(name, rank_override=None, layers=None, dtype="f32", replicas=None):
     """A workload: the bucket's tensor shapes, replicas, rank and input
     recipe; `dtype` is the type of the replica buckets (f32, f16, bf16).
     fp16-scaled is the 8192 x 8192 rank-4 matrix whose N(0, 1e-3) gradients
@@ -101,6 +104,9 @@ def workload_spec(name, rank_override=None, layers=None, dtype="f32"):
         spec = dict(name=name, shapes=shapes, world_size=w["world_size"], rank=w["rank"],
                     mcr=w["mcr"], std=w["std"], heavy=w["heavy"], batch_same_shape=w["batch_same_shape"])
     spec.setdefault("loss_scale", 1.0)
+    if replicas is not None and replicas != spec["world_size"]:
+        spec["world_size"] = replicas
+        spec["name"] = f"{spec['name']}-W{replicas}"
     spec["dtype"] = dtype
     if dtype != "f32" and not spec["name"].endswith(dtype) and name != "fp16-scaled":
         spec["name"] = f"{spec['name']}-{dtype}"
@@ -666,7 +672,8 @@ def main():
     rank_id = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    spec = workload_spec(args.workload, rank_override=args.rank, layers=args.layers, dtype=args.grad_dtype)
+    spec = workload_spec(args.workload, rank_override=args.rank, layers=args.layers, dtype=args.grad_dtype,
+                         replicas=args.replicas)
     base_cfg = {"workload": spec["name"], "world_size_W": spec["world_size"],
                 "matrix_approximation_rank": spec["rank"], "min_compression_rate": spec["mcr"],
                 "start_powerSGD_iter": 0, "use_error_feedback": True, "warm_start": True,

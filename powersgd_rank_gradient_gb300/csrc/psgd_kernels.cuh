@@ -527,8 +527,10 @@ __device__ __forceinline__ void store4_split(float* p, const float (&v)[4], int 
 // lane stages the aligned gradient chunk that holds its first column, lane 31
 // also the chunk after it (at XOFF in the stage), and a lane takes its four
 // values from its own chunk and the next lane's.  The error store and mbar
-// rows (stride ld) are aligned in both modes.
-template <int RP, int WT, typename GT, int MINB, int MODE>
+// rows (stride ld) are aligned in both modes.  PW: the bucket has a.W < WT
+// replicas (the stage is laid out for WT; replicas a.W.. are neither read nor
+// written), so one instantiation per WT serves every count up to it.
+template <int RP, int WT, typename GT, int MINB, int MODE, bool PW = false>
 __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDesc& td, const Item& item,
                                               const float* __restrict__ Qp, const float* __restrict__ Qc,
                                               const float* __restrict__ Pc, int cur, float& chk,
@@ -585,6 +587,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         if (cin) {
 #pragma unroll
           for (int w = 0; w < WT; ++w) {
+            if (PW && w >= a.W) break;
             const GT* gsrc = reinterpret_cast<const GT*>(a.grads.p[w]) + go;
             if constexpr (GB == 16) cp_async16(slot + w * St::GSEG + lane * GB, gsrc);
             else cp_async8(slot + w * St::GSEG + lane * GB, gsrc);
@@ -602,6 +605,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
           if (c < cend) {
 #pragma unroll
             for (int w = 0; w < WT; ++w) {
+              if (PW && w >= a.W) break;
               const GT* g = reinterpret_cast<const GT*>(a.grads.p[w]);
               char* dst = slot + w * St::GSEG + lane * GB;
               if (gp + 4 <= a.gn) {
@@ -644,6 +648,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         };
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
+          if (PW && w >= a.W) break;
           const GT* g = reinterpret_cast<const GT*>(a.grads.p[w]);
           if (gneed) gcopy(slot + w * St::GSEG + lane * GB, g, gp - rg);
           if (gx) gcopy(slot + St::XOFF + w * 16, g, gp - rg + 4);
@@ -712,6 +717,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
         const int rg = SH ? (int)((td.g_off + g_pos) & 3) : 0;
 #pragma unroll
         for (int w = 0; w < WT; ++w) {
+          if (PW && w >= a.W) break;
           float gv[4];
           if (SH && !(GB == 16 || (rg & 1) == 0)) {
             float lo[4], hi[4];
@@ -800,7 +806,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
 // skips the rest; KIND 1 takes the rest: shifted chunks (MODE 1) when the
 // pointers are aligned, else the element path.  Separate instantiations keep
 // the aligned kernel free of the other paths' registers and checks.
-template <int RP, int WT, typename GT, int MINB, int KIND>
+template <int RP, int WT, typename GT, int MINB, int KIND, bool PW = false>
 __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
   extern __shared__ __align__(16) char p1smem[];
   using St = Pass1CS<RP, WT, GT, MINB, KIND == 1>;
@@ -818,13 +824,13 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
     const TensorDesc td = a.tensors[item.t];
     const bool aligned = td.vec && a.vec_ok && (long long)(item.row0 + item.nrows) * td.m <= td.valid;
     if constexpr (KIND == 0) {
-      if (aligned) pass1_tile_cs<RP, WT, GT, MINB, 0>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+      if (aligned) pass1_tile_cs<RP, WT, GT, MINB, 0, PW>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
     } else {
       if (aligned) continue;
       if (a.vec_ok)
-        pass1_tile_cs<RP, WT, GT, MINB, 1>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+        pass1_tile_cs<RP, WT, GT, MINB, 1, PW>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
       else
-        pass1_tile<RP, WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
+        pass1_tile<RP, PW ? 0 : WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
     }
   }
   bad |= !(chk == 0.f);

@@ -7,7 +7,6 @@
 #include "psgd_gs.cuh"
 #include "psgd_kernels.cuh"
 #include "psgd_launch.h"
-#include "psgd_mma.cuh"
 #include "psgd_tc.cuh"
 
 namespace psgd {
@@ -38,24 +37,29 @@ void launch_pass1_mma(const StepArgs& a, int grid, cudaStream_t s) {
   if (!a.vec_ok || a.has_unaligned) k_pass1_rest<RP, GT><<<grid * 2, kThreads, 0, s>>>(a);
 }
 
-template <int RP, int WT, typename GT, int MINB>
+// PW: a.W < WT replicas on the stage layout of WT.
+template <int RP, int WT, typename GT, int MINB, bool PW = false>
 void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
   using St0 = Pass1CS<RP, WT, GT, MINB, false>;
   using St1 = Pass1CS<RP, WT, GT, MINB, true>;
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, St0::SMEM);
-    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, St1::SMEM);
+    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 0, PW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         St0::SMEM);
+    cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 1, PW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         St1::SMEM);
     configured = true;
   }
-  if (a.vec_ok && a.has_aligned) k_pass1_cs<RP, WT, GT, MINB, 0><<<grid * MINB, kThreads, St0::SMEM, s>>>(a);
+  if (a.vec_ok && a.has_aligned) k_pass1_cs<RP, WT, GT, MINB, 0, PW><<<grid * MINB, kThreads, St0::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned)
-    k_pass1_cs<RP, WT, GT, MINB, 1><<<grid * MINB, kThreads, a.vec_ok ? St1::SMEM : 0, s>>>(a);
+    k_pass1_cs<RP, WT, GT, MINB, 1, PW><<<grid * MINB, kThreads, a.vec_ok ? St1::SMEM : 0, s>>>(a);
 }
 
 // grid = one CTA per SM; the kernels run MINB CTAs per SM.  Ranks up to 8 use
-// the chunk-stationary kernel (two CTAs per SM for W <= 2, one above); ranks
-// 16 and 32 the tensor-core kernel (one CTA per SM, any W).
+// the chunk-stationary kernel (two CTAs per SM for W <= 2, one above; W = 3
+// on the four-replica stage, 5 to 8 on the eight-replica one, larger W on the
+// element kernel); ranks 16 and 32 the tensor-core kernel (one CTA per SM,
+// any W).
 template <int RP>
 void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
   by_gtype(a.gtype, [&](auto tag) {
@@ -66,6 +70,10 @@ void launch_pass1(const StepArgs& a, int grid, cudaStream_t s) {
         case 2: launch_pass1_cs<RP, 2, GT, 2>(a, grid, s); break;
         case 4: launch_pass1_cs<RP, 4, GT, 1>(a, grid, s); break;
         case 8: launch_pass1_cs<RP, 8, GT, 1>(a, grid, s); break;
+        case 3: launch_pass1_cs<RP, 4, GT, 1, true>(a, grid, s); break;
+        case 5:
+        case 6:
+        case 7: launch_pass1_cs<RP, 8, GT, 1, true>(a, grid, s); break;
         default: k_pass1<RP, 0, GT, 1><<<grid * 2, kThreads, 0, s>>>(a); break;
       }
     } else {
@@ -138,20 +146,6 @@ void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s) {
         launch_pass2_tc<RP, 2>(a, src_mode, s);
       else
         launch_pass2_tc<RP, 1>(a, src_mode, s);
-      return;
-    }
-  }
-  if constexpr (RP == 32) {
-    // the Mbar scratch, or the single replica's store half: tensor cores
-    // (at rank 16 the fp32 kernel is faster)
-    if (src_mode == 0 || (src_mode == 1 && a.W == 1)) {
-      using T = Pass2Mma<RP>;
-      static bool configured = false;
-      if (!configured) {
-        cudaFuncSetAttribute(k_pass2_mma<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-        configured = true;
-      }
-      k_pass2_mma<RP><<<std::min(a.n_items, (grid + 2) / 3), kThreads, T::SMEM, s>>>(a);
       return;
     }
   }

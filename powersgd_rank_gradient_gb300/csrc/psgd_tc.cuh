@@ -22,9 +22,41 @@
 #include <stdint.h>
 
 #include "psgd_kernels.cuh"
-#include "psgd_mma.cuh"
 
 namespace psgd {
+
+// cp.async that fills the destination with zeros when `valid` is false (the
+// source address is then not read, but still points into the buffer).
+__device__ __forceinline__ void cp_async16_z(void* smem, const void* gmem, bool valid) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async8_z(void* smem, const void* gmem, bool valid) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  const int n = valid ? 8 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+
+// The pass-1 items the tensor-core kernel does not take (rows not 16-byte aligned
+// in the bucket, or items the bucket does not wholly back): element path.
+template <int RP, typename GT>
+__global__ void __launch_bounds__(kThreads) k_pass1_rest(const StepArgs a) {
+  const int cur = a.ctrl->cur;
+  const bool use_init = (!a.warm_start) || (a.ctrl->warm_valid == 0);
+  const float* Qc = a.Qf + (long long)cur * a.q_total;
+  const float* Pc = a.Pf + (long long)cur * a.p_total;
+  const float* Qp = use_init ? a.qinit : Qc;
+  int bad = 0;
+  for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
+    const Item item = a.p1items[it];
+    const TensorDesc td = a.tensors[item.t];
+    if (td.vec && a.vec_ok && (long long)(item.row0 + item.nrows) * td.m <= td.valid) continue;
+    pass1_tile<RP, 0, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->flag, 1);
+}
+
 namespace tc {
 
 // Iterations of a bounded mbarrier wait before it gives up (each try_wait

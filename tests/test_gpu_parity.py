@@ -67,7 +67,10 @@ def test_config1_256x512_rank1_two_steps():
     st.close()
 
 
-@pytest.mark.parametrize("world", [1, 2, 3, 4, 8])
+# 1, 2, 4, 8: the chunk-stationary pass 1 laid out for exactly W replicas;
+# 3 and 5-7: the same kernel on the four- and eight-replica layouts with the
+# rest unused; 9: the element kernel (any W).
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_mixed_bucket_worlds(world):
     _run(MIXED, world, 4, 3, label=f"W={world}")
 
@@ -496,7 +499,7 @@ def test_library_draw_matches_oracle_philox(warm):
 
 
 @pytest.mark.parametrize("rank", [4, 32])
-@pytest.mark.parametrize("world,ef", [(1, True), (2, True), (3, False), (8, True)])
+@pytest.mark.parametrize("world,ef", [(1, True), (2, True), (3, False), (5, True), (8, True)])
 def test_bf16_buckets(world, ef, rank):
     """16-bit (bf16) replica buckets, as the bf16 compress wrapper produces:
     the oracle is fed the same bf16 values widened to float64."""
