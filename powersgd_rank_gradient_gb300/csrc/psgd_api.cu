@@ -471,14 +471,17 @@ void build_plan(psgd_state* s) {
   };
   make_items(&s->items, s->row_block, CT, false);
   make_items(&s->fitems, kFineRows3, ctile3_for(RP), true);
-  // pass 1: half-height items for small buckets (fewer than six items per
-  // SM at full height), so that the last wave over the SMs is short
+  // pass 1: items of fewer rows in small buckets (down to 32 rows while a
+  // bucket holds fewer than six items per SM), so that the last wave over
+  // the SMs is short; tall items in large buckets, so that each warp's copy
+  // pipeline drains and refills (and the item's setup loads wait) less often
   int rows1 = rows1_for(RP);
   {
     long long nc = 0;
     for (auto& h : s->tensors)
       if (h.compressed) nc += h.numel;
-    if (RP <= 8 && nc < 6LL * s->sms * rows1 * CT1) rows1 /= 2;
+    if (RP <= 8)
+      while (rows1 > 32 && nc < 6LL * s->sms * rows1 * CT1) rows1 /= 2;
   }
   make_items(&s->p1items, rows1, 0, true);
   // tensor-core pass 3 (ranks 16 and 32): 128 x 256 items of the tensors
@@ -1021,7 +1024,6 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   s->batch = batch ? 1 : 0;
   s->dtype = grad_dtype;
   cudaDeviceGetAttribute(&s->sms, cudaDevAttrMultiProcessorCount, device);
-  build_plan(s);
   // Where pass 2 reads the replica mean: a scratch copy written by pass 1
   // costs 8 bytes per element; re-reading the W sources costs W * 4 (store)
   // or W * sizeof(grad) (no error feedback).  Take the cheaper.
@@ -1029,6 +1031,7 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   const int reread = s->W * (s->ef ? 4 : gsz);
   s->pass2_src = (reread <= 8) ? (s->ef ? 1 : 2) : 0;
   if (s->W == 1 && s->ef) s->pass2_src = 1;
+  build_plan(s);
 
   if (s->dp_world) s->fold_psum = 0;   // P_raw must be dense before the exchange
   const size_t RP = s->RP;

@@ -26,7 +26,7 @@ namespace psgd {
 
 constexpr int kThreads = 256;      // threads per CTA of the streaming passes
 constexpr int kRowBlock = 512;     // rows per work item of pass 2 (one Q partial each)
-constexpr int kFineRows = 64;      // rows per work item of pass 1 (ranks <= 8)
+constexpr int kFineRows = 128;     // rows per work item of pass 1 (ranks <= 8; fewer in small buckets)
 constexpr int kRows1High = 128;   // rows per work item of pass 1 (ranks 16 and 32)
 constexpr int kFineRows3 = 32;     // rows per work item of pass 3 and the error views
 constexpr int kGsRows = 256;       // rows per work item of the Gram-Schmidt kernels

@@ -482,8 +482,8 @@ struct Pass1CS {
   // lane 31's, for every gradient and error segment
   static constexpr int XOFF = WT * (GSEG + ESEG);
   static constexpr int UNIT_BYTES = XOFF + (SH ? 2 * WT * 16 : 0);   // one row x 128 columns
-  static constexpr int RED_BYTES = kFineRows * NCH * RP * 4;
-  static constexpr int BUDGET = (MINB == 1 ? 200 * 1024 : 96 * 1024) - RED_BYTES;
+  static constexpr int RED_BYTES = rows1_for(RP) * NCH * RP * 4;
+  static constexpr int BUDGET = (MINB == 1 ? 200 * 1024 : 112 * 1024) - RED_BYTES;
   static constexpr int S_RAW = BUDGET / (8 * UNIT_BYTES);
   static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
   static constexpr int SMEM = 8 * S * UNIT_BYTES + RED_BYTES;
