@@ -109,10 +109,10 @@ int plan_tensors(const int64_t* dims, const int32_t* ndims, int32_t n, int32_t r
 }
 
 enum Kind { K_MEAN = 0, K_PASS1, K_GRAM, K_SOLVE, K_APPLY, K_PASS2, K_QREDUCE, K_PASS3, K_COMMIT, K_RANDN,
-            K_PSUM, K_DP, K_IMG, K_COUNT };
+            K_PSUM, K_DP, K_IMG, K_GS, K_COUNT };
 const char* kKindNames[K_COUNT] = {"mean", "pass1", "gs_gram", "gs_solve", "gs_apply",
                                    "pass2", "qreduce", "pass3", "commit", "randn", "psum", "dp_exchange",
-                                   "images"};
+                                   "images", "gs_stage"};
 
 struct EventPair {
   cudaEvent_t a, b;
@@ -189,6 +189,8 @@ struct psgd_state {
   float* tmat = nullptr;
   float* tmat2 = nullptr;   // fused Gram-Schmidt stage: second sweep's transforms
   int* gs_cnt = nullptr;    // fused Gram-Schmidt stage: per-tensor partial counters
+  unsigned int* gs_bar = nullptr;   // its cooperative launch: the grid barrier's counter
+  int gs_coop = 1;          // the fused stage as one cooperative launch (0 after a refusal)
   float2* gram = nullptr;   // per Gram-Schmidt item RP x RP double-float partials
   float2* gram_t = nullptr; // per tensor RP x RP summed Gram matrix (double-float)
   Ctrl* ctrl = nullptr;
@@ -289,6 +291,21 @@ struct DeviceGuard {
     if (prev >= 0 && now != prev) cudaSetDevice(prev);
   }
 };
+
+// The longest CTA load when G resident CTAs take items of the given sizes
+// (elements, in the order the kernels take them) round-robin, as the
+// persistent pass kernels do: an item costs its elements x bpe bytes plus c0
+// (its setup loads and the fill and drain of its copy pipeline).
+double rr_makespan(const std::vector<long long>& sizes, long long G, double bpe, double c0) {
+  if (G < 1) G = 1;
+  std::vector<double> load((size_t)std::min<long long>(G, (long long)sizes.size() + 1), 0.0);
+  for (size_t i = 0; i < sizes.size(); ++i) load[i % load.size()] += (double)sizes[i] * bpe + c0;
+  return *std::max_element(load.begin(), load.end());
+}
+
+// Bytes a CTA streams while its item setup stalls for t seconds, with G CTAs
+// sharing about 6.8 TB/s of HBM (only the ratio between candidates matters).
+double stall_bytes(double t, long long G) { return t * 6.8e12 / (double)std::max<long long>(G, 1); }
 
 // Builds the work lists of the compressed tensors.
 void build_plan(psgd_state* s) {
@@ -471,17 +488,44 @@ void build_plan(psgd_state* s) {
   };
   make_items(&s->items, s->row_block, CT, false);
   make_items(&s->fitems, kFineRows3, ctile3_for(RP), true);
-  // pass 1: items of fewer rows in small buckets (down to 32 rows while a
-  // bucket holds fewer than six items per SM), so that the last wave over
-  // the SMs is short; tall items in large buckets, so that each warp's copy
-  // pipeline drains and refills (and the item's setup loads wait) less often
+  // pass 1 (ranks <= 8): items of fewer rows in small buckets (down to 32
+  // rows while a bucket holds fewer than six items per SM), so that the last
+  // wave over the SMs is short; tall items in large buckets, so that each
+  // warp's copy pipeline drains and refills (and the item's setup loads wait)
+  // less often.  When every compressed tensor has the same shape the items
+  // are alike and the waves can be counted: the height (16 to 128 rows, a
+  // multiple of 16) with the shortest round-robin makespan is taken (8192 x
+  // 8192 alone: 112 rows, 592 items over 304 CTAs, against 1024 64-row ones).
   int rows1 = rows1_for(RP);
-  {
+  if (RP <= 8 && !s->cdesc.empty()) {
     long long nc = 0;
     for (auto& h : s->tensors)
       if (h.compressed) nc += h.numel;
-    if (RP <= 8)
+    bool alike = true;
+    for (const TensorDesc& td : s->cdesc)
+      alike = alike && td.n == s->cdesc[0].n && td.m == s->cdesc[0].m;
+    if (!alike) {
       while (rows1 > 32 && nc < 6LL * s->sms * rows1 * CT1) rows1 /= 2;
+    } else {
+      const double g = s->dtype == PSGD_F32 ? 4.0 : 2.0;
+      const double bpe = s->W * (g + (s->ef ? 8.0 : 0.0)) + (s->pass2_src == 0 ? 4.0 : 0.0);
+      const int minb = s->W <= 2 ? 2 : 1;   // CTAs per SM of the chunk-stationary kernel
+      double best = -1.0;
+      int best_rows = rows1;
+      for (int r = rows1_for(RP); r >= 16; r -= 16) {
+        std::vector<Item> cand;
+        make_items(&cand, r, 0, true);
+        std::vector<long long> sizes(cand.size());
+        for (size_t i = 0; i < cand.size(); ++i) sizes[i] = (long long)cand[i].nrows * cand[i].ncols;
+        const long long G = std::min<long long>((long long)cand.size(), s->sms) * minb;
+        const double t = rr_makespan(sizes, G, bpe, stall_bytes(5e-6, G));
+        if (best < 0 || t < best * 0.995) {
+          best = t;
+          best_rows = r;
+        }
+      }
+      rows1 = best_rows;
+    }
   }
   make_items(&s->p1items, rows1, 0, true);
   // tensor-core pass 3 (ranks 16 and 32): 128 x 256 items of the tensors
@@ -551,8 +595,8 @@ void build_plan(psgd_state* s) {
   }
   for (size_t c = 0; c < s->cdesc.size(); ++c) {
     const long long len = (long long)s->cdesc[c].m * RP;
-    for (long long f = 0; f < len; f += 1024)
-      s->qr.push_back({(int)c, (int)f, (int)std::min<long long>(1024, len - f), 0});
+    for (long long f = 0; f < len; f += kQrChunk)
+      s->qr.push_back({(int)c, (int)f, (int)std::min<long long>(kQrChunk, len - f), 0});
     const long long plen = (long long)s->cdesc[c].n * RP;
     for (long long f = 0; f < plen; f += 1024)
       s->ps.push_back({(int)c, (int)f, (int)std::min<long long>(1024, plen - f), 0});
@@ -680,7 +724,22 @@ struct Ops {
     const int n_items = is_q ? a.n_gsq : a.n_gsp;
     const int grid = std::max(1, std::min(n_items, s->sms * 4));
     const float* src_dense = is_q ? s->qdraw : s->praw;
-    if (!is_q && !s->fold_psum && do_psum) {
+    const bool psum = !is_q && !s->fold_psum && do_psum;
+    if (s->gs_fused && s->gs_coop) {
+      // the whole stage (with the P_raw sum) in one cooperative launch
+      const bool parts = !is_q && s->fold_psum;
+      L.begin(K_GS);
+      const cudaError_t e = launch_gs_coop<RP>(
+          a, parts ? s->praw_part : src_dense, parts ? s->praw : nullptr, is_q, parts ? 1 : 0, s->pgs,
+          is_q ? s->qinit : s->Pf, is_q ? -1 : 1, psum ? 1 : 0, s->gs_bar,
+          std::max(grid, psum ? std::min(a.n_ps, s->sms * 4) : 1), L.st);
+      L.end();
+      if (e == cudaSuccess) return;
+      // refused (no cooperative launch here): the three-launch stage from now on
+      (void)cudaGetLastError();
+      s->gs_coop = 0;
+    }
+    if (psum) {
       // P_raw = sum of pass 1's column-tile partials
       L.begin(K_PSUM);
       launch_psum<RP>(a, std::max(1, std::min(a.n_ps, s->sms * 8)), L.st);
@@ -1104,6 +1163,7 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   TRY(dalloc(s, (void**)&s->tmat, std::max(1, nt) * RP * RP * sizeof(float)));
   TRY(dalloc(s, (void**)&s->tmat2, std::max(1, nt) * RP * RP * sizeof(float)));
   TRY(dalloc(s, (void**)&s->gs_cnt, std::max(1, nt) * sizeof(int)));
+  TRY(dalloc(s, (void**)&s->gs_bar, 16));
   TRY(zero_now(s->gs_cnt, std::max(1, nt) * sizeof(int)));
   TRY(dalloc(s, (void**)&s->gram, std::max<size_t>(1, std::max(s->gsp.size(), s->gsq.size())) * RP * RP * sizeof(float2)));
   TRY(dalloc(s, (void**)&s->gram_t, std::max(1, nt) * RP * RP * sizeof(float2)));

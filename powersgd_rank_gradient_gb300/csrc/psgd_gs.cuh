@@ -27,15 +27,14 @@ namespace psgd {
 // then reads dense rows).  Each work item is a chunk of one tensor's rows x RP
 // values, four per thread.
 template <int RP>
-__global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
-  if (a.ctrl->flag) return;
-  for (int it = blockIdx.x; it < a.n_ps; it += gridDim.x) {
+__device__ __forceinline__ void psum_item(const StepArgs& a, int it) {
+  {
     const GsItem gi = a.ps_items[it];
     const TensorDesc td = a.tensors[gi.t];
     const long long len = (long long)td.n * RP;
     const float* src = a.praw_part + td.pp_off;
     const int f = gi.row0 + threadIdx.x * 4;
-    if (f >= gi.row0 + gi.nrows) continue;
+    if (f >= gi.row0 + gi.nrows) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (RP >= 4) {
       int c = 0;
@@ -61,43 +60,73 @@ __global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
   }
 }
 
-// Q'(j, k) = sum over row blocks of the partials, in row-block order, written
-// k-major into the next half of Qf (or, in the data-parallel split, into the
-// exchange buffer a.qx, same layout).  Each work item is a chunk of one
-// tensor's RP * m values, four per thread.
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
+  if (a.ctrl->flag) return;
+  for (int it = blockIdx.x; it < a.n_ps; it += gridDim.x) psum_item<RP>(a, it);
+}
+
+// Q'(j, k) = sum over row blocks of the partials, written k-major into the
+// next half of Qf (or, in the data-parallel split, into the exchange buffer
+// a.qx, same layout).  Each work item is a chunk of kQrChunk values of one
+// tensor's RP * m; four consecutive lanes share four consecutive values, lane
+// q summing (in row-block order) the q-th quarter of the row blocks, and the
+// quarters are added in order (((s0 + s1) + s2) + s3): a quarter of the
+// dependent loads of one chain per value, eight of them in flight.
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
   if (a.ctrl->flag) return;
   float* Q = a.qx ? a.qx : a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
+  const int q = threadIdx.x & 3;
   for (int it = blockIdx.x; it < a.n_qr; it += gridDim.x) {
     const GsItem gi = a.qr_items[it];
     const TensorDesc td = a.tensors[gi.t];
     const long long len = (long long)RP * td.m;
     const float* src = a.qpart + td.qp_off;
-    const int f = gi.row0 + threadIdx.x * 4;
-    if (f >= gi.row0 + gi.nrows) continue;
-    if (len % 4 == 0) {
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      int b = 0;
-      // eight row blocks' loads in flight, added in row-block order
-      for (; b + 8 <= td.rblocks; b += 8) {
+    const int f = gi.row0 + (threadIdx.x >> 2) * 4;   // this lane group's first value
+    const int nb = td.rblocks;
+    const int b0 = (int)((long long)nb * q / 4), b1 = (int)((long long)nb * (q + 1) / 4);
+    const bool live = f < gi.row0 + gi.nrows;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live && len % 4 == 0) {
+      int b = b0;
+      for (; b + 8 <= b1; b += 8) {
         float4 x[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) x[u] = ld_stream4(src + (long long)(b + u) * len + f);
 #pragma unroll
         for (int u = 0; u < 8; ++u) { s.x += x[u].x; s.y += x[u].y; s.z += x[u].z; s.w += x[u].w; }
       }
-      for (; b < td.rblocks; ++b) {
-        float4 x = ld_stream4(src + (long long)b * len + f);
+      for (; b < b1; ++b) {
+        const float4 x = ld_stream4(src + (long long)b * len + f);
         s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
       }
-      *reinterpret_cast<float4*>(Q + td.q_off + f) = s;
-    } else {
-      for (int e = f; e < min(f + 4, gi.row0 + gi.nrows); ++e) {
-        float s = 0.f;
-        for (int b = 0; b < td.rblocks; ++b) s += src[(long long)b * len + e];
-        Q[td.q_off + e] = s;
+    } else if (live) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = 0.f;
+        if (f + e < gi.row0 + gi.nrows)
+          for (int b = b0; b < b1; ++b) v += src[(long long)b * len + f + e];
+        if (e == 0) s.x = v; else if (e == 1) s.y = v; else if (e == 2) s.z = v; else s.w = v;
       }
+    }
+    // the quarters in order: lane q = 0 of the group adds q = 1, 2, 3
+    float4 t = s;
+#pragma unroll
+    for (int j = 1; j < 4; ++j) {
+      const float x = __shfl_down_sync(0xffffffffu, s.x, j), y = __shfl_down_sync(0xffffffffu, s.y, j);
+      const float z = __shfl_down_sync(0xffffffffu, s.z, j), w = __shfl_down_sync(0xffffffffu, s.w, j);
+      t.x += x; t.y += y; t.z += z; t.w += w;
+    }
+    if (!live || q != 0) continue;
+    if (len % 4 == 0) {
+      *reinterpret_cast<float4*>(Q + td.q_off + f) = t;
+    } else {
+      const int ne = min(4, gi.row0 + gi.nrows - f);
+      Q[td.q_off + f] = t.x;
+      if (ne > 1) Q[td.q_off + f + 1] = t.y;
+      if (ne > 2) Q[td.q_off + f + 2] = t.z;
+      if (ne > 3) Q[td.q_off + f + 3] = t.w;
     }
   }
 }
@@ -441,7 +470,7 @@ __device__ __forceinline__ void apply_item(const StepArgs& a, int it, const floa
   const TensorDesc td = a.tensors[gi.t];
   const long long base = is_q ? td.q_off : td.p_off;
   __syncthreads();
-  for (int idx = threadIdx.x; idx < RP * RP; idx += kThreads) T[idx] = tsrc[(long long)gi.t * RP * RP + idx];
+  for (int idx = threadIdx.x; idx < RP * RP; idx += kThreads) T[idx] = __ldcg(tsrc + (long long)gi.t * RP * RP + idx);
   __syncthreads();
   const int span = is_q ? (gi.nrows + 31) / 32 * 32 * KG : gi.nrows * KG;
   for (int idx = threadIdx.x; idx < span; idx += kThreads) {
@@ -568,6 +597,80 @@ __global__ void __launch_bounds__(kThreads) k_gs_second(const StepArgs a, const 
     gram_item<RP>(a, it, mid, nullptr, is_q, 0, a.gram, tile, red);
     gs_count_and_solve<RP>(a, it, is_q, 1, a.tmat2, &last_s);
   }
+}
+
+// ---------------------------------------------------------------------------
+// The fused stage in one cooperative launch (all CTAs resident): the P_raw
+// sum (when asked), k_gs_first's, k_gs_second's and the final apply's work
+// in the same order and on the same items, with grid-wide barriers where the
+// launches ended.  Each CTA takes the same items in every phase, so the rows
+// a phase reads back (X, X T) are the CTA's own writes; the transforms come
+// from the tensors' last CTAs through L2.
+//
+// grid_barrier: CTA k of the launch's b-th barrier adds one to *bar (zeroed
+// before the launch) and waits until it reaches b x gridDim.x.  The wait is
+// bounded: after kBarrierPolls polls it sets the step's timeout flag (the
+// commit then leaves the state unchanged and the step reports PSGD_ETIMEOUT)
+// and the CTA returns.
+// ---------------------------------------------------------------------------
+constexpr long kBarrierPolls = 1L << 22;
+
+__device__ __forceinline__ bool grid_barrier(const StepArgs& a, unsigned int* bar, unsigned int target, int* ok_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    int ok = 0;
+    for (long i = 0; i < kBarrierPolls; ++i) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
+      if (v >= target) {
+        ok = 1;
+        break;
+      }
+      __nanosleep(32);
+    }
+    if (!ok) atomicExch(&a.ctrl->timeout, 1);
+    __threadfence();
+    *ok_s = ok;
+  }
+  __syncthreads();
+  return *ok_s != 0;
+}
+
+template <int RP>
+__global__ void __launch_bounds__(kThreads) k_gs_coop(const StepArgs a, const float* __restrict__ src,
+                                                      float* __restrict__ dense_out, int is_q, int from_parts,
+                                                      float* __restrict__ mid, float* __restrict__ dst,
+                                                      int dst_half, int do_psum, unsigned int* bar) {
+  __shared__ float tile[kGramTile][RP + 1];
+  __shared__ float2 red[kThreads];
+  __shared__ __align__(16) float T[RP * RP];
+  __shared__ int last_s, ok_s;
+  const int n_items = is_q ? a.n_gsq : a.n_gsp;
+  if (a.ctrl->flag) return;   // the same for every CTA: none waits at a barrier
+  unsigned int nb = 0;
+  if (do_psum) {
+    for (int it = blockIdx.x; it < a.n_ps; it += gridDim.x) psum_item<RP>(a, it);
+    if (!grid_barrier(a, bar, ++nb * gridDim.x, &ok_s)) return;
+  }
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    gram_item<RP>(a, it, src, dense_out, is_q, from_parts, a.gram, tile, red);
+    gs_count_and_solve<RP>(a, it, is_q, 0, a.tmat, &last_s);
+  }
+  if (!grid_barrier(a, bar, ++nb * gridDim.x, &ok_s)) return;
+  const float* x = dense_out ? dense_out : src;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    apply_item<RP>(a, it, x, mid, is_q, 0, a.tmat, T);
+    __syncthreads();   // the CTA's rows of X T are visible to its Gram
+    gram_item<RP>(a, it, mid, nullptr, is_q, 0, a.gram, tile, red);
+    gs_count_and_solve<RP>(a, it, is_q, 1, a.tmat2, &last_s);
+  }
+  if (!grid_barrier(a, bar, ++nb * gridDim.x, &ok_s)) return;
+  long long half_off = 0;
+  if (dst_half >= 0) half_off = (long long)(a.ctrl->cur ^ 1) * (is_q ? a.q_total : a.p_total);
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x)
+    apply_item<RP>(a, it, mid, dst, is_q, half_off, a.tmat2, T);
 }
 
 }  // namespace psgd

@@ -30,6 +30,7 @@ constexpr int kFineRows = 128;     // rows per work item of pass 1 (ranks <= 8; 
 constexpr int kRows1High = 128;   // rows per work item of pass 1 (ranks 16 and 32)
 constexpr int kFineRows3 = 32;     // rows per work item of pass 3 and the error views
 constexpr int kGsRows = 256;       // rows per work item of the Gram-Schmidt kernels
+constexpr int kQrChunk = kThreads;  // values per work item of the Q reduction (64 groups of four)
 
 // Columns per thread (CPT) and column-tile width of the streaming passes for
 // a padded rank RP: the per-thread accumulators hold CPT x RP floats.

@@ -21,6 +21,9 @@ template <int RP> void launch_gs_first(const StepArgs& a, const float* src, floa
                                        int from_parts, int grid, cudaStream_t s);
 template <int RP> void launch_gs_second(const StepArgs& a, const float* src, float* mid, int is_q, int grid,
                                         cudaStream_t s);
+template <int RP> cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out, int is_q,
+                                              int from_parts, float* mid, float* dst, int dst_half, int do_psum,
+                                              unsigned int* bar, int grid, cudaStream_t s);
 template <int RP> void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s);
 template <int RP> void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s);
 template <int RP> void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s);

@@ -121,6 +121,30 @@ void launch_gs_second(const StepArgs& a, const float* src, float* mid, int is_q,
   k_gs_second<RP><<<grid, kThreads, 0, s>>>(a, src, mid, is_q);
 }
 
+// The fused stage as one cooperative launch (every CTA resident, which the
+// cooperative launch guarantees or refuses): at most `grid` CTAs and no more
+// than fit on the device at once.  *bar is zeroed first on the same stream.
+template <int RP>
+cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts,
+                           float* mid, float* dst, int dst_half, int do_psum, unsigned int* bar, int grid,
+                           cudaStream_t s) {
+  static int fit = -1;
+  if (fit < 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gs_coop<RP>, kThreads, 0);
+    fit = std::max(0, per_sm * sms);
+  }
+  if (fit == 0) return cudaErrorCooperativeLaunchTooLarge;
+  grid = std::max(1, std::min(grid, fit));
+  cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  void* args[] = {const_cast<StepArgs*>(&a), &src, &dense_out, &is_q, &from_parts, &mid, &dst, &dst_half,
+                  &do_psum, &bar};
+  return cudaLaunchCooperativeKernel((const void*)k_gs_coop<RP>, dim3(grid), dim3(kThreads), args, 0, s);
+}
+
 template <int RP, int NSRC>
 void launch_pass2_tc(const StepArgs& a, int src_mode, cudaStream_t s) {
   using T = Pass2Tc<RP, NSRC>;
@@ -221,6 +245,8 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
                                   cudaStream_t, const float*);                                  \
   template void launch_gs_first<RPV>(const StepArgs&, const float*, float*, int, int, int,      \
                                      cudaStream_t);                                             \
+  template cudaError_t launch_gs_coop<RPV>(const StepArgs&, const float*, float*, int, int, float*, float*, \
+                                            int, int, unsigned int*, int, cudaStream_t);                \
   template void launch_gs_second<RPV>(const StepArgs&, const float*, float*, int, int,          \
                                       cudaStream_t);                                            \
   template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
