@@ -615,12 +615,15 @@ void build_plan(psgd_state* s) {
     for (int r0 = 0; r0 < td.m; r0 += per_q) s->gsq.push_back({(int)c, r0, std::min(per_q, td.m - r0), 0});
     s->gsq_count.push_back((int)s->gsq.size() - s->gsq_first.back());
   }
-  // the fused Gram-Schmidt stage: ranks up to 8 and at most 128 row items
-  // per tensor (the completing CTA adds a tensor's partials by itself)
+  // the fused Gram-Schmidt stage: ranks up to 16 and at most 128 row items
+  // per tensor (the completing CTA adds a tensor's partials and solves by
+  // itself while the others wait at the next barrier; at rank 32 the 32 x 32
+  // sums and solves are long enough that the eight-launch stage, whose sums
+  // spread over many CTAs, is faster: 8192 x 8192 stage 190 against 127 us)
   {
     int most = 0;
     for (size_t c = 0; c < s->cdesc.size(); ++c) most = std::max(most, std::max(s->gsp_count[c], s->gsq_count[c]));
-    s->gs_fused = (RP <= 8 && most <= 128) ? 1 : 0;
+    s->gs_fused = (RP <= 16 && most <= 128) ? 1 : 0;
   }
 }
 
@@ -720,7 +723,9 @@ template <int RP>
 struct Ops {
   // do_psum: P_raw still has to be summed from pass 1's partials (the
   // data-parallel split sums them before its exchange instead)
-  static void gs(psgd_state* s, const StepArgs& a, Launcher& L, int is_q, bool do_psum = true) {
+  // Returns true when the stage also wrote P's operand images (ranks 16 and
+  // 32, the cooperative launch), so images(mode 0) is not needed.
+  static bool gs(psgd_state* s, const StepArgs& a, Launcher& L, int is_q, bool do_psum = true) {
     const int n_items = is_q ? a.n_gsq : a.n_gsp;
     const int grid = std::max(1, std::min(n_items, s->sms * 4));
     const float* src_dense = is_q ? s->qdraw : s->praw;
@@ -731,10 +736,10 @@ struct Ops {
       L.begin(K_GS);
       const cudaError_t e = launch_gs_coop<RP>(
           a, parts ? s->praw_part : src_dense, parts ? s->praw : nullptr, is_q, parts ? 1 : 0, s->pgs,
-          is_q ? s->qinit : s->Pf, is_q ? -1 : 1, psum ? 1 : 0, s->gs_bar,
+          is_q ? s->qinit : s->Pf, is_q ? -1 : 1, psum ? 1 : 0, s->gs_bar, (RP >= 16 && !is_q) ? 1 : 0,
           std::max(grid, psum ? std::min(a.n_ps, s->sms * 4) : 1), L.st);
       L.end();
-      if (e == cudaSuccess) return;
+      if (e == cudaSuccess) return RP >= 16 && !is_q;
       // refused (no cooperative launch here): the three-launch stage from now on
       (void)cudaGetLastError();
       s->gs_coop = 0;
@@ -762,7 +767,7 @@ struct Ops {
       else
         launch_apply<RP>(a, s->pgs, s->Pf, 0, 1, grid, L.st, s->tmat2);
       L.end();
-      return;
+      return false;
     }
     L.begin(K_GRAM);
     if (is_q || !s->fold_psum) {
@@ -793,6 +798,7 @@ struct Ops {
     else
       launch_apply<RP>(a, s->pgs, s->Pf, 0, 1, grid, L.st);
     L.end();
+    return false;
   }
 
   // ranks 16 and 32: the factor images the tensor-core passes read
@@ -824,15 +830,13 @@ struct Ops {
     L.begin(K_PASS1);
     launch_pass1<RP>(a, grid_p1, L.st);
     L.end();
-    gs(s, a, L, 0);
-    images(s, a, L, 0);
+    if (!gs(s, a, L, 0)) images(s, a, L, 0);
     L.begin(K_PASS2);
     launch_pass2<RP>(a, s->pass2_src, grid_items, L.st);
     L.end();
     L.begin(K_QREDUCE);
-    launch_qreduce<RP>(a, grid_qr, L.st);
+    launch_qreduce<RP>(a, grid_qr, L.st, RP >= 16 ? 1 : 0);   // with Q's row image
     L.end();
-    images(s, a, L, 1);
     L.begin(K_PASS3);
     launch_pass3<RP>(a, 0, grid_fine, L.st);
     L.end();
@@ -867,8 +871,7 @@ struct Ops {
   static void dp_project(psgd_state* s, const StepArgs& a, Launcher& L) {
     const int grid_items = std::max(1, std::min(a.n_items, s->sms * 3));
     const int grid_qr = std::max(1, std::min(a.n_qr, s->sms * 8));
-    gs(s, a, L, 0, false);
-    images(s, a, L, 0);
+    if (!gs(s, a, L, 0, false)) images(s, a, L, 0);
     L.begin(K_PASS2);
     launch_pass2<RP>(a, s->pass2_src, grid_items, L.st);
     L.end();

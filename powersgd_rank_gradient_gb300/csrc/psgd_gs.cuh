@@ -6,6 +6,7 @@
 #pragma once
 
 #include "psgd_kernels.cuh"
+#include "psgd_tc.cuh"
 
 namespace psgd {
 
@@ -73,8 +74,9 @@ __global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
 // q summing (in row-block order) the q-th quarter of the row blocks, and the
 // quarters are added in order (((s0 + s1) + s2) + s3): a quarter of the
 // dependent loads of one chain per value, eight of them in flight.
+// img (ranks 16 and 32): also write Q's row image, as k_images mode 1 does.
 template <int RP>
-__global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
+__global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a, int img) {
   if (a.ctrl->flag) return;
   float* Q = a.qx ? a.qx : a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
   const int q = threadIdx.x & 3;
@@ -119,6 +121,15 @@ __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a) {
       t.x += x; t.y += y; t.z += z; t.w += w;
     }
     if (!live || q != 0) continue;
+    if constexpr (RP >= 16) {
+      if (img) {
+        const int ne = min(4, gi.row0 + gi.nrows - f);
+        const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e < ne) img_put_q<RP>(a, td, (f + e) % td.m, (f + e) / td.m, tv[e], false);
+      }
+    }
     if (len % 4 == 0) {
       *reinterpret_cast<float4*>(Q + td.q_off + f) = t;
     } else {
@@ -459,7 +470,9 @@ __global__ void __launch_bounds__(kThreads) k_solve(const StepArgs a, const floa
 // over the row's RP inputs.  P (row-major) puts a row's KG threads next to
 // each other; Q (k-major) puts 32 consecutive rows in a warp, so its column
 // reads and writes are coalesced.
-template <int RP>
+// IMG (P, ranks 16 and 32): also write the output rows into P's operand
+// images (row and chunk), as k_images mode 0 does.
+template <int RP, bool IMG = false>
 __device__ __forceinline__ void apply_item(const StepArgs& a, int it, const float* __restrict__ src,
                                            float* __restrict__ dst, int is_q, long long half_off,
                                            const float* __restrict__ tsrc, float* T) {
@@ -498,6 +511,12 @@ __device__ __forceinline__ void apply_item(const StepArgs& a, int it, const floa
       } else {
 #pragma unroll
         for (int o = 0; o < OPT; ++o) y[o] = fmaf(x[l], T[l * RP + o], y[o]);
+      }
+    }
+    if constexpr (IMG) {
+      if (!is_q) {
+#pragma unroll
+        for (int o = 0; o < OPT; ++o) img_put_p<RP>(a, td, row, kg * OPT + o, y[o], true);
       }
     }
     if (is_q) {
@@ -642,7 +661,7 @@ template <int RP>
 __global__ void __launch_bounds__(kThreads) k_gs_coop(const StepArgs a, const float* __restrict__ src,
                                                       float* __restrict__ dense_out, int is_q, int from_parts,
                                                       float* __restrict__ mid, float* __restrict__ dst,
-                                                      int dst_half, int do_psum, unsigned int* bar) {
+                                                      int dst_half, int do_psum, unsigned int* bar, int img) {
   __shared__ float tile[kGramTile][RP + 1];
   __shared__ float2 red[kThreads];
   __shared__ __align__(16) float T[RP * RP];
@@ -669,8 +688,12 @@ __global__ void __launch_bounds__(kThreads) k_gs_coop(const StepArgs a, const fl
   if (!grid_barrier(a, bar, ++nb * gridDim.x, &ok_s)) return;
   long long half_off = 0;
   if (dst_half >= 0) half_off = (long long)(a.ctrl->cur ^ 1) * (is_q ? a.q_total : a.p_total);
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x)
-    apply_item<RP>(a, it, mid, dst, is_q, half_off, a.tmat2, T);
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    if (RP >= 16 && img)
+      apply_item<RP, true>(a, it, mid, dst, is_q, half_off, a.tmat2, T);
+    else
+      apply_item<RP>(a, it, mid, dst, is_q, half_off, a.tmat2, T);
+  }
 }
 
 }  // namespace psgd

@@ -126,8 +126,8 @@ void launch_gs_second(const StepArgs& a, const float* src, float* mid, int is_q,
 // than fit on the device at once.  *bar is zeroed first on the same stream.
 template <int RP>
 cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts,
-                           float* mid, float* dst, int dst_half, int do_psum, unsigned int* bar, int grid,
-                           cudaStream_t s) {
+                           float* mid, float* dst, int dst_half, int do_psum, unsigned int* bar, int img,
+                           int grid, cudaStream_t s) {
   static int fit = -1;
   if (fit < 0) {
     int dev = 0, sms = 0, per_sm = 0;
@@ -141,7 +141,7 @@ cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out
   cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<StepArgs*>(&a), &src, &dense_out, &is_q, &from_parts, &mid, &dst, &dst_half,
-                  &do_psum, &bar};
+                  &do_psum, &bar, &img};
   return cudaLaunchCooperativeKernel((const void*)k_gs_coop<RP>, dim3(grid), dim3(kThreads), args, 0, s);
 }
 
@@ -196,8 +196,8 @@ void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s) {
 }
 
 template <int RP>
-void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s) {
-  k_qreduce<RP><<<grid, kThreads, 0, s>>>(a);
+void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s, int img) {
+  k_qreduce<RP><<<grid, kThreads, 0, s>>>(a, img);
 }
 
 template <int RP>
@@ -246,11 +246,11 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
   template void launch_gs_first<RPV>(const StepArgs&, const float*, float*, int, int, int,      \
                                      cudaStream_t);                                             \
   template cudaError_t launch_gs_coop<RPV>(const StepArgs&, const float*, float*, int, int, float*, float*, \
-                                            int, int, unsigned int*, int, cudaStream_t);                \
+                                            int, int, unsigned int*, int, int, cudaStream_t);           \
   template void launch_gs_second<RPV>(const StepArgs&, const float*, float*, int, int,          \
                                       cudaStream_t);                                            \
   template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
-  template void launch_qreduce<RPV>(const StepArgs&, int, cudaStream_t);                        \
+  template void launch_qreduce<RPV>(const StepArgs&, int, cudaStream_t, int);                        \
   template void launch_pass3<RPV>(const StepArgs&, int, int, cudaStream_t);                     \
   template void launch_images<RPV>(const StepArgs&, int, int, cudaStream_t);
 

@@ -222,6 +222,39 @@ __device__ __forceinline__ void timed_out(const StepArgs& a) { atomicExch(&a.ctr
 
 }  // namespace tc
 
+// Writers of one factor value x = X(r, k) into the operand images (hi and lo
+// halves; layouts below, at k_images).  P: its row image and, when `chunk`,
+// its chunk image.  Q (r = the column index): its row image or its chunk image.
+template <int RP>
+__device__ __forceinline__ void img_put_p(const StepArgs& a, const TensorDesc& td, long long r, int k, float x,
+                                          bool chunk) {
+  const float h = tc::hi_part(x), l = x - h;
+  const long long rpad = (td.n + 127) / 128 * 128;
+  const long long o = td.pi_off + tc::swz((int)r, k);
+  a.img[o] = h;
+  a.img[o + rpad * 32] = l;
+  if (chunk) {
+    const long long c = td.pti_off + (r >> 5) * 2 * RP * 32 + tc::swz(k, (int)(r & 31));
+    a.img[c] = h;
+    a.img[c + RP * 32] = l;
+  }
+}
+template <int RP>
+__device__ __forceinline__ void img_put_q(const StepArgs& a, const TensorDesc& td, long long r, int k, float x,
+                                          bool chunk) {
+  const float h = tc::hi_part(x), l = x - h;
+  if (!chunk) {
+    const long long rpad = (td.m + 127) / 128 * 128;
+    const long long o = td.qi_off + tc::swz((int)r, k);
+    a.img[o] = h;
+    a.img[o + rpad * 32] = l;
+  } else {
+    const long long c = td.qti_off + (r >> 5) * 2 * RP * 32 + tc::swz(k, (int)(r & 31));
+    a.img[c] = h;
+    a.img[c + RP * 32] = l;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Operand images of the factors (ranks 16 and 32), hi and lo halves:
 //   row image of X (R x RP): rows r of 32 values (zero beyond RP), the layout
@@ -259,8 +292,6 @@ __global__ void __launch_bounds__(kThreads) k_images(const StepArgs a, int mode)
     const bool is_p = it < np;
     const GsItem gi = is_p ? a.gsp_items[it] : a.gsq_items[it - np];
     const TensorDesc td = a.tensors[gi.t];
-    const int R = is_p ? td.n : td.m;
-    const long long rpad = (R + 127) / 128 * 128;
     for (int idx = threadIdx.x; idx < gi.nrows * RP; idx += kThreads) {
       int r, k;
       float x;
@@ -273,23 +304,12 @@ __global__ void __launch_bounds__(kThreads) k_images(const StepArgs a, int mode)
         r = gi.row0 + idx % gi.nrows;
         x = Qsrc[td.q_off + (long long)k * td.m + r];
       }
-      const float h = tc::hi_part(x);
-      const float l = x - h;
-      const bool row_img = is_p ? true : (mode != 2);
-      const bool chunk_img = is_p ? (mode == 0) : (mode == 2);
-      if (row_img) {
-        const long long base = is_p ? td.pi_off : td.qi_off;
-        const long long o = base + tc::swz(r, k);
-        a.img[o] = h;
-        a.img[o + rpad * 32] = l;
-      }
-      if (chunk_img) {
-        // chunk (r / 32): RP rows of hi, then RP rows of lo (one stacked operand)
-        const long long base = is_p ? td.pti_off : td.qti_off;
-        const long long o = base + (long long)(r >> 5) * 2 * RP * 32 + tc::swz(k, r & 31);
-        a.img[o] = h;
-        a.img[o + RP * 32] = l;
-      }
+      // chunk images: for chunk r / 32, RP rows of hi then RP rows of lo (one
+      // stacked operand)
+      if (is_p)
+        img_put_p<RP>(a, td, r, k, x, mode == 0);
+      else
+        img_put_q<RP>(a, td, r, k, x, mode == 2);
     }
   }
 }
