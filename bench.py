@@ -395,6 +395,7 @@ def run_native(spec, args, dist, rank_id, world, device, light=False):
         kernels=kernels, counts=counts, dtype=spec["dtype"], loss_scale=spec["loss_scale"])
     if not light:
         res["rows"] = run_rows(spec, args, dist, device, sets, out, W, N)
+        res["rows"]["steady_step_graph"] = run_graph(st, spec, args, dist, device, sets[0], out, W, N)
         if args.batched:
             res["rows"]["next_batched_hook"] = run_batched(spec, args, dist, device, sets, out, W, N)
         if args.buckets > 0:
@@ -404,6 +405,39 @@ def run_native(spec, args, dist, rank_id, world, device, light=False):
     if not args.no_e2e and not light:
         res["e2e"] = run_e2e(st, spec, args, dist, device, N, W)
     st.close()
+    return res
+
+
+def run_graph(st, spec, args, dist, device, grads, out, W, N):
+    """The same steady step replayed as one CUDA graph (psgd_set_graph), against
+    the launched step on the same inputs: what launch gaps cost.  The graph is
+    keyed by the buffers' addresses, so both runs step one resident input set
+    (far larger than L2).  No per-kernel events inside a graph: step time only."""
+    import torch
+
+    stream = torch.cuda.current_stream(device)
+    inv_scale = 1.0 / spec["loss_scale"]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    res = {}
+    for label, graph in (("launched_ms_per_step", False), ("graph_ms_per_step", True)):
+        st.set_graph(graph)
+        for _ in range(3):
+            st.step(grads, out=out, inv_loss_scale=inv_scale)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(args.steps):
+            st.step(grads, out=out, inv_loss_scale=inv_scale)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        res[label] = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
+    caps, reps = st.graph_stats()
+    st.set_graph(False)
+    if st.status():
+        raise RuntimeError("graph-replayed step was skipped (non-finite input)")
+    res["graph_gradient_gbs"] = W * N * GSIZE[spec["dtype"]] / (res["graph_ms_per_step"] / 1e3) / 1e9
+    res["graph_captures"] = caps
+    res["graph_replays"] = reps
     return res
 
 
@@ -614,18 +648,21 @@ def run_e2e(st, spec, args, dist, device, N, W):
 # oracle timing (CPU baseline / reference arm)
 # ---------------------------------------------------------------------------
 def oracle_sample(spec, budget):
-    """A window of the bucket's tensors (skipping any tensor larger than the
-    budget) with at most `budget` elements."""
-    sel = []
+    """The first tensor of each distinct shape, in bucket order, up to `budget`
+    elements (a tensor larger than the budget is skipped): every kind of layer
+    matrix and vector of the bucket, once."""
+    sel, seen = [], set()
     tot = 0
     for s in spec["shapes"]:
+        key = tuple(s)
+        if key in seen:
+            continue
         n = 1
         for d in s:
             n *= d
-        if n > budget:
+        if n > budget or tot + n > budget:
             continue
-        if tot + n > budget:
-            break
+        seen.add(key)
         sel.append(s)
         tot += n
     return sel, tot
@@ -639,7 +676,7 @@ def time_oracle(spec, steps, budget=None, target_s=None, warmup=1):
 
     W = spec["world_size"]
     if budget is None:
-        budget = 2_000_000 if W >= 8 else 6_000_000
+        budget = 10_500_000 if W >= 8 else (13_000_000 if W >= 4 else 32_000_000)
     shapes, n = oracle_sample(spec, budget)
     if not shapes:
         shapes, n = spec["shapes"][:1], 1
@@ -661,8 +698,8 @@ def time_oracle(spec, steps, budget=None, target_s=None, warmup=1):
             break
     t = statistics.median(times)
     return dict(value=W * n * GSIZE[spec["dtype"]] / t / 1e9, unit=UNIT, cores=os.cpu_count(), kind="oracle",
-                sample=f"{len(shapes)} tensors ({n} elements per replica, W={W}) of the {spec['name']} "
-                       f"bucket, fp64 NumPy, median of {len(times)} steps",
+                sample=f"{len(shapes)} tensors, the first of each distinct shape ({n} elements per replica, "
+                       f"W={W}) of the {spec['name']} bucket, fp64 NumPy, median of {len(times)} steps",
                 s_per_step=t)
 
 
