@@ -483,10 +483,11 @@ struct Pass1CS {
   static constexpr int XOFF = WT * (GSEG + ESEG);
   static constexpr int UNIT_BYTES = XOFF + (SH ? 2 * WT * 16 : 0);   // one row x 128 columns
   static constexpr int RED_BYTES = rows1_for(RP) * NCH * RP * 4;
-  static constexpr int BUDGET = (MINB == 1 ? 200 * 1024 : 112 * 1024) - RED_BYTES;
+  static constexpr int PST_BYTES = rows1_for(RP) * RP * 4;          // the item's committed P rows
+  static constexpr int BUDGET = (MINB == 1 ? 200 * 1024 : 112 * 1024) - RED_BYTES - PST_BYTES;
   static constexpr int S_RAW = BUDGET / (8 * UNIT_BYTES);
   static constexpr int S = S_RAW > 8 ? 8 : (S_RAW < 2 ? 2 : S_RAW);
-  static constexpr int SMEM = 8 * S * UNIT_BYTES + RED_BYTES;
+  static constexpr int SMEM = 8 * S * UNIT_BYTES + RED_BYTES + PST_BYTES;
 };
 
 // Four values of a row that starts r elements (0..3, warp-uniform) into the
@@ -534,7 +535,8 @@ template <int RP, int WT, typename GT, int MINB, int MODE, bool PW = false>
 __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDesc& td, const Item& item,
                                               const float* __restrict__ Qp, const float* __restrict__ Qc,
                                               const float* __restrict__ Pc, int cur, float& chk,
-                                              char* __restrict__ wsm, float* __restrict__ red) {
+                                              char* __restrict__ wsm, float* __restrict__ red,
+                                              float* __restrict__ pst) {
   constexpr bool SH = (MODE == 1);
   using St = Pass1CS<RP, WT, GT, MINB, SH>;
   constexpr int S = St::S;
@@ -552,11 +554,14 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
   const int phase = warp / nch;
   const bool unit_scale = (a.scale == 1.0f);
   const bool same_q = (Qp == Qc);
-  if (warp < nch * wpc) {
+  // pass-1 tiles have 8, 4, 2 or 1 chunks, so every warp has a chunk; a warp
+  // without one would take no units but still meet the CTA barriers
+  const bool active = warp < nch * wpc;
+  {
     const int c = item.col0 + ch * 128 + lane * 4;
-    const bool cin = c < cend;
+    const bool cin = active && c < cend;
     const int ncv = cin ? (int)min(4LL, (long long)cend - c) : 0;   // this lane's columns in the tile
-    const int units = phase < item.nrows ? (item.nrows - phase + wpc - 1) / wpc : 0;
+    const int units = (active && phase < item.nrows) ? (item.nrows - phase + wpc - 1) / wpc : 0;
     float qc[4][RP], qp[4][RP];
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc)
@@ -657,19 +662,27 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       }
       cp_async_commit();
     };
+    // the item's committed P rows into shared memory, copied (one group of
+    // its own) ahead of the first units and read there by every warp: the
+    // unit loop then waits on no global load
+    if (a.ef) {
+      const float* psrc = Pc + td.p_off + (long long)item.row0 * RP;
+      const int nv = item.nrows * RP;
+      if constexpr (RP >= 4) {   // P rows (RP floats) are 16-byte aligned
+        for (int idx = threadIdx.x * 4; idx < nv; idx += kThreads * 4) cp_async16(pst + idx, psrc + idx);
+      } else {
+        for (int idx = threadIdx.x; idx < nv; idx += kThreads) cp_async4(pst + idx, psrc + idx);
+      }
+    }
+    cp_async_commit();
 #pragma unroll
     for (int u = 0; u < S - 1; ++u) {
       const long long r = row_first + (long long)u * wpc;
       if (u < units) issue(wsm + u * St::UNIT_BYTES, td.g_off + r * m + c, ecur + td.c_off + r * ld + c);
       else cp_async_commit();
     }
-    // the committed P row of the next unit is loaded one unit ahead
-    const float* p_next = Pc + td.p_off + row_first * RP;
-    float pn[RP];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) pn[k] = 0.f;
-    if (a.ef && units > 0) load_row<RP>(p_next, pn);
-    p_next += wpc * RP;
+    cp_async_wait<S - 1>();   // this thread's P pieces have landed (the units may not)
+    __syncthreads();          // and every thread's
     long long r_off = td.c_off + row_first * ld + c;   // store / mbar offset of the unit
     long long g_pos = row_first * m + c;               // its position in the tensor's view
     const long long g_ahead = td.g_off + (S - 1) * gstep, e_ahead = ecur + (S - 1) * estep;
@@ -686,11 +699,20 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       const char* slot = wsm + s_use * St::UNIT_BYTES;
       s_use = (s_use + 1 == S) ? 0 : s_use + 1;
       float po[RP];
+      if (a.ef) {
+        if constexpr (RP >= 4) {
 #pragma unroll
-      for (int k = 0; k < RP; ++k) po[k] = pn[k];
-      if (a.ef && u + 1 < units) {
-        load_row<RP>(p_next, pn);
-        p_next += wpc * RP;
+          for (int k = 0; k < RP; k += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(pst + rr * RP + k);
+            po[k] = x.x; po[k + 1] = x.y; po[k + 2] = x.z; po[k + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < RP; ++k) po[k] = pst[rr * RP + k];
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < RP; ++k) po[k] = 0.f;
       }
       float pacc[RP];
 #pragma unroll
@@ -817,6 +839,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
   const float* Qp = use_init ? a.qinit : Qc;
   char* wsm = p1smem + (threadIdx.x >> 5) * (St::S * St::UNIT_BYTES);
   float* red = reinterpret_cast<float*>(p1smem + 8 * St::S * St::UNIT_BYTES);
+  float* pst = reinterpret_cast<float*>(p1smem + 8 * St::S * St::UNIT_BYTES + St::RED_BYTES);
   int bad = 0;
   float chk = 0.f;
   for (int it = blockIdx.x; it < a.n_p1items; it += gridDim.x) {
@@ -824,11 +847,11 @@ __global__ void __launch_bounds__(kThreads, MINB) k_pass1_cs(const StepArgs a) {
     const TensorDesc td = a.tensors[item.t];
     const bool aligned = td.vec && a.vec_ok && (long long)(item.row0 + item.nrows) * td.m <= td.valid;
     if constexpr (KIND == 0) {
-      if (aligned) pass1_tile_cs<RP, WT, GT, MINB, 0, PW>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+      if (aligned) pass1_tile_cs<RP, WT, GT, MINB, 0, PW>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red, pst);
     } else {
       if (aligned) continue;
       if (a.vec_ok)
-        pass1_tile_cs<RP, WT, GT, MINB, 1, PW>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red);
+        pass1_tile_cs<RP, WT, GT, MINB, 1, PW>(a, td, item, Qp, Qc, Pc, cur, chk, wsm, red, pst);
       else
         pass1_tile<RP, PW ? 0 : WT, GT, 1, 1>(a, td, item, Qp, Qc, Pc, cur, bad);
     }
