@@ -275,9 +275,17 @@ size_t psgd_workspace_bytes(const psgd_state* s);
  * then returns for kernel kind `kind` (0 .. psgd_profile_kinds()-1) its name,
  * the number of launches and the summed device time since the last read, and
  * the algorithmic bytes one launch must move (the roofline numerator); it
- * then clears that kind's record.
+ * then clears that kind's record.  With launches and total_ms both NULL it
+ * returns the name and bytes only and leaves the record.
  */
 int psgd_profile(psgd_state* s, int32_t enable);
+/*
+ * psgd_profile_select -- as psgd_profile, for the kinds whose bit is set in
+ * kind_mask only (bit k: kind k; 0 stops): a timed region that needs one
+ * kernel's duration then carries two events per step, not two per kernel.
+ * Returns PSGD_EINVAL for a NULL state.
+ */
+int psgd_profile_select(psgd_state* s, uint32_t kind_mask);
 int32_t psgd_profile_kinds(void);
 int psgd_profile_read(psgd_state* s, int32_t kind, const char** name, int64_t* launches,
                       double* total_ms, double* bytes_per_launch);

@@ -190,6 +190,7 @@ struct psgd_state {
   float* tmat2 = nullptr;   // fused Gram-Schmidt stage: second sweep's transforms
   int* gs_cnt = nullptr;    // fused Gram-Schmidt stage: per-tensor partial counters
   unsigned int* gs_bar = nullptr;   // its cooperative launch: the grid barrier's counter
+  int* p3_cnt = nullptr;    // ranks <= 8: pass 3's finished CTAs (the last commits the step)
   int gs_coop = 1;          // the fused stage as one cooperative launch (0 after a refusal)
   float2* gram = nullptr;   // per Gram-Schmidt item RP x RP double-float partials
   float2* gram_t = nullptr; // per tensor RP x RP summed Gram matrix (double-float)
@@ -236,6 +237,7 @@ struct psgd_state {
   int sms = 148;
   // profiling
   bool prof = false;
+  uint32_t prof_mask = 0xffffffffu;   // kinds recorded while prof (psgd_profile_select)
   std::vector<std::vector<EventPair>> ev;
   std::vector<EventPair> ev_pool;
   double kind_bytes[K_COUNT] = {0};
@@ -268,8 +270,11 @@ int dupload(psgd_state* s, T** dst, const std::vector<T>& v) {
   return PSGD_OK;
 }
 
-void add_segments(std::vector<Segment>* segs, long long off, long long len) {
-  const long long piece = 65536;
+// piece: elements per segment (one CTA's work item).  The step's uncompressed
+// ranges are small and scattered (biases, norms): 1024-element pieces give
+// each thread one vector of every replica, so the mean costs about one load
+// latency; the vanilla phase streams the whole bucket in 64K pieces.
+void add_segments(std::vector<Segment>* segs, long long off, long long len, long long piece = 65536) {
   for (long long o = 0; o < len; o += piece) {
     Segment sg;
     sg.off = off + o;
@@ -367,7 +372,7 @@ void build_plan(psgd_state* s) {
   long long run_start = -1, run_len = 0;
   for (auto& h : s->tensors) {
     if (h.compressed) {
-      if (run_len) add_segments(&s->unc_segs, run_start, run_len);
+      if (run_len) add_segments(&s->unc_segs, run_start, run_len, 1024);
       run_start = -1;
       run_len = 0;
       TensorDesc td;
@@ -421,7 +426,7 @@ void build_plan(psgd_state* s) {
       run_len += h.numel;
     }
   }
-  if (run_len) add_segments(&s->unc_segs, run_start, run_len);
+  if (run_len) add_segments(&s->unc_segs, run_start, run_len, 1024);
   add_segments(&s->all_segs, 0, s->N);
   s->Nc_pad = c_off;
   s->Ne = e_off;
@@ -652,6 +657,8 @@ StepArgs make_args(psgd_state* s) {
   a.tmat = s->tmat;
   a.tmat2 = s->tmat2;
   a.gs_cnt = s->gs_cnt;
+  a.commit_cnt = nullptr;
+  a.status = nullptr;
   a.tensors = s->d_tensors;
   a.items = s->d_items;
   a.n_items = (int)s->items.size();
@@ -700,7 +707,7 @@ struct Launcher {
   int kind = 0;
   void begin(int k) {
     kind = k;
-    on = s->prof;
+    on = s->prof && ((s->prof_mask >> k) & 1u);
     if (!on) return;
     if (s->ev_pool.empty()) {
       EventPair p;
@@ -1167,6 +1174,8 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
   TRY(dalloc(s, (void**)&s->tmat2, std::max(1, nt) * RP * RP * sizeof(float)));
   TRY(dalloc(s, (void**)&s->gs_cnt, std::max(1, nt) * sizeof(int)));
   TRY(dalloc(s, (void**)&s->gs_bar, 16));
+  TRY(dalloc(s, (void**)&s->p3_cnt, 16));
+  TRY(zero_now(s->p3_cnt, 16));
   TRY(zero_now(s->gs_cnt, std::max(1, nt) * sizeof(int)));
   TRY(dalloc(s, (void**)&s->gram, std::max<size_t>(1, std::max(s->gsp.size(), s->gsq.size())) * RP * RP * sizeof(float2)));
   TRY(dalloc(s, (void**)&s->gram_t, std::max(1, nt) * RP * RP * sizeof(float2)));
@@ -1229,6 +1238,7 @@ namespace {
 int enqueue_step(psgd_state* s, const StepArgs& a, cudaStream_t st, bool vanilla, bool compressed_step,
                  bool need_fresh, const std::vector<int>& mask) {
   Launcher L{s, st};
+  bool committed = false;
   PSGD_CUDA_TRY(cudaMemsetAsync(&s->ctrl->flag, 0, 2 * sizeof(int), st));   // flag, timeout
   const int grid_seg = std::max(1, std::min<int>((int)s->all_segs.size(), s->sms * 4));
   if (vanilla) {
@@ -1244,11 +1254,22 @@ int enqueue_step(psgd_state* s, const StepArgs& a, cudaStream_t st, bool vanilla
                   std::max(1, std::min<int>((int)s->unc_segs.size(), s->sms * 4)), st);
       L.end();
     }
-    if (compressed_step) by_rp<RunCompressed>(s->RP, s, a, L, need_fresh, mask);
+    if (compressed_step) {
+      // ranks <= 8: pass 3 is one launch, whose last CTA commits the step
+      StepArgs c = a;
+      if (s->RP <= 8) {
+        c.commit_cnt = s->p3_cnt;
+        c.status = s->d_status;
+      }
+      by_rp<RunCompressed>(s->RP, s, c, L, need_fresh, mask);
+      committed = s->RP <= 8;
+    }
   }
-  L.begin(K_COMMIT);
-  launch_commit(s->ctrl, compressed_step ? 1 : 0, s->d_status, st);
-  L.end();
+  if (!committed) {
+    L.begin(K_COMMIT);
+    launch_commit(s->ctrl, compressed_step ? 1 : 0, s->d_status, st);
+    L.end();
+  }
   PSGD_CUDA_TRY(cudaGetLastError());
   PSGD_CUDA_TRY(cudaMemcpyAsync(s->h_status, s->d_status, sizeof(int), cudaMemcpyDeviceToHost, st));
   return PSGD_OK;
@@ -1756,6 +1777,14 @@ size_t psgd_workspace_bytes(const psgd_state* s) { return s ? s->bytes : 0; }
 int psgd_profile(psgd_state* s, int32_t enable) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
   s->prof = enable != 0;
+  s->prof_mask = 0xffffffffu;
+  return PSGD_OK;
+}
+
+int psgd_profile_select(psgd_state* s, uint32_t kind_mask) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  s->prof = kind_mask != 0;
+  s->prof_mask = kind_mask;
   return PSGD_OK;
 }
 
@@ -1765,6 +1794,11 @@ int psgd_profile_read(psgd_state* s, int32_t kind, const char** name, int64_t* l
                       double* bytes_per_launch) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
   if (kind < 0 || kind >= K_COUNT) return fail(PSGD_EINVAL, "kind out of range");
+  if (!launches && !total_ms) {   // the name and bytes only; the record stays
+    if (name) *name = kKindNames[kind];
+    if (bytes_per_launch) *bytes_per_launch = s->kind_bytes[kind];
+    return PSGD_OK;
+  }
   DeviceGuard g(s->device);
   PSGD_CUDA_TRY(cudaDeviceSynchronize());
   double ms = 0.0;

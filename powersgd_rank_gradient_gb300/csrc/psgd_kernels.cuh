@@ -65,6 +65,9 @@ struct StepArgs {
   float* tmat;        // per tensor RP x RP transform
   float* tmat2;       // fused Gram-Schmidt stage: the second sweep's transforms
   int* gs_cnt;        // fused Gram-Schmidt stage: Gram partials counted per tensor
+  int* commit_cnt;    // set: pass 3 (k_pass3, mode 0) ends the step with the commit,
+                      // in the CTA that finishes last (counted here)
+  int* status;        // the step's status word the commit writes
   const TensorDesc* tensors;
   const Item* items;         // tall (row block) x (column tile) items: pass 2
   int n_items;
@@ -1123,10 +1126,34 @@ __device__ __forceinline__ void pass3_tile(const StepArgs& a, const TensorDesc& 
   }
 }
 
+// The end-of-step commit (k_commit's work for a compressed step) done by the
+// CTA of a pass that finishes last: every other CTA has counted itself done,
+// so none still reads which half is current.  The counter is left at zero.
+__device__ __forceinline__ void commit_last(const StepArgs& a) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.commit_cnt, 1) == (int)gridDim.x - 1) {
+      __threadfence();
+      const int bad = *reinterpret_cast<volatile int*>(&a.ctrl->flag);
+      const int late = *reinterpret_cast<volatile int*>(&a.ctrl->timeout);
+      if (!bad && !late) {
+        a.ctrl->cur ^= 1;
+        a.ctrl->warm_valid = 1;
+      }
+      *a.status = late ? 2 : (bad ? 1 : 0);
+      *a.commit_cnt = 0;
+    }
+  }
+}
+
 template <int RP, int MODE>
 __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
   __shared__ __align__(16) float ps[kPStage][RP];
-  if (MODE == 0 && a.ctrl->flag) return;
+  if (MODE == 0 && a.ctrl->flag) {   // skipped step: only the commit (if asked) is left
+    if (a.commit_cnt) commit_last(a);
+    return;
+  }
   // MODE 0 reads the factors just computed (next half); the error views read
   // the committed half.
   const int half = (MODE == 0) ? (a.ctrl->cur ^ 1) : a.ctrl->cur;
@@ -1152,6 +1179,7 @@ __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
     else
       pass3_tile<RP, MODE, 1>(a, td, item, P, Q, ps, store);
   }
+  if (MODE == 0 && a.commit_cnt) commit_last(a);
 }
 
 }  // namespace psgd

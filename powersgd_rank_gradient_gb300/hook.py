@@ -174,6 +174,25 @@ class PowerSGDState:
     def profile(self, enable=True):
         check(self._lib.psgd_profile(self._h, int(enable)))
 
+    def profile_select(self, kinds):
+        """psgd_profile_select: record only the named kernel kinds (an empty
+        list stops recording)."""
+        names = self.profile_kind_names()
+        mask = 0
+        for k in kinds:
+            mask |= 1 << names.index(k)
+        check(self._lib.psgd_profile_select(self._h, mask))
+
+    def profile_kind_names(self):
+        """The kernel kinds' names, in kind order."""
+        names = []
+        for k in range(self._lib.psgd_profile_kinds()):
+            name = ctypes.c_char_p()
+            # no launches / time pointers: the name only, the record stays
+            check(self._lib.psgd_profile_read(self._h, k, ctypes.byref(name), None, None, None))
+            names.append(name.value.decode())
+        return names
+
     def profile_read(self):
         """{kind: (launches, total_ms, algorithmic bytes per launch)} since the last read."""
         res = {}

@@ -576,3 +576,30 @@ def test_graph_replay_bit_identical():
     assert graphed.graph_stats() == (3, 4), graphed.graph_stats()
     plain.close()
     graphed.close()
+
+
+def test_profile_select_records_one_kind():
+    """psgd_profile_select: only the selected kind's launches are recorded;
+    psgd_profile(1) records every kind again."""
+    from powersgd_rank_gradient_gb300 import PowerSGDState
+
+    shapes = [(700, 1100), (1100,), (256, 512)]
+    st = PowerSGDState(shapes, 2, matrix_approximation_rank=4, start_powerSGD_iter=0, device=DEV)
+    g = [torch.from_numpy(x).to(DEV) for x in grads_for(shapes, 2, 0)]
+    names = st.profile_kind_names()
+    assert "pass1" in names and "pass3" in names
+    st.step(g)
+    torch.cuda.synchronize()
+    st.profile_select(["pass1"])
+    for _ in range(3):
+        st.step(g)
+    rec = st.profile_read()
+    assert rec["pass1"][0] == 3 and rec["pass1"][1] > 0.0
+    assert all(v[0] == 0 for k, v in rec.items() if k != "pass1")
+    st.profile(True)
+    st.step(g)
+    rec = st.profile_read()
+    assert rec["pass1"][0] == 1 and rec["pass2"][0] == 1 and rec["pass3"][0] == 1
+    st.profile(False)
+    assert not st.status()
+    st.close()
