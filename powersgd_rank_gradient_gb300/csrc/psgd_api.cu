@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <string>
 #include <vector>
 
@@ -358,14 +359,52 @@ void build_plan(psgd_state* s) {
   long long c_off = 0, p_off = 0, q_off = 0, pp_off = 0, qp_off = 0, e_off = 0, i_off = 0;
   long long unc = 0;
   // pass 2: row blocks of kRowBlock rows, shorter for small buckets so that
-  // there are several items per resident CTA (one Q partial per item)
+  // there are several items per resident CTA (one Q partial per item).  When
+  // every compressed tensor has one shape the items are alike and the waves
+  // can be counted: the row block (a multiple of 64) with the shortest
+  // round-robin makespan, each item also paying its Q partial and its setup
+  // (8192 x 8192: 192 rows at ranks <= 8, 512 at rank 32, measured best; the
+  // count is used for the two kernels it was checked on, the four-column
+  // fp32 kernel of ranks <= 8 and the tensor-core kernel of rank 32)
   {
     long long nc = 0;
-    for (auto& h : s->tensors)
-      if (h.compressed) nc += h.numel;
+    bool alike = true;
+    long long n0 = -1, m0 = -1;
+    for (auto& h : s->tensors) {
+      if (!h.compressed) continue;
+      nc += h.numel;
+      if (n0 < 0) {
+        n0 = h.rows;
+        m0 = h.cols;
+      }
+      alike = alike && h.rows == n0 && h.cols == m0;
+    }
     const long long target = (long long)s->sms * 3 * 4;
     int rb = kRowBlock;
     while (rb > 64 && nc / ((long long)rb * CT) < target) rb >>= 1;
+    if (alike && n0 > 0 && (RP <= 8 || RP == 32)) {
+      const bool tc2 = RP == 32;   // 128-column items, one CTA per SM
+      const int ctw = tc2 ? 128 : CT;
+      const double bpe = s->pass2_src == 0 ? 4.0 : (s->pass2_src == 1 ? 4.0 * s->W
+                                                                        : (s->dtype == PSGD_F32 ? 4.0 : 2.0) * s->W);
+      double best = -1.0;
+      for (int r = kRowBlock; r >= 64; r -= 64) {
+        std::vector<long long> sizes;
+        for (auto& h : s->tensors) {
+          if (!h.compressed) continue;
+          for (long long r0 = 0; r0 < h.rows; r0 += r)
+            for (long long c0 = 0; c0 < h.cols; c0 += ctw)
+              sizes.push_back(std::min<long long>(r, h.rows - r0) * std::min<long long>(ctw, h.cols - c0));
+        }
+        std::stable_sort(sizes.begin(), sizes.end(), std::greater<long long>());
+        const long long G = std::min<long long>((long long)sizes.size(), (long long)s->sms * (tc2 ? 1 : 3));
+        const double t = rr_makespan(sizes, G, bpe, stall_bytes(2e-6, G) + 8.0 * RP * ctw);
+        if (best < 0 || t < best * 0.999) {
+          best = t;
+          rb = r;
+        }
+      }
+    }
     s->row_block = rb;
   }
   // uncompressed ranges, merged

@@ -575,7 +575,16 @@ __device__ __forceinline__ void gs_count_and_solve(const StepArgs& a, int it, in
   const int count = is_q ? a.gsq_count[t] : a.gsp_count[t];
   for (int e = threadIdx.x; e < ENT; e += kThreads) {
     float hi = 0.f, lo = 0.f;
-    for (int i = 0; i < count; ++i) {
+    // in item order, eight loads in flight
+    int i = 0;
+    for (; i + 8 <= count; i += 8) {
+      float2 x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = __ldcg(a.gram + (long long)(first + i + u) * ENT + e);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) df_add(hi, lo, x[u].x, x[u].y);
+    }
+    for (; i < count; ++i) {
       const float2 x = __ldcg(a.gram + (long long)(first + i) * ENT + e);
       df_add(hi, lo, x.x, x.y);
     }
