@@ -574,15 +574,6 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       if (a.ef) load_qcols<RP, 4, !SH>(Qc + td.q_off, m, c, qc, ncv);
       if (!(a.ef && same_q)) load_qcols<RP, 4, !SH>(Qp + td.q_off, m, c, qp, ncv);
     }
-    // the same values as column pairs (0, 1) and (2, 3) for fma.rn.f32x2
-    uint64_t qc2[2][RP], qp2[2][RP];
-#pragma unroll
-    for (int k = 0; k < RP; ++k) {
-      qc2[0][k] = f2pack(qc[0][k], qc[1][k]);
-      qc2[1][k] = f2pack(qc[2][k], qc[3][k]);
-      qp2[0][k] = f2pack(qp[0][k], qp[1][k]);
-      qp2[1][k] = f2pack(qp[2][k], qp[3][k]);
-    }
     // units are issued and consumed in order, wpc rows apart, the issued one
     // S - 1 units ahead of the consumed one: running offsets of the consumed
     // unit (bucket position, store offset) and rotating stage slots replace
@@ -683,6 +674,17 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
       const long long r = row_first + (long long)u * wpc;
       if (u < units) issue(wsm + u * St::UNIT_BYTES, td.g_off + r * m + c, ecur + td.c_off + r * ld + c);
       else cp_async_commit();
+    }
+    // Q's columns (loaded above, before the copies were issued) as column
+    // pairs (0, 1) and (2, 3) for fma.rn.f32x2: packed only now, so that
+    // their loads' latency overlaps the copies in flight
+    uint64_t qc2[2][RP], qp2[2][RP];
+#pragma unroll
+    for (int k = 0; k < RP; ++k) {
+      qc2[0][k] = f2pack(qc[0][k], qc[1][k]);
+      qc2[1][k] = f2pack(qc[2][k], qc[3][k]);
+      qp2[0][k] = f2pack(qp[0][k], qp[1][k]);
+      qp2[1][k] = f2pack(qp[2][k], qp[3][k]);
     }
     cp_async_wait<S - 1>();   // this thread's P pieces have landed (the units may not)
     __syncthreads();          // and every thread's
