@@ -842,9 +842,9 @@ struct Ops {
     if (is_q)
       launch_apply<RP>(a, s->pgs, s->qinit, 1, -1, grid, L.st);
     else
-      launch_apply<RP>(a, s->pgs, s->Pf, 0, 1, grid, L.st);
+      launch_apply<RP>(a, s->pgs, s->Pf, 0, 1, grid, L.st, nullptr, RP >= 16 ? 1 : 0);   // with P's images
     L.end();
-    return false;
+    return RP >= 16 && !is_q;
   }
 
   // ranks 16 and 32: the factor images the tensor-core passes read
@@ -872,7 +872,9 @@ struct Ops {
       L.end();
       gs(s, a, L, 1);
     }
-    images(s, a, L, 2);
+    // Q's chunk image (pass 1's projection operand): the last committed step
+    // (or set_q) wrote it for a warm Q, so only a fresh draw needs it here
+    if (need_fresh || !s->warm) images(s, a, L, 2);
     L.begin(K_PASS1);
     launch_pass1<RP>(a, grid_p1, L.st);
     L.end();
@@ -903,7 +905,9 @@ struct Ops {
       L.end();
       gs(s, a, L, 1);
     }
-    images(s, a, L, 2);
+    // Q's chunk image (pass 1's projection operand): the last committed step
+    // (or set_q) wrote it for a warm Q, so only a fresh draw needs it here
+    if (need_fresh || !s->warm) images(s, a, L, 2);
     L.begin(K_PASS1);
     launch_pass1<RP>(a, grid_p1, L.st);
     L.end();
@@ -1672,7 +1676,17 @@ int psgd_step_status(psgd_state* s, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");
   DeviceGuard g(s->device);
   PSGD_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
-  if (*s->h_status == 2) return fail(PSGD_ETIMEOUT, "a bounded device-side wait gave up; the step was not committed");
+  if (*s->h_status == 2) {
+    if (s->img) {
+      // a kernel may have written the operand images of factors that were not
+      // committed: rebuild them from the committed half before the next step
+      StepArgs a = make_args(s);
+      Launcher L{s, (cudaStream_t)stream};
+      by_rp<RunImages>(s->RP, s, a, L, 3);
+      PSGD_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+    }
+    return fail(PSGD_ETIMEOUT, "a bounded device-side wait gave up; the step was not committed");
+  }
   return *s->h_status ? PSGD_SKIPPED_NONFINITE : PSGD_OK;
 }
 

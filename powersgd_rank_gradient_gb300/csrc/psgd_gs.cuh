@@ -74,10 +74,12 @@ __global__ void __launch_bounds__(kThreads) k_psum(const StepArgs a) {
 // q summing (in row-block order) the q-th quarter of the row blocks, and the
 // quarters are added in order (((s0 + s1) + s2) + s3): a quarter of the
 // dependent loads of one chain per value, eight of them in flight.
-// img (ranks 16 and 32): also write Q's row image, as k_images mode 1 does.
+// img (ranks 16 and 32): also write Q's row and chunk images, as k_images
+// mode 1 does.
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a, int img) {
   if (a.ctrl->flag) return;
+  if (img && a.ctrl->timeout) return;   // not committed: the images keep the committed Q
   float* Q = a.qx ? a.qx : a.Qf + (long long)(a.ctrl->cur ^ 1) * a.q_total;
   const int q = threadIdx.x & 3;
   for (int it = blockIdx.x; it < a.n_qr; it += gridDim.x) {
@@ -127,7 +129,10 @@ __global__ void __launch_bounds__(kThreads) k_qreduce(const StepArgs a, int img)
         const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (e < ne) img_put_q<RP>(a, td, (f + e) % td.m, (f + e) / td.m, tv[e], false);
+          if (e < ne) {
+            img_put_q<RP>(a, td, (f + e) % td.m, (f + e) / td.m, tv[e], false);
+            img_put_q<RP>(a, td, (f + e) % td.m, (f + e) / td.m, tv[e], true);
+          }
       }
     }
     if (len % 4 == 0) {
@@ -532,18 +537,24 @@ __device__ __forceinline__ void apply_item(const StepArgs& a, int it, const floa
 }
 
 // dst_half >= 0: write into half (cur ^ 1) of Pf/Qf (dst is the base).
-// tsrc: the transforms (a.tmat when NULL).
+// tsrc: the transforms (a.tmat when NULL).  img (P, ranks 16 and 32): also
+// write P's operand images (k_images mode 0).
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_apply(const StepArgs a, const float* __restrict__ src,
                                                     float* __restrict__ dst, int is_q, int dst_half,
-                                                    const float* __restrict__ tsrc) {
+                                                    const float* __restrict__ tsrc, int img) {
   __shared__ __align__(16) float T[RP * RP];
   const int n_items = is_q ? a.n_gsq : a.n_gsp;
   if (a.ctrl->flag) return;
   long long half_off = 0;
   if (dst_half >= 0) half_off = (long long)(a.ctrl->cur ^ 1) * (is_q ? a.q_total : a.p_total);
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x)
-    apply_item<RP>(a, it, src, dst, is_q, half_off, tsrc ? tsrc : a.tmat, T);
+  if (img && a.ctrl->timeout) img = 0;   // not committed: keep the images
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    if (RP >= 16 && img)
+      apply_item<RP, true>(a, it, src, dst, is_q, half_off, tsrc ? tsrc : a.tmat, T);
+    else
+      apply_item<RP>(a, it, src, dst, is_q, half_off, tsrc ? tsrc : a.tmat, T);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -697,6 +708,7 @@ __global__ void __launch_bounds__(kThreads) k_gs_coop(const StepArgs a, const fl
   if (!grid_barrier(a, bar, ++nb * gridDim.x, &ok_s)) return;
   long long half_off = 0;
   if (dst_half >= 0) half_off = (long long)(a.ctrl->cur ^ 1) * (is_q ? a.q_total : a.p_total);
+  if (img && *reinterpret_cast<volatile int*>(&a.ctrl->timeout)) img = 0;   // not committed: keep the images
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     if (RP >= 16 && img)
       apply_item<RP, true>(a, it, mid, dst, is_q, half_off, a.tmat2, T);

@@ -15,8 +15,10 @@ template <int RP> void launch_gram(const StepArgs& a, const float* src, float* d
                                    int from_parts, float2* gram, int grid, cudaStream_t s);
 template <int RP> void launch_gram_sum(const StepArgs& a, int is_q, cudaStream_t s);
 template <int RP> void launch_solve(const StepArgs& a, const float2* gram, int is_q, int sweep, cudaStream_t s);
+// img: ranks 16 and 32, P's operand images written too (k_images mode 0)
 template <int RP> void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q,
-                                    int dst_half, int grid, cudaStream_t s, const float* tsrc = nullptr);
+                                    int dst_half, int grid, cudaStream_t s, const float* tsrc = nullptr,
+                                    int img = 0);
 template <int RP> void launch_gs_first(const StepArgs& a, const float* src, float* dense_out, int is_q,
                                        int from_parts, int grid, cudaStream_t s);
 template <int RP> void launch_gs_second(const StepArgs& a, const float* src, float* mid, int is_q, int grid,

@@ -106,8 +106,8 @@ void launch_solve(const StepArgs& a, const float2* gram, int is_q, int sweep, cu
 
 template <int RP>
 void launch_apply(const StepArgs& a, const float* src, float* dst, int is_q, int dst_half, int grid,
-                  cudaStream_t s, const float* tsrc) {
-  k_apply<RP><<<grid, kThreads, 0, s>>>(a, src, dst, is_q, dst_half, tsrc);
+                  cudaStream_t s, const float* tsrc, int img) {
+  k_apply<RP><<<grid, kThreads, 0, s>>>(a, src, dst, is_q, dst_half, tsrc, img);
 }
 
 template <int RP>
@@ -242,7 +242,7 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
   template void launch_gram_sum<RPV>(const StepArgs&, int, cudaStream_t);                      \
   template void launch_solve<RPV>(const StepArgs&, const float2*, int, int, cudaStream_t);      \
   template void launch_apply<RPV>(const StepArgs&, const float*, float*, int, int, int,         \
-                                  cudaStream_t, const float*);                                  \
+                                  cudaStream_t, const float*, int);                             \
   template void launch_gs_first<RPV>(const StepArgs&, const float*, float*, int, int, int,      \
                                      cudaStream_t);                                             \
   template cudaError_t launch_gs_coop<RPV>(const StepArgs&, const float*, float*, int, int, float*, float*, \

@@ -268,16 +268,20 @@ __device__ __forceinline__ void img_put_q(const StepArgs& a, const TensorDesc& t
 //     P's chunk image is the B operand of pass 2 (K = the tensor's rows);
 //     Q's the B operand of pass 1's projection (K = the tensor's columns).
 // mode 0: P row and chunk images from the factors just orthogonalised (next
-//         half); mode 1: Q row image from the next half's Q; mode 2: Q chunk
-//         image from the projection Q of this step (the fresh orthogonalised
-//         draw or the warm Q, decided on the device as pass 1 decides it);
-//         mode 3: P and Q row images from the committed half (after the
-//         factors were replaced on the host).  Modes 0 and 1 do nothing in a
-//         skipped step, so the images keep describing the committed factors.
+//         half); mode 1: Q row and chunk images from the next half's Q (the
+//         chunk image is the next step's projection operand when that step
+//         is warm-started); mode 2: Q chunk image from the projection Q of
+//         this step (the fresh orthogonalised draw or the warm Q, decided on
+//         the device as pass 1 decides it; launched only when a fresh draw
+//         can be the projection Q); mode 3: P row image and Q row and chunk
+//         images from the committed half (after the factors were replaced on
+//         the host).  Modes 0 and 1 do nothing in a skipped step, so the
+//         images keep describing the committed factors.
 // ---------------------------------------------------------------------------
 template <int RP>
 __global__ void __launch_bounds__(kThreads) k_images(const StepArgs a, int mode) {
-  if ((mode == 0 || mode == 1) && a.ctrl->flag) return;
+  // a skipped or timed-out step keeps the committed factors, and the images too
+  if ((mode == 0 || mode == 1) && (a.ctrl->flag || a.ctrl->timeout)) return;
   const int cur = a.ctrl->cur;
   const int half = (mode == 3) ? cur : (cur ^ 1);
   const bool do_p = (mode == 0 || mode == 3);
@@ -306,10 +310,12 @@ __global__ void __launch_bounds__(kThreads) k_images(const StepArgs a, int mode)
       }
       // chunk images: for chunk r / 32, RP rows of hi then RP rows of lo (one
       // stacked operand)
-      if (is_p)
+      if (is_p) {
         img_put_p<RP>(a, td, r, k, x, mode == 0);
-      else
-        img_put_q<RP>(a, td, r, k, x, mode == 2);
+      } else {
+        if (mode != 2) img_put_q<RP>(a, td, r, k, x, false);
+        img_put_q<RP>(a, td, r, k, x, true);
+      }
     }
   }
 }
