@@ -1298,14 +1298,16 @@ int enqueue_step(psgd_state* s, const StepArgs& a, cudaStream_t st, bool vanilla
       L.end();
     }
     if (compressed_step) {
-      // ranks <= 8: pass 3 is one launch, whose last CTA commits the step
+      // pass 3 as one launch (ranks <= 8; at ranks 16 and 32 when the
+      // tensor-core kernel covers every tensor): its last CTA commits the step
       StepArgs c = a;
-      if (s->RP <= 8) {
+      const bool one_pass3 = s->RP <= 8 || (!s->t3items.empty() && !s->any_unaligned);
+      if (one_pass3) {
         c.commit_cnt = s->p3_cnt;
         c.status = s->d_status;
       }
       by_rp<RunCompressed>(s->RP, s, c, L, need_fresh, mask);
-      committed = s->RP <= 8;
+      committed = one_pass3;
     }
   }
   if (!committed) {

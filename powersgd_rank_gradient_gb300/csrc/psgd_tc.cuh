@@ -364,10 +364,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 template <int RP>
 __global__ void __launch_bounds__(288, 1) k_pass3_tc(const StepArgs a) {
   using T = Pass3Tc<RP>;
-  if (a.ctrl->flag) return;
+  // a.commit_cnt set (this kernel is the step's only pass-3 launch): the CTA
+  // that finishes last commits the step, whichever way it leaves
+  if (a.ctrl->flag) {
+    if (a.commit_cnt) commit_last(a);
+    return;
+  }
   const int per = (a.n_t3 + gridDim.x - 1) / gridDim.x;
   const int first = blockIdx.x * per, last = min(a.n_t3, first + per);
-  if (first >= last) return;
+  if (first >= last) {
+    if (a.commit_cnt) commit_last(a);
+    return;
+  }
   extern __shared__ unsigned char p3_dsm[];
   __shared__ __align__(8) uint64_t bfull[2], bfree[2], tfull[2], tfree[2], afull, drain;
   __shared__ uint32_t tslot;
@@ -523,6 +531,7 @@ __global__ void __launch_bounds__(288, 1) k_pass3_tc(const StepArgs a) {
   __syncthreads();
   tc::fence_after();
   if (warp == 0) tc::tmem_free(tmem, T::TCOLS);
+  if (a.commit_cnt) commit_last(a);
 }
 
 // ---------------------------------------------------------------------------
