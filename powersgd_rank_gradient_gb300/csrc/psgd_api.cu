@@ -193,6 +193,7 @@ struct psgd_state {
   unsigned int* gs_bar = nullptr;   // its cooperative launch: the grid barrier's counter
   int* p3_cnt = nullptr;    // ranks <= 8: pass 3's finished CTAs (the last commits the step)
   int gs_coop = 1;          // the fused stage as one cooperative launch (0 after a refusal)
+  unsigned int test_wait_skew = 0;   // tests: the next cooperative stage's first barrier never completes
   float2* gram = nullptr;   // per Gram-Schmidt item RP x RP double-float partials
   float2* gram_t = nullptr; // per tensor RP x RP summed Gram matrix (double-float)
   Ctrl* ctrl = nullptr;
@@ -783,7 +784,8 @@ struct Ops {
       const cudaError_t e = launch_gs_coop<RP>(
           a, parts ? s->praw_part : src_dense, parts ? s->praw : nullptr, is_q, parts ? 1 : 0, s->pgs,
           is_q ? s->qinit : s->Pf, is_q ? -1 : 1, psum ? 1 : 0, s->gs_bar, (RP >= 16 && !is_q) ? 1 : 0,
-          std::max(grid, psum ? std::min(a.n_ps, s->sms * 4) : 1), L.st);
+          std::max(grid, psum ? std::min(a.n_ps, s->sms * 4) : 1), L.st, s->test_wait_skew);
+      s->test_wait_skew = 0;
       L.end();
       if (e == cudaSuccess) return RP >= 16 && !is_q;
       // refused (no cooperative launch here): the three-launch stage from now on
@@ -1673,6 +1675,18 @@ int psgd_internal_set_tensor_base(psgd_state* s, int32_t base) {
 }
 
 int psgd_internal_compressed_count(const psgd_state* s) { return s ? (int)s->cdesc.size() : 0; }
+
+// Tests of the bounded waits: the next cooperative Gram-Schmidt launch's first
+// grid barrier waits for one arrival more than the launch has CTAs (a count
+// nothing completes), so every CTA gives up after its bounded polls and the
+// step reports PSGD_ETIMEOUT.  Only states on the cooperative stage (small
+// buckets, ranks up to 16) have that launch; returns PSGD_EINVAL otherwise.
+int psgd_internal_force_wait_timeout(psgd_state* s) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (!s->gs_fused || !s->gs_coop) return fail(PSGD_EINVAL, "the state has no cooperative stage");
+  s->test_wait_skew = 1;
+  return PSGD_OK;
+}
 
 int psgd_step_status(psgd_state* s, void* stream) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");

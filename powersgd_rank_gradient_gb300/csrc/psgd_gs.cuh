@@ -681,23 +681,27 @@ template <int RP>
 __global__ void __launch_bounds__(kThreads) k_gs_coop(const StepArgs a, const float* __restrict__ src,
                                                       float* __restrict__ dense_out, int is_q, int from_parts,
                                                       float* __restrict__ mid, float* __restrict__ dst,
-                                                      int dst_half, int do_psum, unsigned int* bar, int img) {
+                                                      int dst_half, int do_psum, unsigned int* bar, int img,
+                                                      unsigned int skew) {
   __shared__ float tile[kGramTile][RP + 1];
   __shared__ float2 red[kThreads];
   __shared__ __align__(16) float T[RP * RP];
   __shared__ int last_s, ok_s;
   const int n_items = is_q ? a.n_gsq : a.n_gsp;
   if (a.ctrl->flag) return;   // the same for every CTA: none waits at a barrier
-  unsigned int nb = 0;
+  // skew (tests of the bounded wait): the first barrier waits for skew more
+  // arrivals than there are CTAs, so every CTA gives up and reports a timeout
+  unsigned int nb = 0, extra = skew;
   if (do_psum) {
     for (int it = blockIdx.x; it < a.n_ps; it += gridDim.x) psum_item<RP>(a, it);
-    if (!grid_barrier(a, bar, ++nb * gridDim.x, &ok_s)) return;
+    if (!grid_barrier(a, bar, ++nb * gridDim.x + extra, &ok_s)) return;
+    extra = 0;
   }
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     gram_item<RP>(a, it, src, dense_out, is_q, from_parts, a.gram, tile, red);
     gs_count_and_solve<RP>(a, it, is_q, 0, a.tmat, &last_s);
   }
-  if (!grid_barrier(a, bar, ++nb * gridDim.x, &ok_s)) return;
+  if (!grid_barrier(a, bar, ++nb * gridDim.x + extra, &ok_s)) return;
   const float* x = dense_out ? dense_out : src;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     apply_item<RP>(a, it, x, mid, is_q, 0, a.tmat, T);

@@ -25,7 +25,8 @@ template <int RP> void launch_gs_second(const StepArgs& a, const float* src, flo
                                         cudaStream_t s);
 template <int RP> cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out, int is_q,
                                               int from_parts, float* mid, float* dst, int dst_half, int do_psum,
-                                              unsigned int* bar, int img, int grid, cudaStream_t s);
+                                              unsigned int* bar, int img, int grid, cudaStream_t s,
+                                              unsigned int skew = 0);
 template <int RP> void launch_pass2(const StepArgs& a, int src_mode, int grid, cudaStream_t s);
 // img: ranks 16 and 32, also write Q's row image (k_images mode 1)
 template <int RP> void launch_qreduce(const StepArgs& a, int grid, cudaStream_t s, int img = 0);

@@ -127,7 +127,7 @@ void launch_gs_second(const StepArgs& a, const float* src, float* mid, int is_q,
 template <int RP>
 cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts,
                            float* mid, float* dst, int dst_half, int do_psum, unsigned int* bar, int img,
-                           int grid, cudaStream_t s) {
+                           int grid, cudaStream_t s, unsigned int skew) {
   static int fit = -1;
   if (fit < 0) {
     int dev = 0, sms = 0, per_sm = 0;
@@ -141,7 +141,7 @@ cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out
   cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<StepArgs*>(&a), &src, &dense_out, &is_q, &from_parts, &mid, &dst, &dst_half,
-                  &do_psum, &bar, &img};
+                  &do_psum, &bar, &img, &skew};
   return cudaLaunchCooperativeKernel((const void*)k_gs_coop<RP>, dim3(grid), dim3(kThreads), args, 0, s);
 }
 
@@ -246,7 +246,8 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
   template void launch_gs_first<RPV>(const StepArgs&, const float*, float*, int, int, int,      \
                                      cudaStream_t);                                             \
   template cudaError_t launch_gs_coop<RPV>(const StepArgs&, const float*, float*, int, int, float*, float*, \
-                                            int, int, unsigned int*, int, int, cudaStream_t);           \
+                                            int, int, unsigned int*, int, int, cudaStream_t,            \
+                                            unsigned int);                                              \
   template void launch_gs_second<RPV>(const StepArgs&, const float*, float*, int, int,          \
                                       cudaStream_t);                                            \
   template void launch_pass2<RPV>(const StepArgs&, int, int, cudaStream_t);                     \

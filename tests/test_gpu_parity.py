@@ -603,3 +603,50 @@ def test_profile_select_records_one_kind():
     st.profile(False)
     assert not st.status()
     st.close()
+
+
+@pytest.mark.parametrize("rank", [4, 16])
+def test_bounded_wait_timeout_leaves_state_unchanged(rank):
+    """A grid barrier of the cooperative Gram-Schmidt stage that can never
+    complete (it waits for one arrival more than the launch has CTAs): every
+    CTA gives up after its bounded polls, the step reports PSGD_ETIMEOUT and
+    is not committed, the GPU stays usable, and the next steps equal, bit for
+    bit, those of a state that never saw the failed step (at rank 16 the
+    tensor-core operand images are rebuilt from the committed factors)."""
+    import ctypes
+
+    from powersgd_rank_gradient_gb300 import PowerSGDState, _lib
+
+    world = 2
+    make = lambda: PowerSGDState(ALIGNED, world, matrix_approximation_rank=rank, start_powerSGD_iter=0,
+                                 min_compression_rate=0.25, device=DEV)
+    a, b = make(), make()
+    dev = lambda k: [torch.from_numpy(x).to(DEV) for x in grads_for(ALIGNED, world, k)]
+    for st in (a, b):
+        st.step(dev(0))
+        assert not st.status()
+    nt = [t for t in range(len(ALIGNED)) if len(ALIGNED[t]) > 1]
+    snap = lambda st: ([st.get_q(t).clone() for t in nt], [st.get_p(t).clone() for t in nt],
+                       [st.get_error(w).cpu().clone() for w in range(world)])
+    before = snap(a)
+    L = _lib.lib()
+    L.psgd_internal_force_wait_timeout.argtypes = [ctypes.c_void_p]
+    L.psgd_internal_force_wait_timeout.restype = ctypes.c_int
+    assert L.psgd_internal_force_wait_timeout(a._h) == 0
+    a.step(dev(1))
+    with pytest.raises(_lib.PsgdError) as err:
+        a.status()
+    assert err.value.code == _lib.PSGD_ETIMEOUT
+    after = snap(a)
+    for xs, ys in zip(before, after):
+        for x, y in zip(xs, ys):
+            assert torch.equal(x, y)
+    for k in (2, 3):
+        oa, ob = a.step(dev(k)), b.step(dev(k))
+        assert not a.status() and not b.status()
+        assert torch.equal(oa, ob)
+    for xs, ys in zip(snap(a), snap(b)):
+        for x, y in zip(xs, ys):
+            assert torch.equal(x, y)
+    a.close()
+    b.close()
