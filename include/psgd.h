@@ -200,8 +200,10 @@ int psgd_graph_stats(const psgd_state* s, int64_t* captures, int64_t* replays);
 /*
  * psgd_step_status -- synchronises `stream` and returns the outcome of the
  * last step enqueued: PSGD_OK, PSGD_SKIPPED_NONFINITE, PSGD_ETIMEOUT (a
- * bounded wait inside a tensor-core kernel gave up; the step was not
- * committed and the state is as before it), or PSGD_ECUDA.
+ * bounded wait inside a tensor-core kernel or at a grid barrier of the
+ * cooperative Gram-Schmidt stage gave up; the step was not committed and the
+ * state is as before it -- the call rebuilds the tensor-core operand images
+ * of the committed factors, on `stream`, before returning), or PSGD_ECUDA.
  */
 int psgd_step_status(psgd_state* s, void* stream);
 
