@@ -344,6 +344,9 @@ typedef struct psgd_group psgd_group; /* opaque, library-owned */
  * tensors, and dims/ndims list every tensor of every bucket in bucket order,
  * as psgd_state_create takes them for one bucket.  The other arguments are
  * psgd_state_create's and apply to every bucket; n_streams in [1, 16].
+ * More than 8 streams overlap fully only when the process starts CUDA with
+ * as many hardware work queues (CUDA_DEVICE_MAX_CONNECTIONS >= n_streams;
+ * CUDA's default is 8) or replays the steps as graphs (psgd_set_graph).
  * Allocates every bucket's state and the streams on `device`.
  * Errors: PSGD_EINVAL, PSGD_ENOMEM, PSGD_ECUDA (nothing is left allocated).
  */
