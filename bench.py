@@ -415,6 +415,10 @@ def run_native(spec, args, dist, rank_id, world, device, light=False):
     if not light:
         res["rows"] = run_rows(spec, args, dist, device, sets, out, W, N)
         res["rows"]["steady_step_graph"] = run_graph(st, spec, args, dist, device, sets[0], out, W, N)
+        try:
+            res["rows"]["dp_split_one_process"] = run_dp(spec, args, dist, device, sets[0][0], out, N)
+        except Exception as e:   # a row, not the headline: report it and go on
+            res["rows"]["dp_split_one_process"] = {"error": str(e)}
         if args.batched:
             res["rows"]["next_batched_hook"] = run_batched(spec, args, dist, device, sets, out, W, N)
         if args.buckets > 0:
@@ -457,6 +461,49 @@ def run_graph(st, spec, args, dist, device, grads, out, W, N):
     res["graph_gradient_gbs"] = W * N * GSIZE[spec["dtype"]] / (res["graph_ms_per_step"] / 1e3) / 1e9
     res["graph_captures"] = caps
     res["graph_replays"] = reps
+    return res
+
+
+def run_dp(spec, args, dist, device, grad, out, N):
+    """The data-parallel split (one replica per process: begin, project,
+    finish) in a one-process world, where its two exchanges are identities,
+    against the fused step of a one-replica state on the same bucket: what the
+    split costs a process besides its collectives."""
+    import torch
+
+    from powersgd_rank_gradient_gb300 import DataParallelPowerSGDState, PowerSGDState
+
+    stream = torch.cuda.current_stream(device)
+    inv_scale = 1.0 / spec["loss_scale"]
+    kw = dict(matrix_approximation_rank=spec["rank"], start_powerSGD_iter=0, min_compression_rate=spec["mcr"],
+              batch_tensors_with_same_shape=spec["batch_same_shape"], grad_dtype=torch_dtype(spec), device=device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    res = {"replicas_per_process": 1}
+    dp = DataParallelPowerSGDState(spec["shapes"], world_size=1, **kw)
+
+    def dp_step():
+        dp.begin(grad, out, inv_scale)
+        dp.project()
+        dp.finish()
+
+    fused = PowerSGDState(spec["shapes"], 1, **kw)
+    for label, fn in (("split_ms_per_step", dp_step),
+                      ("fused_ms_per_step", lambda: fused.step([grad], out=out, inv_loss_scale=inv_scale))):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        res[label] = reduce_max(e0.elapsed_time(e1), dist, device) / args.steps
+    if fused.status():
+        raise RuntimeError("one-replica step was skipped (non-finite input)")
+    res["split_gradient_gbs"] = N * GSIZE[spec["dtype"]] / (res["split_ms_per_step"] / 1e3) / 1e9
+    dp.close()
+    fused.close()
     return res
 
 
