@@ -99,7 +99,9 @@ int psgd_plan(const int64_t* dims, const int32_t* ndims, int32_t n_tensors,
  * the initial standard-normal Q when none was injected with psgd_set_q.
  * Errors: PSGD_EINVAL (rank outside [1,32], world_size outside [1,64],
  * negative dims, start_powerSGD_iter < 0, min_compression_rate < 0 or NaN,
- * epsilon < 0), PSGD_ENOMEM, PSGD_ECUDA.  *out is NULL on failure.
+ * epsilon < 0, device ordinal 64 or above), PSGD_ENOMEM, PSGD_ECUDA (no such
+ * device).  *out is NULL on failure.  Every creator takes the same device
+ * rule; states on several devices may live in one process.
  */
 int psgd_state_create(const int64_t* dims, const int32_t* ndims, int32_t n_tensors,
                       int32_t world_size, int32_t matrix_approximation_rank,

@@ -1124,6 +1124,10 @@ int create_common(psgd_state* s, int32_t world_size, int32_t rank, int64_t start
     delete s;
     return fail(PSGD_ECUDA, "no such CUDA device");
   }
+  if (device >= 64) {   // per-device launch settings are kept for ordinals 0-63
+    delete s;
+    return fail(PSGD_EINVAL, "device ordinals from 64 up are not supported");
+  }
   DeviceGuard g(device);
   s->device = device;
   s->W = world_size;

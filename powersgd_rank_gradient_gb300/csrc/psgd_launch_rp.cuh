@@ -23,15 +23,26 @@ inline void by_gtype(int gtype, F&& f) {
     f(0.0f);
 }
 
+// cudaFuncSetAttribute applies to the current device's context: a launcher
+// that raises a kernel's shared-memory limit does so once per device.  `done`
+// holds one bit per device ordinal (the library handles ordinals below 64).
+inline bool first_on_device(unsigned long long& done) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done & bit) return false;
+  done |= bit;
+  return true;
+}
+
 template <int RP, typename GT>
 void launch_pass1_mma(const StepArgs& a, int grid, cudaStream_t s) {
   // the aligned, wholly backed items on the tensor cores (tcgen05), the rest
   // on the element kernel
   using T = Pass1Tc<RP, GT>;
-  static bool configured = false;
-  if (!configured) {
+  static unsigned long long configured = 0;
+  if (first_on_device(configured)) {
     cudaFuncSetAttribute(k_pass1_tc<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-    configured = true;
   }
   if (a.vec_ok && a.n_t1 > 0) k_pass1_tc<RP, GT><<<std::min(grid, a.n_t1), T::THREADS, T::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned) k_pass1_rest<RP, GT><<<grid * 2, kThreads, 0, s>>>(a);
@@ -42,13 +53,12 @@ template <int RP, int WT, typename GT, int MINB, bool PW = false>
 void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
   using St0 = Pass1CS<RP, WT, GT, MINB, false>;
   using St1 = Pass1CS<RP, WT, GT, MINB, true>;
-  static bool configured = false;
-  if (!configured) {
+  static unsigned long long configured = 0;
+  if (first_on_device(configured)) {
     cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 0, PW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          St0::SMEM);
     cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 1, PW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          St1::SMEM);
-    configured = true;
   }
   if (a.vec_ok && a.has_aligned) k_pass1_cs<RP, WT, GT, MINB, 0, PW><<<grid * MINB, kThreads, St0::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned)
@@ -128,10 +138,12 @@ template <int RP>
 cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts,
                            float* mid, float* dst, int dst_half, int do_psum, unsigned int* bar, int img,
                            int grid, cudaStream_t s, unsigned int skew) {
-  static int fit = -1;
-  if (fit < 0) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
+  static int fits[64];   // CTAs resident at once, per device ordinal (0: not known yet)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& fit = fits[dev & 63];
+  if (fit <= 0) {
+    int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gs_coop<RP>, kThreads, 0);
     fit = std::max(0, per_sm * sms);
@@ -148,10 +160,9 @@ cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out
 template <int RP, int NSRC>
 void launch_pass2_tc(const StepArgs& a, int src_mode, cudaStream_t s) {
   using T = Pass2Tc<RP, NSRC>;
-  static bool configured = false;
-  if (!configured) {
+  static unsigned long long configured = 0;
+  if (first_on_device(configured)) {
     cudaFuncSetAttribute(k_pass2_tc<RP, NSRC>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-    configured = true;
   }
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -212,10 +223,9 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
     // fp32 kernel below skips them and takes the rest
     if (mode == 0 && a.vec_ok && a.n_t3 > 0) {
       using T = Pass3Tc<RP>;
-      static bool configured = false;
-      if (!configured) {
+      static unsigned long long configured = 0;
+      if (first_on_device(configured)) {
         cudaFuncSetAttribute(k_pass3_tc<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-        configured = true;
       }
       int dev = 0, sms = 148;
       cudaGetDevice(&dev);
