@@ -273,6 +273,23 @@ int psgd_set_error(psgd_state* s, int32_t replica, const float* dev_in, void* st
 size_t psgd_workspace_bytes(const psgd_state* s);
 
 /*
+ * psgd_set_error_store_halves -- keep the error-feedback store once (1) or
+ * twice (2, the default).  The pages put error feedback's memory at the size
+ * of the model's gradients ([DDP] "PowerSGD Hooks", the warning on error
+ * feedback): one half is that, W x (compressed elements) floats per state.
+ * With one half, pass 1 writes each step's M_w over the residual it has just
+ * read, so the results are the same bits; but a step that meets an inf/NaN
+ * has by then overwritten the store with that step's M_w, so its skip leaves
+ * the factors as they were and the error feedback changed (reset it with
+ * psgd_set_error, or keep two halves when gradients can be non-finite, as
+ * with a GradScaler).  Must precede the first psgd_step (reallocates the
+ * store, zeroed).  Errors: PSGD_EINVAL (NULL state, halves not 1 or 2, a step
+ * already taken, a data-parallel state), PSGD_ENOMEM, PSGD_ECUDA.  A state
+ * without error feedback has no store: the call then only returns PSGD_OK.
+ */
+int psgd_set_error_store_halves(psgd_state* s, int32_t halves);
+
+/*
  * Kernel timing for measurement.  psgd_profile(s, 1) makes later psgd_step
  * calls record a CUDA event pair around every kernel they launch (on the
  * step's stream); 0 stops it.  psgd_profile_read synchronises the device,

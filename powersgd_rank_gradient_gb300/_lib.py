@@ -30,7 +30,7 @@ EXPORTS = [
     "psgd_step", "psgd_step_host",
     "psgd_step_status", "psgd_get_stats", "psgd_tensor_info", "psgd_error_numel", "psgd_set_q",
     "psgd_get_q", "psgd_get_p", "psgd_get_error", "psgd_set_error", "psgd_workspace_bytes",
-    "psgd_profile", "psgd_profile_select", "psgd_profile_kinds", "psgd_profile_read", "psgd_last_error",
+    "psgd_set_error_store_halves", "psgd_profile", "psgd_profile_select", "psgd_profile_kinds", "psgd_profile_read", "psgd_last_error",
     "psgd_project_q_static",
     "psgd_group_create", "psgd_group_destroy", "psgd_group_step", "psgd_group_wait",
     "psgd_group_status", "psgd_group_bucket", "psgd_group_size", "psgd_set_graph", "psgd_graph_stats",
@@ -96,6 +96,8 @@ def lib():
     L.psgd_workspace_bytes.restype = ctypes.c_size_t
     L.psgd_profile.argtypes = [P, c_i32]
     L.psgd_profile.restype = ctypes.c_int
+    L.psgd_set_error_store_halves.argtypes = [P, c_i32]
+    L.psgd_set_error_store_halves.restype = ctypes.c_int
     L.psgd_profile_select.argtypes = [P, ctypes.c_uint32]
     L.psgd_profile_select.restype = ctypes.c_int
     L.psgd_profile_kinds.argtypes = []

@@ -178,6 +178,7 @@ struct psgd_state {
   Segment* d_unc = nullptr;
   Segment* d_all = nullptr;
   float* estore = nullptr;
+  int est_halves = 2;       // error-store halves (1: psgd_set_error_store_halves)
   float* mbar = nullptr;
   float* Pf = nullptr;
   float* Qf = nullptr;
@@ -681,6 +682,7 @@ StepArgs make_args(psgd_state* s) {
   a.invW = 1.f / (float)s->W;
   a.estore = s->estore;
   a.nc_pad = s->Nc_pad;
+  a.est_half = s->est_halves == 2 ? (long long)s->W * s->Nc_pad : 0;
   a.mbar = (s->pass2_src == 0) ? s->mbar : nullptr;
   a.Pf = s->Pf;
   a.Qf = s->Qf;
@@ -1846,6 +1848,36 @@ int psgd_set_error(psgd_state* s, int32_t replica, const float* dev_in, void* st
 }
 
 size_t psgd_workspace_bytes(const psgd_state* s) { return s ? s->bytes : 0; }
+
+int psgd_set_error_store_halves(psgd_state* s, int32_t halves) {
+  if (!s) return fail(PSGD_EINVAL, "state is NULL");
+  if (halves != 1 && halves != 2) return fail(PSGD_EINVAL, "halves must be 1 or 2");
+  if (s->dp_world) return fail(PSGD_EINVAL, "a data-parallel state keeps two halves");
+  if (s->iter != 0) return fail(PSGD_EINVAL, "the error store's halves are set before the first step");
+  if (halves == s->est_halves || !s->ef || !s->estore) {
+    if (s->ef && s->estore) s->est_halves = halves;
+    return PSGD_OK;
+  }
+  DeviceGuard g(s->device);
+  PSGD_CUDA_TRY(cudaDeviceSynchronize());
+  const size_t half = (size_t)s->W * s->Nc_pad * sizeof(float);
+  float* fresh = nullptr;
+  int rc = dalloc(s, (void**)&fresh, (size_t)halves * half);
+  if (rc) return rc;
+  PSGD_CUDA_TRY(cudaMemset(fresh, 0, (size_t)halves * half));
+  // the old store leaves the allocation list and the byte count
+  for (size_t i = 0; i < s->allocs.size(); ++i)
+    if (s->allocs[i] == (void*)s->estore) {
+      cudaFree(s->allocs[i]);
+      s->allocs.erase(s->allocs.begin() + (long)i);
+      s->bytes -= (size_t)s->est_halves * half;
+      break;
+    }
+  s->estore = fresh;
+  s->est_halves = halves;
+  drop_graph(s);
+  return PSGD_OK;
+}
 
 int psgd_profile(psgd_state* s, int32_t enable) {
   if (!s) return fail(PSGD_EINVAL, "state is NULL");

@@ -39,8 +39,10 @@ struct StepArgs {
   float scale;        // inverse loss scale
   float invW;
   float* out;
-  float* estore;      // error store: half b, replica w at (b * W + w) * nc_pad
+  float* estore;      // error store: half b, replica w at b * est_half + w * nc_pad
   long long nc_pad;
+  long long est_half; // offset of the store's second half: W * nc_pad, or 0 for a
+                      // one-half store (both halves the same memory)
   float* mbar;        // replica-mean scratch or nullptr
   float* Pf;          // committed P, half b at b * p_total
   float* Qf;          // committed Q, half b at b * q_total
@@ -382,8 +384,8 @@ __device__ __forceinline__ void pass1_tile(const StepArgs& a, const TensorDesc& 
 #pragma unroll(WT > 0 ? WT : 1)
       for (int w = 0; w < W; ++w) {
         const GT* g = reinterpret_cast<const GT*>(a.grads.p[w]);
-        float* ecur = a.estore + ((long long)cur * a.W + w) * a.nc_pad + td.c_off;
-        float* enxt = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off;
+        float* ecur = a.estore + (long long)cur * a.est_half + (long long)w * a.nc_pad + td.c_off;
+        float* enxt = a.estore + (long long)nxt * a.est_half + (long long)w * a.nc_pad + td.c_off;
 #pragma unroll
         for (int q = 0; q < RW; ++q) {
           if (!rv[q]) continue;
@@ -580,7 +582,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
     // per-row products.  go / eo: bucket and store offsets of the unit issued.
     const long long gstep = (long long)wpc * m, estep = (long long)wpc * ld;
     const long long row_first = (long long)item.row0 + phase;
-    const long long ecur = (long long)cur * a.W * a.nc_pad;
+    const long long ecur = (long long)cur * a.est_half;
     auto issue = [&](char* slot, long long go, long long eo) {
       if constexpr (!SH) {
         if (cin) {
@@ -737,7 +739,7 @@ __device__ __forceinline__ void pass1_tile_cs(const StepArgs& a, const TensorDes
           f2unpack(c23, corr[2], corr[3]);
         }
         float mb[4] = {0.f, 0.f, 0.f, 0.f};
-        float* enxt = a.estore + (long long)nxt * a.W * a.nc_pad + r_off;
+        float* enxt = a.estore + (long long)nxt * a.est_half + r_off;
         // SH: columns taken from the bucket (the tile's and the bucket's ends)
         const long long lim = SH ? td.valid - g_pos : 4;
         const int nvg = lim >= ncv ? ncv : (lim > 0 ? (int)lim : 0);
@@ -918,7 +920,7 @@ __device__ __forceinline__ void load_mbar(const StepArgs& a, const TensorDesc& t
     for (int w = 0; w < W; ++w) {
       float v[NC];
       if constexpr (SRC == 1) {
-        const float* src = a.estore + ((long long)nxt * a.W + w) * a.nc_pad + td.c_off + row * ld + c0;
+        const float* src = a.estore + (long long)nxt * a.est_half + (long long)w * a.nc_pad + td.c_off + row * ld + c0;
         if constexpr (VEC) {
           load_f<4>(src, v, true);
         } else {
@@ -1162,7 +1164,7 @@ __global__ void __launch_bounds__(kThreads) k_pass3(const StepArgs a) {
   const float* P = a.Pf + (long long)half * a.p_total;
   const float* Q = a.Qf + (long long)half * a.q_total;
   float* store = nullptr;
-  if (MODE != 0) store = a.estore + ((long long)a.ctrl->cur * a.W + a.replica) * a.nc_pad;
+  if (MODE != 0) store = a.estore + (long long)a.ctrl->cur * a.est_half + (long long)a.replica * a.nc_pad;
   constexpr int CPT = cpt3_for(RP);
   for (int it = blockIdx.x; it < a.n_fitems; it += gridDim.x) {
     const Item item = a.fitems[it];

@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(416, 1) k_pass2_tc(const StepArgs a, int src_m
   const uint32_t tmem = tslot;
   const int nxt = a.ctrl->cur ^ 1;
   // source row i of an item's tensor: the Mbar scratch, or replica w's store (next half)
-  const float* src0 = (src_mode == 0) ? a.mbar : a.estore + (long long)nxt * a.W * a.nc_pad;
+  const float* src0 = (src_mode == 0) ? a.mbar : a.estore + (long long)nxt * a.est_half;
 
   if (warp < 8) {
     // ---------------- workers
@@ -951,7 +951,7 @@ __global__ void __launch_bounds__(416, 1) k_pass1_tc(const StepArgs a) {
             cp_async8_z(gdst + rr * T::GROW + p4 * 8, src, ok);
         }
         if (ef) {
-          const float* e = a.estore + ((long long)cur * W + l_w) * a.nc_pad + l_it.c_off;
+          const float* e = a.estore + (long long)cur * a.est_half + (long long)l_w * a.nc_pad + l_it.c_off;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int rr = j * 8 + lane / 4, p16 = lane % 4;
@@ -1048,7 +1048,7 @@ __global__ void __launch_bounds__(416, 1) k_pass1_tc(const StepArgs a) {
               *reinterpret_cast<float4*>(ep + lane * T::EROW + 16 * j) =
                   make_float4(mv[4 * j], mv[4 * j + 1], mv[4 * j + 2], mv[4 * j + 3]);
             __syncwarp();
-            float* en = a.estore + ((long long)nxt * W + w) * a.nc_pad + it.c_off;
+            float* en = a.estore + (long long)nxt * a.est_half + (long long)w * a.nc_pad + it.c_off;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int rr = j * 8 + lane / 4, p16 = lane % 4;

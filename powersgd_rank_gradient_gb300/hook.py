@@ -141,6 +141,12 @@ class PowerSGDState:
     def workspace_bytes(self):
         return int(self._lib.psgd_workspace_bytes(self._h))
 
+    def set_error_store_halves(self, halves):
+        """psgd_set_error_store_halves: 1 keeps the error-feedback store once
+        (the pages' memory; a skipped inf/NaN step then leaves the error
+        feedback changed), 2 (default) twice.  Before the first step."""
+        check(self._lib.psgd_set_error_store_halves(self._h, int(halves)))
+
     def set_q(self, t, q, is_draw=True):
         q = torch.as_tensor(q, dtype=torch.float32).contiguous().cpu()
         check(self._lib.psgd_set_q(self._h, int(t), ctypes.c_void_p(q.data_ptr()), int(is_draw)))

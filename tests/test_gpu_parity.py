@@ -650,3 +650,34 @@ def test_bounded_wait_timeout_leaves_state_unchanged(rank):
             assert torch.equal(x, y)
     a.close()
     b.close()
+
+
+@pytest.mark.parametrize("rank,world,which", [(4, 2, "mixed"), (4, 8, "mixed"), (3, 9, "mixed"),
+                                              (16, 2, "aligned"), (32, 3, "aligned")])
+def test_one_half_error_store_same_bits(rank, world, which):
+    """psgd_set_error_store_halves(1): the error store kept once, pass 1
+    writing M_w over the residual it has just read (chunk-stationary,
+    tensor-core and element paths; the M-bar scratch at W >= 3) gives the same
+    bits as the two-half store, every step, with one half less memory; the
+    call is refused once a step was taken."""
+    from powersgd_rank_gradient_gb300 import PowerSGDState, _lib
+
+    shapes = MIXED if which == "mixed" else ALIGNED
+    kw = dict(matrix_approximation_rank=rank, start_powerSGD_iter=0,
+              min_compression_rate=1.0 if which == "mixed" else 0.25, device=DEV)
+    one, two = PowerSGDState(shapes, world, **kw), PowerSGDState(shapes, world, **kw)
+    before = one.workspace_bytes()
+    one.set_error_store_halves(1)
+    assert 0 < one.workspace_bytes() < before
+    for k in range(3):
+        g = [torch.from_numpy(x).to(DEV) for x in grads_for(shapes, world, k)]
+        o1 = one.step(g).clone()
+        o2 = two.step(g).clone()
+        assert not one.status() and not two.status()
+        assert torch.equal(o1, o2), k
+    for w in range(world):
+        assert torch.equal(one.get_error(w), two.get_error(w))
+    with pytest.raises(_lib.PsgdError):
+        one.set_error_store_halves(2)
+    one.close()
+    two.close()
