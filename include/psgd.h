@@ -30,6 +30,9 @@
  *     the call (psgd_step: past the enqueued work).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  psgd_step enqueues only and never synchronises.
+ *   - Host threads: calls on one state (or one group) must not overlap in
+ *     time; different states may be driven from different threads at once
+ *     (the library's process-wide launch settings are atomic or locked).
  *   - Elements of a bucket are in bucket order: tensor 0 first, each tensor
  *     row-major in its own shape, with no padding between tensors.
  */

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 
 #include "psgd_gs.cuh"
 #include "psgd_kernels.cuh"
@@ -26,13 +27,17 @@ inline void by_gtype(int gtype, F&& f) {
 // cudaFuncSetAttribute applies to the current device's context: a launcher
 // that raises a kernel's shared-memory limit does so once per device.  `done`
 // holds one bit per device ordinal (the library handles ordinals below 64).
-inline bool first_on_device(unsigned long long& done) {
+// States on other host threads share it: the bit is published only after
+// `setup` has run, so no thread launches before the limit is raised (threads
+// that race on a fresh device each run `setup`, which is idempotent).
+template <typename F>
+inline void once_per_device(std::atomic<unsigned long long>& done, F&& setup) {
   int dev = 0;
   cudaGetDevice(&dev);
   const unsigned long long bit = 1ull << (dev & 63);
-  if (done & bit) return false;
-  done |= bit;
-  return true;
+  if (done.load(std::memory_order_acquire) & bit) return;
+  setup();
+  done.fetch_or(bit, std::memory_order_release);
 }
 
 template <int RP, typename GT>
@@ -40,10 +45,10 @@ void launch_pass1_mma(const StepArgs& a, int grid, cudaStream_t s) {
   // the aligned, wholly backed items on the tensor cores (tcgen05), the rest
   // on the element kernel
   using T = Pass1Tc<RP, GT>;
-  static unsigned long long configured = 0;
-  if (first_on_device(configured)) {
+  static std::atomic<unsigned long long> configured{0};
+  once_per_device(configured, [] {
     cudaFuncSetAttribute(k_pass1_tc<RP, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-  }
+  });
   if (a.vec_ok && a.n_t1 > 0) k_pass1_tc<RP, GT><<<std::min(grid, a.n_t1), T::THREADS, T::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned) k_pass1_rest<RP, GT><<<grid * 2, kThreads, 0, s>>>(a);
 }
@@ -53,13 +58,13 @@ template <int RP, int WT, typename GT, int MINB, bool PW = false>
 void launch_pass1_cs(const StepArgs& a, int grid, cudaStream_t s) {
   using St0 = Pass1CS<RP, WT, GT, MINB, false>;
   using St1 = Pass1CS<RP, WT, GT, MINB, true>;
-  static unsigned long long configured = 0;
-  if (first_on_device(configured)) {
+  static std::atomic<unsigned long long> configured{0};
+  once_per_device(configured, [] {
     cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 0, PW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          St0::SMEM);
     cudaFuncSetAttribute(k_pass1_cs<RP, WT, GT, MINB, 1, PW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          St1::SMEM);
-  }
+  });
   if (a.vec_ok && a.has_aligned) k_pass1_cs<RP, WT, GT, MINB, 0, PW><<<grid * MINB, kThreads, St0::SMEM, s>>>(a);
   if (!a.vec_ok || a.has_unaligned)
     k_pass1_cs<RP, WT, GT, MINB, 1, PW><<<grid * MINB, kThreads, a.vec_ok ? St1::SMEM : 0, s>>>(a);
@@ -138,15 +143,18 @@ template <int RP>
 cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out, int is_q, int from_parts,
                            float* mid, float* dst, int dst_half, int do_psum, unsigned int* bar, int img,
                            int grid, cudaStream_t s, unsigned int skew) {
-  static int fits[64];   // CTAs resident at once, per device ordinal (0: not known yet)
+  // CTAs resident at once, per device ordinal (0: not known yet, or none fit;
+  // threads that race on a fresh device each compute the same value)
+  static std::atomic<int> fits[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  int& fit = fits[dev & 63];
+  int fit = fits[dev & 63].load(std::memory_order_relaxed);
   if (fit <= 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gs_coop<RP>, kThreads, 0);
     fit = std::max(0, per_sm * sms);
+    fits[dev & 63].store(fit, std::memory_order_relaxed);
   }
   if (fit == 0) return cudaErrorCooperativeLaunchTooLarge;
   grid = std::max(1, std::min(grid, fit));
@@ -160,10 +168,10 @@ cudaError_t launch_gs_coop(const StepArgs& a, const float* src, float* dense_out
 template <int RP, int NSRC>
 void launch_pass2_tc(const StepArgs& a, int src_mode, cudaStream_t s) {
   using T = Pass2Tc<RP, NSRC>;
-  static unsigned long long configured = 0;
-  if (first_on_device(configured)) {
+  static std::atomic<unsigned long long> configured{0};
+  once_per_device(configured, [] {
     cudaFuncSetAttribute(k_pass2_tc<RP, NSRC>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-  }
+  });
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -223,10 +231,10 @@ void launch_pass3(const StepArgs& a, int mode, int grid, cudaStream_t s) {
     // fp32 kernel below skips them and takes the rest
     if (mode == 0 && a.vec_ok && a.n_t3 > 0) {
       using T = Pass3Tc<RP>;
-      static unsigned long long configured = 0;
-      if (first_on_device(configured)) {
+      static std::atomic<unsigned long long> configured{0};
+      once_per_device(configured, [] {
         cudaFuncSetAttribute(k_pass3_tc<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-      }
+      });
       int dev = 0, sms = 148;
       cudaGetDevice(&dev);
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
