@@ -365,9 +365,9 @@ void build_plan(psgd_state* s) {
   // every compressed tensor has one shape the items are alike and the waves
   // can be counted: the row block (a multiple of 64) with the shortest
   // round-robin makespan, each item also paying its Q partial and its setup
-  // (8192 x 8192: 192 rows at ranks <= 8, 512 at rank 32, measured best; the
-  // count is used for the two kernels it was checked on, the four-column
-  // fp32 kernel of ranks <= 8 and the tensor-core kernel of rank 32)
+  // (8192 x 8192: 192 rows at ranks <= 8, 320 at rank 16, 512 at rank 32,
+  // each measured best for its kernel: the fp32 kernel at four and two
+  // columns a thread, the tensor-core kernel of rank 32)
   {
     long long nc = 0;
     bool alike = true;
@@ -384,7 +384,7 @@ void build_plan(psgd_state* s) {
     const long long target = (long long)s->sms * 3 * 4;
     int rb = kRowBlock;
     while (rb > 64 && nc / ((long long)rb * CT) < target) rb >>= 1;
-    if (alike && n0 > 0 && (RP <= 8 || RP == 32)) {
+    if (alike && n0 > 0) {
       const bool tc2 = RP == 32;   // 128-column items, one CTA per SM
       const int ctw = tc2 ? 128 : CT;
       const double bpe = s->pass2_src == 0 ? 4.0 : (s->pass2_src == 1 ? 4.0 * s->W
